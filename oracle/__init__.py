@@ -1,0 +1,221 @@
+"""CPU oracle for the q4_K x q8_0 decode matvec -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library never does, and this
+package imports nothing from it.  The arithmetic lives in ``mq_oracle.c``
+(plain C, binary64 accumulation); this module is argument marshalling over
+ctypes with numpy arrays.
+
+Formats (a reading of the pages, which name q4_K/q8_0 but do not print them):
+q4_K super-block of 256 weights in 144 bytes, q8_0 block of 32 values in 34
+bytes; see ``mq_oracle.c`` for the byte layout.
+
+Pinned by tests/test_oracle_*.py.  Nothing here is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import numpy as np
+
+from . import build as _build
+
+QK_K = 256
+Q4K_BYTES = 144
+QK8 = 32
+Q8_BYTES = 34
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        f32p = ctypes.POINTER(ctypes.c_float)
+        f64p = ctypes.POINTER(ctypes.c_double)
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        i64p = ctypes.POINTER(ctypes.c_int64)
+        i64 = ctypes.c_int64
+        lib.mqo_f16_to_f32.argtypes = [ctypes.c_uint16]
+        lib.mqo_f16_to_f32.restype = ctypes.c_float
+        lib.mqo_f32_to_f16.argtypes = [ctypes.c_float]
+        lib.mqo_f32_to_f16.restype = ctypes.c_uint16
+        lib.mqo_quantize_q8_0.argtypes = [f32p, i64, u8p]
+        lib.mqo_unpack_q4K.argtypes = [u8p, f64p, f64p, i32p, i32p, i32p]
+        lib.mqo_dequant_q4K_row.argtypes = [u8p, i64, f64p]
+        lib.mqo_dequant_q8_0.argtypes = [u8p, i64, f64p]
+        lib.mqo_block_sums.argtypes = [u8p, u8p, i64, i64, i32p, i32p]
+        lib.mqo_matvec.argtypes = [u8p, u8p, i64, i64, i64, f64p, f64p]
+        lib.mqo_matvec_rows.argtypes = [u8p, u8p, i64, i64, i64p, i64, f64p, f64p]
+        lib.mqo_silu.argtypes = [ctypes.c_double]
+        lib.mqo_silu.restype = ctypes.c_double
+        lib.mqo_silu_mul.argtypes = [f64p, f64p, i64, f64p]
+        lib.mqo_ffn.argtypes = [u8p, u8p, f32p, i64, i64, i64, u8p, f64p, f64p, f32p, u8p, f64p]
+        for name in ("mqo_quantize_q8_0", "mqo_unpack_q4K", "mqo_dequant_q4K_row", "mqo_dequant_q8_0",
+                     "mqo_block_sums", "mqo_matvec", "mqo_matvec_rows", "mqo_silu_mul", "mqo_ffn"):
+            getattr(lib, name).restype = None
+        _lib = lib
+    return _lib
+
+
+def _p(a: np.ndarray, ct):
+    return a.ctypes.data_as(ctypes.POINTER(ct))
+
+
+def _u8(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.uint8)
+
+
+def f16_to_f32(bits: int) -> float:
+    return float(_load().mqo_f16_to_f32(int(bits)))
+
+
+def f32_to_f16(x: float) -> int:
+    return int(_load().mqo_f32_to_f16(float(np.float32(x))))
+
+
+def q4K_row_bytes(K: int) -> int:
+    return K // QK_K * Q4K_BYTES
+
+
+def q8_0_bytes(K: int) -> int:
+    return K // QK8 * Q8_BYTES
+
+
+def quantize_q8_0(x: np.ndarray) -> np.ndarray:
+    """fp32 [ncols, K] (or [K]) -> uint8 [ncols, K/32*34] q8_0 blocks."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    x2 = x.reshape(-1, x.shape[-1])
+    K = x2.shape[1]
+    if K % QK8:
+        raise ValueError("K must be a multiple of 32")
+    out = np.empty((x2.shape[0], q8_0_bytes(K)), dtype=np.uint8)
+    lib = _load()
+    for c in range(x2.shape[0]):
+        row = np.ascontiguousarray(x2[c])
+        o = out[c]
+        lib.mqo_quantize_q8_0(_p(row, ctypes.c_float), K, _p(o, ctypes.c_uint8))
+    return out if x.ndim > 1 else out[0]
+
+
+def unpack_q4K(block: np.ndarray) -> Tuple[float, float, np.ndarray, np.ndarray, np.ndarray]:
+    """One 144-byte super-block -> (d, dmin, sc[8], m[8], q[256])."""
+    b = _u8(block)
+    if b.size != Q4K_BYTES:
+        raise ValueError("a q4_K super-block is 144 bytes")
+    d = ctypes.c_double()
+    dm = ctypes.c_double()
+    sc = np.zeros(8, np.int32)
+    m = np.zeros(8, np.int32)
+    q = np.zeros(256, np.int32)
+    _load().mqo_unpack_q4K(_p(b, ctypes.c_uint8), ctypes.byref(d), ctypes.byref(dm),
+                           _p(sc, ctypes.c_int32), _p(m, ctypes.c_int32), _p(q, ctypes.c_int32))
+    return d.value, dm.value, sc, m, q
+
+
+def dequant_q4K(W: np.ndarray, K: int) -> np.ndarray:
+    """uint8 [rows, K/256*144] -> float64 [rows, K]."""
+    W = _u8(W).reshape(-1, q4K_row_bytes(K))
+    out = np.empty((W.shape[0], K), dtype=np.float64)
+    lib = _load()
+    for r in range(W.shape[0]):
+        row = np.ascontiguousarray(W[r])
+        o = out[r]
+        lib.mqo_dequant_q4K_row(_p(row, ctypes.c_uint8), K, _p(o, ctypes.c_double))
+    return out
+
+
+def dequant_q8_0(xq: np.ndarray, K: int) -> np.ndarray:
+    xq = _u8(xq).reshape(-1, q8_0_bytes(K))
+    out = np.empty((xq.shape[0], K), dtype=np.float64)
+    lib = _load()
+    for c in range(xq.shape[0]):
+        row = np.ascontiguousarray(xq[c])
+        o = out[c]
+        lib.mqo_dequant_q8_0(_p(row, ctypes.c_uint8), K, _p(o, ctypes.c_double))
+    return out
+
+
+def block_sums(W: np.ndarray, xq: np.ndarray, rows: int, K: int) -> Tuple[np.ndarray, np.ndarray]:
+    """Per-32-block int32 sums: sumi [ncols, rows, K/32], sumq [ncols, K/32]."""
+    W = _u8(W)
+    xq = _u8(xq).reshape(-1, q8_0_bytes(K))
+    nc = xq.shape[0]
+    nq = K // QK8
+    sumi = np.empty((nc, rows, nq), np.int32)
+    sumq = np.empty((nc, nq), np.int32)
+    lib = _load()
+    for c in range(nc):
+        col = np.ascontiguousarray(xq[c])
+        si = sumi[c]
+        sq = sumq[c]
+        lib.mqo_block_sums(_p(W, ctypes.c_uint8), _p(col, ctypes.c_uint8), rows, K,
+                           _p(si, ctypes.c_int32), _p(sq, ctypes.c_int32))
+    return sumi, sumq
+
+
+def matvec(W: np.ndarray, xq: np.ndarray, rows: int, K: int,
+           row_ids: Optional[np.ndarray] = None) -> Tuple[np.ndarray, np.ndarray]:
+    """y, T as float64 [ncols, rows] (or [ncols, len(row_ids)]).
+
+    T[c, r] is the sum of the magnitudes of the per-block products, the
+    scale of the float tolerance |y - y_ref| <= 1e-3 * T + 1e-5.
+    """
+    W = _u8(W)
+    xq = _u8(xq).reshape(-1, q8_0_bytes(K))
+    nc = xq.shape[0]
+    lib = _load()
+    if row_ids is None:
+        y = np.empty((nc, rows), np.float64)
+        T = np.empty((nc, rows), np.float64)
+        lib.mqo_matvec(_p(W, ctypes.c_uint8), _p(xq, ctypes.c_uint8), rows, K, nc,
+                       _p(y, ctypes.c_double), _p(T, ctypes.c_double))
+    else:
+        ids = np.ascontiguousarray(row_ids, dtype=np.int64)
+        if ids.size and (ids.min() < 0 or ids.max() >= rows):
+            raise IndexError("row id out of range")
+        y = np.empty((nc, ids.size), np.float64)
+        T = np.empty((nc, ids.size), np.float64)
+        lib.mqo_matvec_rows(_p(W, ctypes.c_uint8), _p(xq, ctypes.c_uint8), K, nc,
+                            _p(ids, ctypes.c_int64), ids.size, _p(y, ctypes.c_double), _p(T, ctypes.c_double))
+    return y, T
+
+
+def silu(g: float) -> float:
+    return float(_load().mqo_silu(float(g)))
+
+
+def silu_mul(g: np.ndarray, u: np.ndarray) -> np.ndarray:
+    g = np.ascontiguousarray(g, dtype=np.float64)
+    u = np.ascontiguousarray(u, dtype=np.float64)
+    if g.shape != u.shape:
+        raise ValueError("g and u must have the same shape")
+    h = np.empty_like(g)
+    _load().mqo_silu_mul(_p(g, ctypes.c_double), _p(u, ctypes.c_double), g.size, _p(h, ctypes.c_double))
+    return h
+
+
+def ffn(W_gu: np.ndarray, W_down: np.ndarray, x: np.ndarray, H: int, I: int) -> Tuple[np.ndarray, np.ndarray]:
+    """Whole FFN chain: (y float64 [ncols, H], hq uint8 [ncols, I/32*34])."""
+    x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1, H)
+    nc = x.shape[0]
+    xq = np.empty(q8_0_bytes(H), np.uint8)
+    gu = np.empty(2 * I, np.float64)
+    h = np.empty(I, np.float64)
+    hf = np.empty(I, np.float32)
+    hq = np.empty((nc, q8_0_bytes(I)), np.uint8)
+    y = np.empty((nc, H), np.float64)
+    _load().mqo_ffn(_p(_u8(W_gu), ctypes.c_uint8), _p(_u8(W_down), ctypes.c_uint8), _p(x, ctypes.c_float),
+                    H, I, nc, _p(xq, ctypes.c_uint8), _p(gu, ctypes.c_double), _p(h, ctypes.c_double),
+                    _p(hf, ctypes.c_float), _p(hq, ctypes.c_uint8), _p(y, ctypes.c_double))
+    return y, hq
+
+
+def within_tolerance(y: np.ndarray, y_ref: np.ndarray, T: np.ndarray) -> np.ndarray:
+    """|y - y_ref| <= 1e-3 * T + 1e-5, elementwise."""
+    return np.abs(np.asarray(y, np.float64) - y_ref) <= 1e-3 * T + 1e-5

@@ -1,0 +1,33 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
+    config.addinivalue_line("markers", "slow: long-running test")
+
+
+@pytest.fixture(scope="session")
+def mq_lib():
+    """The C-ABI library, built in-tree if missing or stale."""
+    from quantized_decode_matvec_gb300 import build as mqbuild
+    mqbuild.build()
+    from quantized_decode_matvec_gb300 import _binding
+    return _binding
+
+
+@pytest.fixture(scope="session")
+def cuda_ready(mq_lib):
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.init()
+    st = mq_lib.mq_init(torch.cuda.current_device())
+    assert st == 0, mq_lib.status_string(st)
+    return mq_lib
