@@ -1,0 +1,448 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 q4_K x q8_0 decode matvec.
+
+Default workload: the 7B-class whole decode step of matvecs -- 28 layers, per
+layer q|k|v [4608 x 3584], o [3584 x 3584], ffn_gu [37888 x 3584] with fused
+SiLU*mul and q8_0 of h, down [3584 x 18944]; batch 1; 3,670,474,752 bytes of
+q4_K weights per step -- captured once as a CUDA graph and replayed.  One step
+= one replay (every kernel of all 28 layers).  Weights are synthetic (seeded
+generator), inputs are fp32 N(0,1) with 0.1% x20 outliers.
+
+Prints ONE JSON line (rank 0): value = weight GB/s of the step (whole job,
+all ranks), ms_per_step, the dominant kernel's roofline, the oracle's CPU
+baseline, an end-to-end number through host buffers, clocks seen during the
+timed region.  ``--impl reference`` times the CPU oracle instead (the
+reference arm: there is no other implementation to run).
+
+Multi-GPU: the step does not shard here (one GPU per box); N ranks run N
+independent replicas (weak scaling), value = all ranks' bytes / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "q4_K×q8_0 decode matvec weight GB/s vs HBM peak; 7B-class step µs (1 GPU)"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+
+
+# ---------------------------------------------------------------------------------------------------------
+# multi-rank plumbing (torchrun): barrier, max of times, sum of work
+# ---------------------------------------------------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_over_ranks(ms_local: float, units_local: float, device=None):
+    """(max over ranks of ms, sum over ranks of units); identity without a process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms_local, units_local
+    t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+    u = torch.tensor([units_local], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="mq_clocks_", suffix=".csv")
+            self.fh = os.fdopen(fd, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------------------------
+# workload
+# ---------------------------------------------------------------------------------------------------------
+
+def measured_hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "quantized_decode_matvec_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(profile_name: str):
+    """DRAM bytes per launch recorded from an ncu capture, if taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", profile_name)
+    try:
+        fields = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and line.strip().startswith("- "):
+                    k, v = line.strip()[2:].split(":", 1)
+                    fields[k.strip()] = v.strip().strip("`")
+        if fields.get("kernel_source_sha") == kernel_source_sha():
+            return float(fields["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+def build_step(case, device, mq):
+    """Upload the step's weights (q|k|v concatenated on the device with mq_concat_rows)."""
+    import torch
+    from quantized_decode_matvec_gb300 import synth
+    stream = torch.cuda.current_stream().cuda_stream
+    layers = []
+    for l in range(case.n_layers):
+        w = synth.step_layer_weights(case, l)
+        q, k, v = (torch.from_numpy(w[n]).to(device) for n in ("q", "k", "v"))
+        qkv = torch.empty((case.qkv_rows, q.shape[1]), dtype=torch.uint8, device=device)
+        st = mq.mq_concat_rows(qkv.data_ptr(), [q.data_ptr(), k.data_ptr(), v.data_ptr()],
+                               [case.q_rows, case.kv_rows, case.kv_rows], mq.MQ_TYPE_Q4_K, case.H, stream)
+        mq._check(st, "mq_concat_rows")
+        layers.append({"qkv": qkv, "o": torch.from_numpy(w["o"]).to(device),
+                       "gu": torch.from_numpy(w["gu"]).to(device), "down": torch.from_numpy(w["down"]).to(device)})
+        del q, k, v
+    torch.cuda.synchronize()
+    return layers
+
+
+def fill_inputs(bufs, case, replay):
+    import torch
+    from quantized_decode_matvec_gb300 import synth
+    for l in range(case.n_layers):
+        inp = synth.step_layer_inputs(case, l, replay)
+        bufs.a[l].copy_(torch.from_numpy(inp["a"]))
+        bufs.b[l].copy_(torch.from_numpy(inp["b"]))
+        bufs.c[l].copy_(torch.from_numpy(inp["c"]))
+
+
+def time_replays(run, stream, steps):
+    """Per-step device times (ms) of `steps` runs, CUDA events on the launching stream."""
+    import torch
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    evs[0].record(stream)
+    for i in range(steps):
+        run()
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    return [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
+
+
+def sem(v):
+    return statistics.stdev(v) / len(v) ** 0.5 if len(v) > 1 else 0.0
+
+
+# ---------------------------------------------------------------------------------------------------------
+# CPU oracle baseline (test infrastructure, timed as it stands)
+# ---------------------------------------------------------------------------------------------------------
+
+def oracle_step_layers(case, layers, replay=0, budget_s=None, layer_ids=None):
+    """Run the oracle over layers of the step; returns (weight bytes processed, seconds, layers done)."""
+    import oracle
+    from quantized_decode_matvec_gb300 import synth
+    done, nbytes, spent = 0, 0, 0.0
+    ids = layer_ids if layer_ids is not None else range(case.n_layers)
+    for l in ids:
+        w = layers(l)
+        inp = synth.step_layer_inputs(case, l, replay)
+        t0 = time.perf_counter()
+        qkv = np.concatenate([w["q"], w["k"], w["v"]])
+        oracle.matvec(qkv, oracle.quantize_q8_0(inp["a"]), case.qkv_rows, case.H)
+        oracle.matvec(w["o"], oracle.quantize_q8_0(inp["b"]), case.H, case.q_rows)
+        oracle.ffn(w["gu"], w["down"], inp["c"], case.H, case.I)
+        spent += time.perf_counter() - t0
+        nbytes += sum(w[n].nbytes for n in ("q", "k", "v", "o", "gu", "down"))
+        done += 1
+        if budget_s is not None and spent >= budget_s:
+            break
+    return nbytes, spent, done
+
+
+def cpu_baseline(case, budget_s=12.0):
+    from quantized_decode_matvec_gb300 import synth
+    cache = {}
+
+    def layers(l):
+        if l not in cache:
+            cache.clear()
+            cache[l] = synth.step_layer_weights(case, l)
+        return cache[l]
+
+    nbytes, spent, done = oracle_step_layers(case, layers, budget_s=budget_s)
+    return {"value": nbytes / spent / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{done} of {case.n_layers} layers of one step (q|k|v, o, ffn_gu+SiLU*mul+q8_0, down), "
+                      f"single-threaded C oracle, fp64 accumulation, {spent:.1f} s"}
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle as it stands, each step a bounded sample of the workload."""
+    from quantized_decode_matvec_gb300 import synth
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    case = synth.STEP_7B
+    n_cached = 2
+    cache = {l: synth.step_layer_weights(case, l) for l in range(n_cached)}
+    layers = lambda l: cache[l % n_cached]
+    for i in range(args.warmup):
+        oracle_step_layers(case, layers, layer_ids=[i % n_cached])
+    times, nbytes = [], 0
+    for i in range(args.steps):
+        b, s, _ = oracle_step_layers(case, layers, layer_ids=[i % n_cached])
+        times.append(s)
+        nbytes += b
+    total = sum(times)
+    value = nbytes / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": case.name, "sample_per_step": "one layer of the 28 (q|k|v, o, FFN chain)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle", "cores": 1,
+                         "sample": "one of 28 layers per step, single-threaded C oracle"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from quantized_decode_matvec_gb300 import build as mqbuild
+    mqbuild.build()
+    from quantized_decode_matvec_gb300 import mq, synth
+    from quantized_decode_matvec_gb300.graph import PinnedFeeder, StepGraph
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", torch.cuda.current_device())
+    mq.init(device.index)
+    case = synth.STEP_7B
+    wbytes = synth.weight_bytes_step(case)
+    per_layer = wbytes // case.n_layers
+
+    layers = build_step(case, device, mq)
+    bufs = mq.StepBuffers(layers, case.H, case.I, case.qkv_rows, case.H, case.q_rows, case.ncols)
+    fill_inputs(bufs, case, 0)
+    flags = mq.MQ_STEP_PDL if args.pdl else 0
+    g = StepGraph(bufs, flags=flags)
+    g_alt = StepGraph(bufs, flags=(0 if args.pdl else mq.MQ_STEP_PDL))
+    stream = g.stream
+
+    # warm-up (untimed)
+    for _ in range(args.warmup):
+        g.run()
+        g_alt.run()
+    torch.cuda.synchronize()
+
+    # ---- the timed region: K graph replays, inputs resident in HBM (3.67 GB >> L2: no flush needed)
+    clocks = ClockSampler(device.index)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    per_step = time_replays(g.run, stream, args.steps)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms_local = sum(per_step) / len(per_step)
+    ms, total_bytes = reduce_over_ranks(ms_local, float(wbytes), device if ws > 1 else None)
+    value = total_bytes / (ms / 1e3) / 1e9
+
+    # ---- interleaved arms (context): the other PDL setting, and eager launches
+    arms = {"graph": [], "graph_alt": [], "eager": []}
+    eager_run = lambda: bufs.step(stream, flags)
+    for _ in range(3):
+        arms["graph"] += time_replays(g.run, stream, 5)
+        arms["graph_alt"] += time_replays(g_alt.run, stream, 5)
+        with torch.cuda.stream(stream):
+            arms["eager"] += time_replays(eager_run, stream, 5)
+    arm_stats = {k: {"median_ms": statistics.median(v), "mean_ms": statistics.mean(v), "sem_ms": sem(v)}
+                 for k, v in arms.items()}
+
+    # ---- dominant kernel alone: ffn_gu + SiLU*mul + q8_0(h), over the 28 layers' weights
+    ffn_descs = [bufs.table[l * 192 + 112:l * 192 + 192] for l in range(case.n_layers)]
+    reps = 3
+
+    def gu_all():
+        for l in range(case.n_layers):
+            mq._check(mq.mq_ffn_gate_up(ffn_descs[l].data_ptr(), case.H, case.I, case.ncols, stream.cuda_stream),
+                      "mq_ffn_gate_up")
+
+    with torch.cuda.stream(stream):
+        gu_all()
+        t = time_replays(gu_all, stream, reps)
+    gu_ms = sum(t) / (reps * case.n_layers)
+    gu_bytes = (2 * case.I * (case.H // 256) * 144 + case.H * 4 * case.ncols
+                + case.I // 32 * 34 * case.ncols)
+    peak, peak_kind = measured_hbm_peak()
+    gu_gbs = gu_bytes / (gu_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": gu_gbs, "peak": peak, "unit": "GB/s", "frac": gu_gbs / peak,
+                "traffic": recorded_traffic("ffn_gate_up_7B.md"),
+                "kernel": "gu_kernel (ffn_gu matvec + SiLU*mul + q8_0 of h), 37888x3584",
+                "peak_kind": f"{peak_kind} (copy bandwidth)", "avg_launch_us": gu_ms * 1e3,
+                "algorithmic_bytes_per_launch": gu_bytes}
+
+    # ---- end to end through host buffers: pinned H2D of the inputs, replay, D2H of the outputs
+    feeder = PinnedFeeder(bufs)
+    outs = [bufs.y_qkv, bufs.y_o, bufs.y_ffn]
+    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+    inp = [synth.step_layer_inputs(case, l, 1) for l in range(case.n_layers)]
+    feeder.load(np.stack([i["a"] for i in inp]), np.stack([i["b"] for i in inp]), np.stack([i["c"] for i in inp]))
+
+    def e2e_step():
+        feeder.push(stream)
+        g.run()
+        with torch.cuda.stream(stream):
+            for h, o in zip(host_out, outs):
+                h.copy_(o, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    e2e_ms_local = (time.perf_counter() - t0) * 1e3 / args.steps
+    barrier()
+    e2e_ms, _ = reduce_over_ranks(e2e_ms_local, 0.0, device if ws > 1 else None)
+    e2e = {"value": total_bytes / (e2e_ms / 1e3) / 1e9, "unit": UNIT, "ms_per_step": e2e_ms,
+           "h2d_bytes_per_step": feeder.h2d_bytes, "d2h_bytes_per_step": d2h,
+           "api": "mq_step via a captured CUDA graph; pinned host inputs and outputs"}
+
+    cpu = cpu_baseline(case) if (rank == 0 and ws == 1 and not args.no_cpu_baseline) else None
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "step_us": ms * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+            "config": {
+                "workload": f"{case.name}: 28 layers x (q|k|v 4608x3584, o 3584x3584, ffn_gu 37888x3584 + "
+                            f"SiLU*mul + q8_0(h), down 3584x18944), batch 1, one CUDA graph replay per step",
+                "weight_bytes_per_step": wbytes, "weight_bytes_per_layer": per_layer,
+                "l2": "inputs larger than L2 (3.67 GB of weights per step vs 129 MB L2); no flush",
+                "parallelism": "replicas" if ws > 1 else "single GPU",
+                "pdl": bool(args.pdl),
+            },
+            "frac_of_measured_hbm": value / ws / peak, "frac_of_nominal_8TBs": value / ws / NOMINAL_HBM_GBS,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": 4 * case.n_layers * args.steps,
+            "clocks": clk,
+            "arms": arm_stats,
+            "graph_kernel_nodes": g.node_count(),
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--pdl", type=int, default=0, help="launch the step with programmatic dependent launch")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

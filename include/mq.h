@@ -1,0 +1,227 @@
+/*
+ * mq.h -- C ABI of libmq, the GB300 (sm_103a) q4_K x q8_0 decode matvec.
+ *
+ * What the library computes (pages: "07 . R3 -- Small-model per-token
+ * overhead" section 1 for MMVQ = dp4a x q8_0 on q4_K weights; "04 . 8o --
+ * Killing the CPU stall at decode start" sections 1, 3.1 and 3.2 for the
+ * concatenated gate/up weight ffn_gu and the row-concat preconditions;
+ * "Part 4 . Lecture 08 -- Graph-Resident Decode" sections 2-4 for shapes and
+ * pointers held in device memory, grid sizes as capture keys and lazy state
+ * pre-warmed before capture):
+ *
+ *   xq = q8_0(x)                          32-value blocks, f16 scale
+ *   y  = W . xq                           W rows of 256-weight q4_K super-blocks
+ *   h  = SiLU(W_gu[0:I] . xq) * (W_gu[I:2I] . xq);  y = W_down . q8_0(h)
+ *   step = for each layer: qkv, o, FFN, in that order, on one stream
+ *
+ * Formats (the pages name them; the bytes are the GGUF-compatible reading):
+ *   q4_K super-block, 256 weights, 144 bytes: [0:2] d f16, [2:4] dmin f16,
+ *     [4:16] eight 6-bit scale/min pairs, [16:144] 4-bit quants; weight =
+ *     d*sc*q - dmin*m.  A row of K weights is K/256 blocks, K % 256 == 0.
+ *   q8_0 block, 32 values, 34 bytes: [0:2] f16 scale d = amax/127 (fp32 IEEE
+ *     division, then round-to-nearest-even to f16), [2:34] int8
+ *     round_half_away(x/d).
+ *
+ * Layouts: matrices are row-major with dense rows (row stride = K/256*144
+ * bytes).  Multi-column activations are column-major by token: column c of an
+ * fp32 input is x[c*K .. c*K+K), of a q8_0 input the bytes
+ * [c*K/32*34, (c+1)*K/32*34); column c of an output is y[c*y_ld .. +rows).
+ *
+ * Ownership: the caller allocates and owns every buffer (weights, inputs,
+ * outputs, descriptors, the FFN's h_q8 scratch).  After mq_init the library
+ * allocates nothing, never synchronizes inside a compute call and never reads
+ * device memory from the host, so every compute call can be captured into a
+ * CUDA graph.  Weights must stay unchanged while a graph that reads them lives.
+ *
+ * Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ * stream).  Every compute call is asynchronous on that stream.
+ *
+ * Errors: each call returns an mq_status.  Host-side checks run before any
+ * launch; a call that fails them launches nothing.  A failed CUDA launch
+ * returns MQ_ERR_CUDA and mq_last_cuda_error() gives the cudaError_t.  Kernels
+ * re-check the device descriptor against the host-side shapes they were
+ * sized for; on a mismatch they write nothing and record the problem in the
+ * device status word (mq_read_device_status).  Nothing aborts, throws or exits.
+ */
+#ifndef MQ_H
+#define MQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MQ_ABI_VERSION 1
+
+typedef int mq_status;
+#define MQ_OK 0
+#define MQ_ERR_INVALID_ARG 1     /* null pointer, unknown type, bad count */
+#define MQ_ERR_SHAPE 2           /* K % 256 (q4_K) or K % 32 (q8_0), ncols outside 0..8, negative sizes */
+#define MQ_ERR_ALIGN 3           /* a pointer is not aligned as its layout requires */
+#define MQ_ERR_CUDA 4            /* a CUDA call failed; see mq_last_cuda_error */
+#define MQ_ERR_UNSUPPORTED 5     /* size beyond the library's limits (see MQ_MAX_*) */
+#define MQ_ERR_NOT_INITIALIZED 6 /* mq_init was not called for the current device */
+
+/* device status word bits (mq_read_device_status) */
+#define MQ_DEV_DESC_MISMATCH 1u  /* a kernel's device descriptor disagreed with its launch shape */
+#define MQ_DEV_DESC_ALIGN 2u     /* a device descriptor held a misaligned pointer */
+
+/* quantization types (mq_concat_rows*) */
+#define MQ_TYPE_Q4_K 1
+#define MQ_TYPE_Q8_0 2
+
+/* limits: K * ncols <= MQ_MAX_K_TIMES_NCOLS (the q8_0 activation is staged in
+ * shared memory), K <= MQ_MAX_K, ncols <= MQ_MAX_NCOLS */
+#define MQ_MAX_NCOLS 8
+#define MQ_MAX_K 131072
+#define MQ_MAX_K_TIMES_NCOLS 163840
+
+const char* mq_status_string(mq_status s);
+int mq_abi_version(void);
+/* cudaError_t of the last CUDA failure seen by this thread (0 if none) */
+int mq_last_cuda_error(void);
+
+/* Pre-warm everything a compute call would otherwise do lazily: device
+ * properties, shared-memory opt-ins of every kernel, the device status word.
+ * Call once per device, outside any stream capture, before other calls.
+ * Leaves the caller's current device unchanged. */
+mq_status mq_init(int device);
+
+/* Read the device status word of the current device and reset it to zero.
+ * Synchronizes `stream`; not for use inside a capture. */
+mq_status mq_read_device_status(uint32_t* bits, void* stream);
+
+/* ---- sizes (pure host) ---------------------------------------------------- */
+/* bytes of one q4_K row of K weights: K/256*144 (0 if K % 256 != 0) */
+size_t mq_q4K_row_bytes(int64_t K);
+/* bytes of one q8_0 column of K values: K/32*34 (0 if K % 32 != 0) */
+size_t mq_q8_0_bytes(int64_t K);
+/* elements and bytes per block of a type (0 for an unknown type) */
+int mq_quant_block_elems(int32_t ttype);
+int mq_quant_block_bytes(int32_t ttype);
+
+/* ---- row concatenation ("04 . 8o", section 3.2) ----------------------------
+ * Feasible iff n >= 2, every tensor has type ttype[0], the same ne0, ne0 is a
+ * multiple of the type's block size, and each tensor's byte length equals
+ * ne1 * (ne0/block_elems) * block_bytes.  Reads the metadata only.
+ * Returns 1 if feasible, 0 otherwise (also for null arrays). */
+int mq_concat_rows_feasible(int32_t n, const int32_t* ttype, const int64_t* ne0,
+                            const int64_t* ne1, const uint64_t* nbytes);
+/* dst = rows of srcs[0], then srcs[1], ...; device pointers; the same
+ * preconditions as mq_concat_rows_feasible (checked with nbytes computed from
+ * rows).  Device-to-device copies on `stream`.  Builds ffn_gu (gate rows then
+ * up rows) and the q|k|v projection. */
+mq_status mq_concat_rows(void* dst, const void* const* srcs, const int64_t* rows, int32_t n,
+                         int32_t ttype, int64_t ne0, void* stream);
+
+/* ---- q8_0 quantization -----------------------------------------------------
+ * x: fp32 [ncols][K] device, 4-byte aligned; xq: q8_0 [ncols][K/32] blocks,
+ * 2-byte aligned.  K % 32 == 0.  ncols == 0 or K == 0 launches nothing. */
+mq_status mq_quantize_q8_0(const float* x, void* xq, int64_t K, int32_t ncols, void* stream);
+
+/* ---- matvec ------------------------------------------------------------------
+ * Device-resident descriptor (caller-allocated, 8-byte aligned).  The kernel
+ * reads it at start, so a captured graph follows any change made to it
+ * between replays, as long as the shapes stay those the launch was sized for.
+ *   W      q4_K [rows][K/256] super-blocks, 16-byte aligned
+ *   x      fp32 [ncols][K], 4-byte aligned, or NULL; when set the kernel
+ *          quantizes it to q8_0 itself (bit-identical to mq_quantize_q8_0)
+ *   xq     q8_0 [ncols][K/32], 2-byte aligned; read when x == NULL
+ *   xq_out nullable; when x is set, the q8_0 of x is also written here
+ *   y      fp32 [ncols][y_ld], 4-byte aligned, y_ld >= rows
+ */
+typedef struct mq_mv_desc {
+    const void* W;
+    const float* x;
+    const void* xq;
+    void* xq_out;
+    float* y;
+    int32_t rows;
+    int32_t K;
+    int32_t ncols;
+    int32_t y_ld;
+} mq_mv_desc;
+
+/* host-side validation of a host copy of a descriptor (shapes, alignment, nulls) */
+mq_status mq_check_mv_desc(const mq_mv_desc* h_desc);
+/* y[c][r] = sum over K of W[r] . q8_0(x)[c], fp32 output.  rows, K, ncols are
+ * the host copies of the descriptor's shapes: they size the grid (the capture
+ * key) and must equal the device descriptor's.  rows == 0 or ncols == 0
+ * launches nothing; K must be a positive multiple of 256. */
+mq_status mq_matvec_q4K_q8_0(const mq_mv_desc* d_desc, int32_t rows, int32_t K, int32_t ncols,
+                             void* stream);
+
+/* ---- fused FFN -----------------------------------------------------------------
+ *   W_gu   q4_K [2I][H]: gate rows 0..I-1, then up rows I..2I-1 (ffn_gu)
+ *   W_down q4_K [H][I]
+ *   x      fp32 [ncols][H] or NULL (then xq q8_0 [ncols][H/32] is read)
+ *   h_q8   q8_0 [ncols][I/32]: scratch written by the gate/up kernel and read
+ *          by the down kernel (caller-owned, 2-byte aligned)
+ *   gu_dbg nullable fp32 [ncols][2I]: g then u, as the kernel computed them
+ *   h_dbg  nullable fp32 [ncols][I]: SiLU(g)*u before its re-quantization
+ *   y      fp32 [ncols][y_ld], y_ld >= H
+ * H % 256 == 0 and I % 256 == 0. */
+typedef struct mq_ffn_desc {
+    const void* W_gu;
+    const void* W_down;
+    const float* x;
+    const void* xq;
+    void* h_q8;
+    float* gu_dbg;
+    float* h_dbg;
+    float* y;
+    int32_t H;
+    int32_t I;
+    int32_t ncols;
+    int32_t y_ld;
+} mq_ffn_desc;
+
+mq_status mq_check_ffn_desc(const mq_ffn_desc* h_desc);
+/* Two launches on `stream`: (1) g|u = W_gu . q8_0(x), h = SiLU(g)*u, h_q8 =
+ * q8_0(h) in the epilogue; (2) y = W_down . h_q8. */
+mq_status mq_ffn_gu_silu_down(const mq_ffn_desc* d_desc, int32_t H, int32_t I, int32_t ncols,
+                              void* stream);
+/* The first of those two launches alone: fills h_q8 (and the debug outputs),
+ * leaves y untouched.  W_down and y may be NULL in the descriptor. */
+mq_status mq_ffn_gate_up(const mq_ffn_desc* d_desc, int32_t H, int32_t I, int32_t ncols, void* stream);
+
+/* ---- whole decode step of a layer stack ------------------------------------------
+ * Per layer, in order: qkv (the concatenated q|k|v projection, input x = a_l),
+ * o (input b_l), then the FFN (input c_l).  d_layers: device array of
+ * n_layers layer descriptors.  h_shape: host copy of the shapes (grid sizes;
+ * the capture key).  Capturable as one CUDA graph. */
+typedef struct mq_layer_desc {
+    mq_mv_desc qkv;
+    mq_mv_desc o;
+    mq_ffn_desc ffn;
+} mq_layer_desc;
+
+#define MQ_STEP_PDL 1u   /* launch with programmatic dependent launch */
+
+typedef struct mq_step_shape {
+    int32_t n_layers;
+    int32_t H;        /* hidden: K of qkv and of ffn_gu, rows of down */
+    int32_t I;        /* intermediate */
+    int32_t qkv_rows; /* rows of the q|k|v matrix */
+    int32_t o_rows;   /* rows of o */
+    int32_t o_K;      /* K of o */
+    int32_t ncols;
+    uint32_t flags;   /* MQ_STEP_* */
+} mq_step_shape;
+
+mq_status mq_step(const mq_layer_desc* d_layers, const mq_step_shape* h_shape, void* stream);
+
+/* ---- test export ---------------------------------------------------------------------
+ * The per-32-block integer sums of a matvec, computed by the same device code
+ * as the matvec kernel: sumi int32 [ncols][rows][K/32] = sum q4*q8 per block,
+ * sumq int32 [ncols][K/32] = sum q8 per block. */
+mq_status mq_debug_block_sums_q4K_q8_0(const mq_mv_desc* d_desc, int32_t rows, int32_t K, int32_t ncols,
+                                       int32_t* sumi, int32_t* sumq, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MQ_H */

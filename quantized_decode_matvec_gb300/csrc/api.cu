@@ -1,0 +1,405 @@
+// api.cu -- the extern "C" boundary of libmq (declared in include/mq.h):
+// argument validation, launch planning and launches.  No allocation after
+// mq_init, no synchronization and no host read of device memory inside a
+// compute call, so every compute call can be captured into a CUDA graph.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "mq.h"
+#include "mq_internal.h"
+
+namespace mq {
+cudaError_t set_mv_attributes(int max_smem);
+cudaError_t set_gu_attributes(int max_smem);
+}  // namespace mq
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+mq::DeviceInfo g_dev[kMaxDevices];
+thread_local int g_last_cuda_error = 0;
+
+// Device status word (one per device that loads the library): kernels OR in
+// MQ_DEV_* bits when their device descriptor disagrees with their launch.
+__device__ unsigned g_status_word;
+
+mq_status cuda_fail(cudaError_t e)
+{
+    g_last_cuda_error = int(e);
+    return MQ_ERR_CUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+mq_status current_dev(const mq::DeviceInfo** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices || !g_dev[dev].ready) return MQ_ERR_NOT_INITIALIZED;
+    *out = &g_dev[dev];
+    return MQ_OK;
+}
+
+mq_status check_mv_shape(int64_t rows, int64_t K, int64_t ncols)
+{
+    if (rows < 0 || ncols < 0 || K < 0) return MQ_ERR_SHAPE;
+    if (ncols > MQ_MAX_NCOLS) return MQ_ERR_SHAPE;
+    if (K == 0 || K % 256) return MQ_ERR_SHAPE;
+    if (K > MQ_MAX_K || K * ncols > MQ_MAX_K_TIMES_NCOLS || rows > INT32_MAX) return MQ_ERR_UNSUPPORTED;
+    return MQ_OK;
+}
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+namespace mq {
+
+const DeviceInfo* current_device_info()
+{
+    const DeviceInfo* d = nullptr;
+    return current_dev(&d) == MQ_OK ? d : nullptr;
+}
+
+bool plan_mv(int64_t rows, int K, int nc, int kind, int I, const DeviceInfo& dev, MvPlan* p)
+{
+    MvPlan q = {};
+    q.C = K / 64;
+    if (q.C <= 8) {
+        q.L = 8;
+        q.nseg = 1;
+    } else if (q.C <= 16) {
+        q.L = 16;
+        q.nseg = 1;
+    } else {
+        q.L = 32;
+        q.nseg = (q.C + 31) / 32;
+    }
+    // segments of whole super-blocks (4 chunks), at most L chunks
+    q.S = ((q.C + q.nseg - 1) / q.nseg + 3) / 4 * 4;
+    q.nseg = (q.C + q.S - 1) / q.S;
+    // distribution unit: a row, or for the gate/up kernel a 32-index block of h
+    const int64_t units = (kind == KIND_GU) ? I / 32 : rows;
+    if (units <= 0) return false;
+    int64_t G = units < dev.num_sms ? units : dev.num_sms;
+    int64_t rpc = 0, smem = 0;
+    for (;;) {
+        const int64_t upc = (units + G - 1) / G;
+        rpc = (kind == KIND_GU) ? upc * 64 : upc;
+        smem = int64_t(nc) * q.C * 80 + rpc * q.nseg * nc * 4 + ((kind == KIND_GU) ? int64_t(nc) * rpc * 4 : 0);
+        if (smem <= dev.max_smem_optin) break;
+        if (upc == 1) return false;
+        G = (G + dev.num_sms < units) ? G + dev.num_sms : units;
+    }
+    const int ipw = 32 / q.L;
+    int64_t nw = (rpc * q.nseg + ipw - 1) / ipw;
+    if (nw < 4) nw = 4;
+    if (nw > 16) nw = 16;
+    q.rows_per_cta = int(rpc);
+    q.grid = int(G);
+    q.block = int(32 * nw);
+    q.smem = int(smem);
+    *p = q;
+    return true;
+}
+
+cudaError_t set_kernel_attributes(int max_smem)
+{
+    cudaError_t e = set_mv_attributes(max_smem);
+    if (e == cudaSuccess) e = set_gu_attributes(max_smem);
+    return e;
+}
+
+}  // namespace mq
+
+extern "C" {
+
+const char* mq_status_string(mq_status s)
+{
+    switch (s) {
+        case MQ_OK: return "ok";
+        case MQ_ERR_INVALID_ARG: return "invalid argument";
+        case MQ_ERR_SHAPE: return "invalid shape";
+        case MQ_ERR_ALIGN: return "misaligned pointer";
+        case MQ_ERR_CUDA: return "CUDA error";
+        case MQ_ERR_UNSUPPORTED: return "size beyond the library's limits";
+        case MQ_ERR_NOT_INITIALIZED: return "mq_init was not called for this device";
+        default: return "unknown status";
+    }
+}
+
+int mq_abi_version(void) { return MQ_ABI_VERSION; }
+
+int mq_last_cuda_error(void) { return g_last_cuda_error; }
+
+mq_status mq_init(int device)
+{
+    if (device < 0 || device >= kMaxDevices) return MQ_ERR_INVALID_ARG;
+    int prev = 0;
+    cudaError_t e = cudaGetDevice(&prev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaSetDevice(device)) != cudaSuccess) return cuda_fail(e);
+    mq::DeviceInfo info;
+    mq_status st = MQ_OK;
+    do {
+        if ((e = cudaDeviceGetAttribute(&info.num_sms, cudaDevAttrMultiProcessorCount, device)) != cudaSuccess) break;
+        if ((e = cudaDeviceGetAttribute(&info.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device)) !=
+            cudaSuccess)
+            break;
+        if ((e = mq::set_kernel_attributes(info.max_smem_optin)) != cudaSuccess) break;
+        void* p = nullptr;
+        if ((e = cudaGetSymbolAddress(&p, g_status_word)) != cudaSuccess) break;
+        info.status = static_cast<unsigned*>(p);
+        if ((e = cudaMemset(info.status, 0, sizeof(unsigned))) != cudaSuccess) break;
+        if ((e = cudaDeviceSynchronize()) != cudaSuccess) break;
+        info.ready = true;
+    } while (0);
+    if (e != cudaSuccess) st = cuda_fail(e);
+    cudaSetDevice(prev);
+    if (st == MQ_OK) g_dev[device] = info;
+    return st;
+}
+
+mq_status mq_read_device_status(uint32_t* bits, void* stream)
+{
+    if (!bits) return MQ_ERR_INVALID_ARG;
+    const mq::DeviceInfo* dev = nullptr;
+    mq_status st = current_dev(&dev);
+    if (st != MQ_OK) return st;
+    cudaError_t e;
+    unsigned v = 0;
+    if ((e = cudaMemcpyAsync(&v, dev->status, sizeof(unsigned), cudaMemcpyDeviceToHost, as_stream(stream))) !=
+        cudaSuccess)
+        return cuda_fail(e);
+    if ((e = cudaMemsetAsync(dev->status, 0, sizeof(unsigned), as_stream(stream))) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaStreamSynchronize(as_stream(stream))) != cudaSuccess) return cuda_fail(e);
+    *bits = v;
+    return MQ_OK;
+}
+
+size_t mq_q4K_row_bytes(int64_t K) { return (K < 0 || K % 256) ? 0 : size_t(K / 256) * 144; }
+
+size_t mq_q8_0_bytes(int64_t K) { return (K < 0 || K % 32) ? 0 : size_t(K / 32) * 34; }
+
+int mq_quant_block_elems(int32_t ttype)
+{
+    return ttype == MQ_TYPE_Q4_K ? 256 : ttype == MQ_TYPE_Q8_0 ? 32 : 0;
+}
+
+int mq_quant_block_bytes(int32_t ttype)
+{
+    return ttype == MQ_TYPE_Q4_K ? 144 : ttype == MQ_TYPE_Q8_0 ? 34 : 0;
+}
+
+// Mirrors mq_concat_rows' preconditions clause by clause ("04 . 8o",
+// section 3.2): at least two tensors, one type, one ne0 that is a multiple of
+// the block size, and each tensor's bytes == rows * row bytes.
+int mq_concat_rows_feasible(int32_t n, const int32_t* ttype, const int64_t* ne0, const int64_t* ne1,
+                            const uint64_t* nbytes)
+{
+    if (n < 2 || !ttype || !ne0 || !ne1 || !nbytes) return 0;
+    const int32_t tt = ttype[0];
+    for (int32_t i = 0; i < n; ++i)
+        if (ttype[i] != tt) return 0;
+    const int bq = mq_quant_block_elems(tt), bb = mq_quant_block_bytes(tt);
+    if (bb == 0) return 0;
+    const int64_t k = ne0[0];
+    for (int32_t i = 0; i < n; ++i)
+        if (ne0[i] != k) return 0;
+    if (k <= 0 || k % bq) return 0;
+    const uint64_t row = uint64_t(k / bq) * uint64_t(bb);
+    for (int32_t i = 0; i < n; ++i)
+        if (ne1[i] < 0 || nbytes[i] != row * uint64_t(ne1[i])) return 0;
+    return 1;
+}
+
+mq_status mq_concat_rows(void* dst, const void* const* srcs, const int64_t* rows, int32_t n, int32_t ttype,
+                         int64_t ne0, void* stream)
+{
+    if (!dst || !srcs || !rows || n < 2) return MQ_ERR_INVALID_ARG;
+    const int bq = mq_quant_block_elems(ttype), bb = mq_quant_block_bytes(ttype);
+    if (bb == 0) return MQ_ERR_INVALID_ARG;
+    if (ne0 <= 0 || ne0 % bq) return MQ_ERR_SHAPE;
+    const size_t row = size_t(ne0 / bq) * size_t(bb);
+    for (int32_t i = 0; i < n; ++i) {
+        if (rows[i] < 0) return MQ_ERR_SHAPE;
+        if (!srcs[i] && rows[i] > 0) return MQ_ERR_INVALID_ARG;
+    }
+    uint8_t* out = static_cast<uint8_t*>(dst);
+    for (int32_t i = 0; i < n; ++i) {
+        const size_t bytes = row * size_t(rows[i]);
+        if (bytes) {
+            cudaError_t e = cudaMemcpyAsync(out, srcs[i], bytes, cudaMemcpyDeviceToDevice, as_stream(stream));
+            if (e != cudaSuccess) return cuda_fail(e);
+        }
+        out += bytes;
+    }
+    return MQ_OK;
+}
+
+mq_status mq_quantize_q8_0(const float* x, void* xq, int64_t K, int32_t ncols, void* stream)
+{
+    if (K < 0 || ncols < 0 || K % 32) return MQ_ERR_SHAPE;
+    if (K == 0 || ncols == 0) return MQ_OK;
+    if (!x || !xq) return MQ_ERR_INVALID_ARG;
+    if (!aligned(x, 4) || !aligned(xq, 2)) return MQ_ERR_ALIGN;
+    const mq::DeviceInfo* dev = nullptr;
+    mq_status st = current_dev(&dev);
+    if (st != MQ_OK) return st;
+    cudaError_t e = mq::launch_quantize(x, xq, K / 32 * int64_t(ncols), as_stream(stream));
+    return e == cudaSuccess ? MQ_OK : cuda_fail(e);
+}
+
+mq_status mq_check_mv_desc(const mq_mv_desc* h)
+{
+    if (!h) return MQ_ERR_INVALID_ARG;
+    mq_status st = check_mv_shape(h->rows, h->K, h->ncols);
+    if (st != MQ_OK) return st;
+    if (h->y_ld < h->rows) return MQ_ERR_SHAPE;
+    if (h->rows == 0 || h->ncols == 0) return MQ_OK;
+    if (!h->W || !h->y || (!h->x && !h->xq)) return MQ_ERR_INVALID_ARG;
+    if (!aligned(h->W, 16) || !aligned(h->y, 4) || (h->x && !aligned(h->x, 4)) || (!h->x && !aligned(h->xq, 2)) ||
+        !aligned(h->xq_out, 2))
+        return MQ_ERR_ALIGN;
+    return MQ_OK;
+}
+
+static mq_status launch_matvec(const void* d_desc, int kind, int32_t rows, int32_t K, int32_t ncols,
+                               const mq::DeviceInfo* dev, cudaStream_t s, bool pdl)
+{
+    mq::MvPlan p;
+    if (!mq::plan_mv(rows, K, ncols, kind, 0, *dev, &p)) return MQ_ERR_UNSUPPORTED;
+    cudaError_t e = mq::launch_mv(d_desc, kind, rows, K, ncols, p, dev->status, s, pdl);
+    return e == cudaSuccess ? MQ_OK : cuda_fail(e);
+}
+
+mq_status mq_matvec_q4K_q8_0(const mq_mv_desc* d_desc, int32_t rows, int32_t K, int32_t ncols, void* stream)
+{
+    mq_status st = check_mv_shape(rows, K, ncols);
+    if (st != MQ_OK) return st;
+    if (rows == 0 || ncols == 0) return MQ_OK;
+    if (!d_desc) return MQ_ERR_INVALID_ARG;
+    if (!aligned(d_desc, 8)) return MQ_ERR_ALIGN;
+    const mq::DeviceInfo* dev = nullptr;
+    if ((st = current_dev(&dev)) != MQ_OK) return st;
+    return launch_matvec(d_desc, mq::KIND_MV, rows, K, ncols, dev, as_stream(stream), false);
+}
+
+static mq_status check_ffn_shape(int64_t H, int64_t I, int64_t ncols)
+{
+    if (H < 0 || I < 0 || ncols < 0 || ncols > MQ_MAX_NCOLS) return MQ_ERR_SHAPE;
+    if (H == 0 || I == 0 || H % 256 || I % 256) return MQ_ERR_SHAPE;
+    if (H > MQ_MAX_K || I > MQ_MAX_K || H * ncols > MQ_MAX_K_TIMES_NCOLS || I * ncols > MQ_MAX_K_TIMES_NCOLS)
+        return MQ_ERR_UNSUPPORTED;
+    return MQ_OK;
+}
+
+mq_status mq_check_ffn_desc(const mq_ffn_desc* h)
+{
+    if (!h) return MQ_ERR_INVALID_ARG;
+    mq_status st = check_ffn_shape(h->H, h->I, h->ncols);
+    if (st != MQ_OK) return st;
+    if (h->y_ld < h->H) return MQ_ERR_SHAPE;
+    if (h->ncols == 0) return MQ_OK;
+    if (!h->W_gu || !h->W_down || !h->h_q8 || !h->y || (!h->x && !h->xq)) return MQ_ERR_INVALID_ARG;
+    if (!aligned(h->W_gu, 16) || !aligned(h->W_down, 16) || !aligned(h->h_q8, 2) || !aligned(h->y, 4) ||
+        (h->x && !aligned(h->x, 4)) || (!h->x && !aligned(h->xq, 2)) || !aligned(h->gu_dbg, 4) ||
+        !aligned(h->h_dbg, 4))
+        return MQ_ERR_ALIGN;
+    return MQ_OK;
+}
+
+static mq_status launch_ffn(const mq_ffn_desc* d_desc, int32_t H, int32_t I, int32_t ncols,
+                            const mq::DeviceInfo* dev, cudaStream_t s, bool pdl)
+{
+    mq::MvPlan pg, pd;
+    if (!mq::plan_mv(2 * int64_t(I), H, ncols, mq::KIND_GU, I, *dev, &pg)) return MQ_ERR_UNSUPPORTED;
+    if (!mq::plan_mv(H, I, ncols, mq::KIND_DOWN, 0, *dev, &pd)) return MQ_ERR_UNSUPPORTED;
+    cudaError_t e = mq::launch_gu(d_desc, H, I, ncols, pg, dev->status, s, pdl);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = mq::launch_mv(d_desc, mq::KIND_DOWN, H, I, ncols, pd, dev->status, s, pdl);
+    return e == cudaSuccess ? MQ_OK : cuda_fail(e);
+}
+
+mq_status mq_ffn_gu_silu_down(const mq_ffn_desc* d_desc, int32_t H, int32_t I, int32_t ncols, void* stream)
+{
+    mq_status st = check_ffn_shape(H, I, ncols);
+    if (st != MQ_OK) return st;
+    if (ncols == 0) return MQ_OK;
+    if (!d_desc) return MQ_ERR_INVALID_ARG;
+    if (!aligned(d_desc, 8)) return MQ_ERR_ALIGN;
+    const mq::DeviceInfo* dev = nullptr;
+    if ((st = current_dev(&dev)) != MQ_OK) return st;
+    return launch_ffn(d_desc, H, I, ncols, dev, as_stream(stream), false);
+}
+
+mq_status mq_ffn_gate_up(const mq_ffn_desc* d_desc, int32_t H, int32_t I, int32_t ncols, void* stream)
+{
+    mq_status st = check_ffn_shape(H, I, ncols);
+    if (st != MQ_OK) return st;
+    if (ncols == 0) return MQ_OK;
+    if (!d_desc) return MQ_ERR_INVALID_ARG;
+    if (!aligned(d_desc, 8)) return MQ_ERR_ALIGN;
+    const mq::DeviceInfo* dev = nullptr;
+    if ((st = current_dev(&dev)) != MQ_OK) return st;
+    mq::MvPlan pg;
+    if (!mq::plan_mv(2 * int64_t(I), H, ncols, mq::KIND_GU, I, *dev, &pg)) return MQ_ERR_UNSUPPORTED;
+    cudaError_t e = mq::launch_gu(d_desc, H, I, ncols, pg, dev->status, as_stream(stream), false);
+    return e == cudaSuccess ? MQ_OK : cuda_fail(e);
+}
+
+mq_status mq_step(const mq_layer_desc* d_layers, const mq_step_shape* h, void* stream)
+{
+    if (!h) return MQ_ERR_INVALID_ARG;
+    if (h->n_layers < 0) return MQ_ERR_SHAPE;
+    if (h->n_layers == 0 || h->ncols == 0) return MQ_OK;
+    if (!d_layers) return MQ_ERR_INVALID_ARG;
+    if (!aligned(d_layers, 8)) return MQ_ERR_ALIGN;
+    mq_status st;
+    if ((st = check_mv_shape(h->qkv_rows, h->H, h->ncols)) != MQ_OK) return st;
+    if ((st = check_mv_shape(h->o_rows, h->o_K, h->ncols)) != MQ_OK) return st;
+    if ((st = check_ffn_shape(h->H, h->I, h->ncols)) != MQ_OK) return st;
+    if (h->qkv_rows == 0 || h->o_rows == 0) return MQ_ERR_SHAPE;
+    const mq::DeviceInfo* dev = nullptr;
+    if ((st = current_dev(&dev)) != MQ_OK) return st;
+    const bool pdl = (h->flags & MQ_STEP_PDL) != 0;
+    const cudaStream_t s = as_stream(stream);
+    // one plan per projection, decided once for the whole stack
+    mq::MvPlan p_qkv, p_o, p_gu, p_down;
+    if (!mq::plan_mv(h->qkv_rows, h->H, h->ncols, mq::KIND_MV, 0, *dev, &p_qkv) ||
+        !mq::plan_mv(h->o_rows, h->o_K, h->ncols, mq::KIND_MV, 0, *dev, &p_o) ||
+        !mq::plan_mv(2 * int64_t(h->I), h->H, h->ncols, mq::KIND_GU, h->I, *dev, &p_gu) ||
+        !mq::plan_mv(h->H, h->I, h->ncols, mq::KIND_DOWN, 0, *dev, &p_down))
+        return MQ_ERR_UNSUPPORTED;
+    for (int32_t l = 0; l < h->n_layers; ++l) {
+        const mq_layer_desc* L = d_layers + l;
+        cudaError_t e = mq::launch_mv(&L->qkv, mq::KIND_MV, h->qkv_rows, h->H, h->ncols, p_qkv, dev->status, s, pdl);
+        if (e == cudaSuccess) e = mq::launch_mv(&L->o, mq::KIND_MV, h->o_rows, h->o_K, h->ncols, p_o, dev->status, s, pdl);
+        if (e == cudaSuccess) e = mq::launch_gu(&L->ffn, h->H, h->I, h->ncols, p_gu, dev->status, s, pdl);
+        if (e == cudaSuccess)
+            e = mq::launch_mv(&L->ffn, mq::KIND_DOWN, h->H, h->I, h->ncols, p_down, dev->status, s, pdl);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return MQ_OK;
+}
+
+mq_status mq_debug_block_sums_q4K_q8_0(const mq_mv_desc* d_desc, int32_t rows, int32_t K, int32_t ncols,
+                                       int32_t* sumi, int32_t* sumq, void* stream)
+{
+    mq_status st = check_mv_shape(rows, K, ncols);
+    if (st != MQ_OK) return st;
+    if (rows == 0 || ncols == 0) return MQ_OK;
+    if (!d_desc || !sumi || !sumq) return MQ_ERR_INVALID_ARG;
+    if (!aligned(d_desc, 8) || !aligned(sumi, 4) || !aligned(sumq, 4)) return MQ_ERR_ALIGN;
+    const mq::DeviceInfo* dev = nullptr;
+    if ((st = current_dev(&dev)) != MQ_OK) return st;
+    const int64_t smem = int64_t(ncols) * (K / 64) * 80 + int64_t(ncols) * (K / 32) * 4;
+    if (smem > dev->max_smem_optin) return MQ_ERR_UNSUPPORTED;
+    cudaError_t e = mq::launch_block_sums(d_desc, rows, K, ncols, sumi, sumq, int(smem), dev->status,
+                                          as_stream(stream));
+    return e == cudaSuccess ? MQ_OK : cuda_fail(e);
+}
+
+}  // extern "C"

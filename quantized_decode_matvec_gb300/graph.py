@@ -1,0 +1,119 @@
+"""Graph-resident decode step: capture mq_step once, replay it per token.
+
+"Part 4 . Lecture 08 -- Graph-Resident Decode": capture the whole decode step
+as one CUDA graph and replay it (Overview, section 1); everything that varies
+per replay lives in device buffers the graph reads (section 2); lazy state is
+pre-warmed before capture and a failed capture degrades to eager launches
+with a log line instead of failing the run (section 3).
+
+Here the per-replay state is the input of every layer, fed through the fixed
+device buffers of ``StepBuffers`` (copied there from pinned host memory
+before each replay); the descriptors and the grid sizes are fixed at capture.
+"""
+from __future__ import annotations
+
+import logging
+from typing import Callable, Optional
+
+import torch
+
+from . import mq
+
+log = logging.getLogger("quantized_decode_matvec_gb300.graph")
+
+
+class StepGraph:
+    """Captured mq_step over a StepBuffers, with eager fallback.
+
+    ``capture_hook`` (test-only) runs inside the capture window, so a test can
+    plant a capture-illegal host operation and check the fallback.
+    """
+
+    def __init__(self, bufs: "mq.StepBuffers", flags: int = 0, use_graph: bool = True,
+                 capture_hook: Optional[Callable[[], None]] = None, warmup: int = 1):
+        self.bufs = bufs
+        self.flags = flags
+        self.stream = torch.cuda.Stream(device=bufs.device)
+        self.graph: Optional[torch.cuda.CUDAGraph] = None
+        self.captured = False
+        self.capture_error: Optional[str] = None
+        mq.init(bufs.device.index if bufs.device.index is not None else torch.cuda.current_device())
+        # warm-up outside the capture (pre-warms anything lazy on the torch side too)
+        with torch.cuda.stream(self.stream):
+            for _ in range(warmup):
+                bufs.step(self.stream, flags)
+        self.stream.synchronize()
+        if use_graph:
+            self._capture(capture_hook)
+
+    def _capture(self, hook):
+        g = torch.cuda.CUDAGraph()
+        try:
+            with torch.cuda.graph(g, stream=self.stream):
+                if hook is not None:
+                    hook()
+                self.bufs.step(self.stream, self.flags)
+        except Exception as e:  # capture failure: fall back to eager, keep running
+            self.capture_error = f"{type(e).__name__}: {e}"
+            log.warning("mq_step capture failed, running eagerly: %s", self.capture_error)
+            self.graph = None
+            self.captured = False
+            try:
+                torch.cuda.synchronize()
+            except Exception:
+                pass
+            return
+        self.graph = g
+        self.captured = True
+
+    def run(self) -> None:
+        """One decode step on self.stream: graph replay, or eager launches after a failed capture."""
+        if self.captured:
+            self.graph.replay()
+        else:
+            with torch.cuda.stream(self.stream):
+                self.bufs.step(self.stream, self.flags)
+
+    def node_count(self) -> Optional[int]:
+        """Kernel nodes in the captured graph (None if not captured or not queryable)."""
+        if not self.captured:
+            return None
+        try:
+            from cuda.bindings import runtime as rt  # optional: raw graph introspection
+            raw = self.graph.raw_cuda_graph() if hasattr(self.graph, "raw_cuda_graph") else None
+            if raw is None:
+                return None
+            err, _, n = rt.cudaGraphGetNodes(raw, 0)
+            return int(n)
+        except Exception:
+            return None
+
+
+class PinnedFeeder:
+    """Pinned host staging for the per-replay inputs of a StepBuffers.
+
+    ``load(a, b, c)`` copies host arrays into the pinned buffers; ``push(stream)``
+    enqueues the host-to-device copies into the fixed device input buffers.
+    The pinned buffers are allocated once (size of all layers' inputs).
+    """
+
+    def __init__(self, bufs: "mq.StepBuffers"):
+        self.bufs = bufs
+        self.a = torch.empty(bufs.a.shape, dtype=torch.float32, pin_memory=True)
+        self.b = torch.empty(bufs.b.shape, dtype=torch.float32, pin_memory=True)
+        self.c = torch.empty(bufs.c.shape, dtype=torch.float32, pin_memory=True)
+
+    @property
+    def h2d_bytes(self) -> int:
+        return (self.a.numel() + self.b.numel() + self.c.numel()) * 4
+
+    def load(self, a, b, c) -> None:
+        self.a.copy_(torch.as_tensor(a).reshape(self.a.shape))
+        self.b.copy_(torch.as_tensor(b).reshape(self.b.shape))
+        self.c.copy_(torch.as_tensor(c).reshape(self.c.shape))
+
+    def push(self, stream) -> None:
+        with torch.cuda.stream(stream):
+            self.bufs.a.copy_(self.a, non_blocking=True)
+            self.bufs.b.copy_(self.b, non_blocking=True)
+            self.bufs.c.copy_(self.c, non_blocking=True)

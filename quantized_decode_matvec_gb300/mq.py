@@ -1,0 +1,381 @@
+"""Thin ctypes binding of libmq (include/mq.h), same call names as the C ABI.
+
+Argument marshalling only: every step of the compute path runs in the CUDA
+kernels of libmq.so.  There is no CPU fallback: importing this module raises
+if the in-tree library has not been built, and every compute call raises
+``MQError`` on a non-zero status.
+
+Raw calls (``mq_*``) take integer device addresses and a stream handle.
+The tensor-level helpers below them (``quantize_q8_0``, ``matvec_q4K_q8_0``,
+``ffn_gu_silu_down``, ``StepBuffers``) only compute pointers from torch
+tensors, build the descriptor structs and upload them.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, List, Optional, Sequence
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libmq.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"libmq.so is not built ({LIB_PATH}); run `python -c 'import __graft_entry__ as g; g.build()'`")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+c_i32 = ctypes.c_int32
+c_i64 = ctypes.c_int64
+c_u32 = ctypes.c_uint32
+c_vp = ctypes.c_void_p
+
+MQ_OK = 0
+MQ_ERR_INVALID_ARG = 1
+MQ_ERR_SHAPE = 2
+MQ_ERR_ALIGN = 3
+MQ_ERR_CUDA = 4
+MQ_ERR_UNSUPPORTED = 5
+MQ_ERR_NOT_INITIALIZED = 6
+MQ_DEV_DESC_MISMATCH = 1
+MQ_DEV_DESC_ALIGN = 2
+MQ_TYPE_Q4_K = 1
+MQ_TYPE_Q8_0 = 2
+MQ_MAX_NCOLS = 8
+MQ_MAX_K = 131072
+MQ_MAX_K_TIMES_NCOLS = 163840
+MQ_STEP_PDL = 1
+
+
+class MvDesc(ctypes.Structure):
+    _fields_ = [("W", c_vp), ("x", c_vp), ("xq", c_vp), ("xq_out", c_vp), ("y", c_vp),
+                ("rows", c_i32), ("K", c_i32), ("ncols", c_i32), ("y_ld", c_i32)]
+
+
+class FfnDesc(ctypes.Structure):
+    _fields_ = [("W_gu", c_vp), ("W_down", c_vp), ("x", c_vp), ("xq", c_vp), ("h_q8", c_vp),
+                ("gu_dbg", c_vp), ("h_dbg", c_vp), ("y", c_vp),
+                ("H", c_i32), ("I", c_i32), ("ncols", c_i32), ("y_ld", c_i32)]
+
+
+class LayerDesc(ctypes.Structure):
+    _fields_ = [("qkv", MvDesc), ("o", MvDesc), ("ffn", FfnDesc)]
+
+
+class StepShape(ctypes.Structure):
+    _fields_ = [("n_layers", c_i32), ("H", c_i32), ("I", c_i32), ("qkv_rows", c_i32), ("o_rows", c_i32),
+                ("o_K", c_i32), ("ncols", c_i32), ("flags", c_u32)]
+
+
+def _sig(name, res, *args):
+    f = getattr(_lib, name)
+    f.restype = res
+    f.argtypes = list(args)
+    return f
+
+
+_sig("mq_status_string", ctypes.c_char_p, c_i32)
+_sig("mq_abi_version", c_i32)
+_sig("mq_last_cuda_error", c_i32)
+_sig("mq_init", c_i32, c_i32)
+_sig("mq_read_device_status", c_i32, ctypes.POINTER(c_u32), c_vp)
+_sig("mq_q4K_row_bytes", ctypes.c_size_t, c_i64)
+_sig("mq_q8_0_bytes", ctypes.c_size_t, c_i64)
+_sig("mq_quant_block_elems", c_i32, c_i32)
+_sig("mq_quant_block_bytes", c_i32, c_i32)
+_sig("mq_concat_rows_feasible", c_i32, c_i32, ctypes.POINTER(c_i32), ctypes.POINTER(c_i64),
+     ctypes.POINTER(c_i64), ctypes.POINTER(ctypes.c_uint64))
+_sig("mq_concat_rows", c_i32, c_vp, ctypes.POINTER(c_vp), ctypes.POINTER(c_i64), c_i32, c_i32, c_i64, c_vp)
+_sig("mq_quantize_q8_0", c_i32, c_vp, c_vp, c_i64, c_i32, c_vp)
+_sig("mq_check_mv_desc", c_i32, ctypes.POINTER(MvDesc))
+_sig("mq_matvec_q4K_q8_0", c_i32, c_vp, c_i32, c_i32, c_i32, c_vp)
+_sig("mq_check_ffn_desc", c_i32, ctypes.POINTER(FfnDesc))
+_sig("mq_ffn_gu_silu_down", c_i32, c_vp, c_i32, c_i32, c_i32, c_vp)
+_sig("mq_ffn_gate_up", c_i32, c_vp, c_i32, c_i32, c_i32, c_vp)
+_sig("mq_step", c_i32, c_vp, ctypes.POINTER(StepShape), c_vp)
+_sig("mq_debug_block_sums_q4K_q8_0", c_i32, c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp)
+
+# the exported names, one per declaration in include/mq.h
+EXPORTS = ["mq_status_string", "mq_abi_version", "mq_last_cuda_error", "mq_init", "mq_read_device_status",
+           "mq_q4K_row_bytes", "mq_q8_0_bytes", "mq_quant_block_elems", "mq_quant_block_bytes",
+           "mq_concat_rows_feasible", "mq_concat_rows", "mq_quantize_q8_0", "mq_check_mv_desc",
+           "mq_matvec_q4K_q8_0", "mq_check_ffn_desc", "mq_ffn_gu_silu_down", "mq_ffn_gate_up", "mq_step",
+           "mq_debug_block_sums_q4K_q8_0"]
+
+
+class MQError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = f"{where}: {mq_status_string(status)} (status {status})"
+        if status == MQ_ERR_CUDA:
+            msg += f", cudaError {mq_last_cuda_error()}"
+        super().__init__(msg)
+
+
+def status_string(s: int) -> str:
+    return _lib.mq_status_string(s).decode()
+
+
+# ---- raw calls, same names as the C ABI -------------------------------------------------------------
+
+def mq_status_string(s: int) -> str:
+    return status_string(s)
+
+
+def mq_abi_version() -> int:
+    return _lib.mq_abi_version()
+
+
+def mq_last_cuda_error() -> int:
+    return _lib.mq_last_cuda_error()
+
+
+def mq_init(device: int) -> int:
+    return _lib.mq_init(device)
+
+
+def mq_read_device_status(stream: int = 0) -> int:
+    v = c_u32(0)
+    _check(_lib.mq_read_device_status(ctypes.byref(v), c_vp(stream)), "mq_read_device_status")
+    return v.value
+
+
+def mq_q4K_row_bytes(K: int) -> int:
+    return _lib.mq_q4K_row_bytes(K)
+
+
+def mq_q8_0_bytes(K: int) -> int:
+    return _lib.mq_q8_0_bytes(K)
+
+
+def mq_quant_block_elems(t: int) -> int:
+    return _lib.mq_quant_block_elems(t)
+
+
+def mq_quant_block_bytes(t: int) -> int:
+    return _lib.mq_quant_block_bytes(t)
+
+
+def mq_concat_rows_feasible(ttypes: Sequence[int], ne0: Sequence[int], ne1: Sequence[int],
+                            nbytes: Sequence[int]) -> bool:
+    n = len(ttypes)
+    if not (len(ne0) == len(ne1) == len(nbytes) == n):
+        return False
+    A = lambda ct, v: (ct * n)(*v)
+    return bool(_lib.mq_concat_rows_feasible(n, A(c_i32, ttypes), A(c_i64, ne0), A(c_i64, ne1),
+                                             A(ctypes.c_uint64, nbytes)))
+
+
+def mq_concat_rows(dst: int, srcs: Sequence[int], rows: Sequence[int], ttype: int, ne0: int,
+                   stream: int = 0) -> int:
+    n = len(srcs)
+    return _lib.mq_concat_rows(c_vp(dst), (c_vp * n)(*srcs), (c_i64 * n)(*rows), n, ttype, ne0, c_vp(stream))
+
+
+def mq_quantize_q8_0(x: int, xq: int, K: int, ncols: int, stream: int = 0) -> int:
+    return _lib.mq_quantize_q8_0(c_vp(x), c_vp(xq), K, ncols, c_vp(stream))
+
+
+def mq_check_mv_desc(d: MvDesc) -> int:
+    return _lib.mq_check_mv_desc(ctypes.byref(d))
+
+
+def mq_matvec_q4K_q8_0(d_desc: int, rows: int, K: int, ncols: int, stream: int = 0) -> int:
+    return _lib.mq_matvec_q4K_q8_0(c_vp(d_desc), rows, K, ncols, c_vp(stream))
+
+
+def mq_check_ffn_desc(d: FfnDesc) -> int:
+    return _lib.mq_check_ffn_desc(ctypes.byref(d))
+
+
+def mq_ffn_gu_silu_down(d_desc: int, H: int, I: int, ncols: int, stream: int = 0) -> int:
+    return _lib.mq_ffn_gu_silu_down(c_vp(d_desc), H, I, ncols, c_vp(stream))
+
+
+def mq_ffn_gate_up(d_desc: int, H: int, I: int, ncols: int, stream: int = 0) -> int:
+    return _lib.mq_ffn_gate_up(c_vp(d_desc), H, I, ncols, c_vp(stream))
+
+
+def mq_step(d_layers: int, shape: StepShape, stream: int = 0) -> int:
+    return _lib.mq_step(c_vp(d_layers), ctypes.byref(shape), c_vp(stream))
+
+
+def mq_debug_block_sums_q4K_q8_0(d_desc: int, rows: int, K: int, ncols: int, sumi: int, sumq: int,
+                                 stream: int = 0) -> int:
+    return _lib.mq_debug_block_sums_q4K_q8_0(c_vp(d_desc), rows, K, ncols, c_vp(sumi), c_vp(sumq), c_vp(stream))
+
+
+def _check(st: int, where: str):
+    if st != MQ_OK:
+        raise MQError(st, where)
+
+
+# ---- tensor-level marshalling (torch owns memory and streams) ------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    torch = _torch()
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+_initialized = set()
+
+
+def init(device: Optional[int] = None) -> None:
+    """mq_init for a device (default: torch's current device), once."""
+    torch = _torch()
+    dev = torch.cuda.current_device() if device is None else int(device)
+    if dev in _initialized:
+        return
+    torch.cuda.init()
+    _check(mq_init(dev), "mq_init")
+    _initialized.add(dev)
+
+
+def upload_struct(s: ctypes.Structure, device) -> "torch.Tensor":
+    """Copy a descriptor struct to a new device buffer (8-byte aligned)."""
+    torch = _torch()
+    raw = bytes(s) if not isinstance(s, (bytes, bytearray)) else s
+    host = torch.frombuffer(bytearray(raw), dtype=torch.uint8)
+    return host.to(device)
+
+
+def quantize_q8_0(x, out=None, stream=None):
+    """fp32 [ncols, K] cuda tensor -> uint8 [ncols, K/32*34] q8_0."""
+    torch = _torch()
+    x2 = x if x.dim() == 2 else x.reshape(1, -1)
+    ncols, K = x2.shape
+    if out is None:
+        out = torch.empty((ncols, K // 32 * 34), dtype=torch.uint8, device=x.device)
+    _check(mq_quantize_q8_0(_ptr(x2), _ptr(out), K, ncols, _stream(stream)), "mq_quantize_q8_0")
+    return out
+
+
+def mv_desc(W, rows: int, K: int, y, x=None, xq=None, xq_out=None, ncols: int = 1,
+            y_ld: Optional[int] = None) -> MvDesc:
+    return MvDesc(_ptr(W), _ptr(x), _ptr(xq), _ptr(xq_out), _ptr(y), rows, K, ncols,
+                  rows if y_ld is None else y_ld)
+
+
+def matvec_q4K_q8_0(W, rows: int, K: int, x=None, xq=None, y=None, xq_out=None, ncols: Optional[int] = None,
+                    stream=None):
+    """y [ncols, rows] fp32 = W . q8_0(x) (or W . xq).  Returns (y, desc_buffer)."""
+    torch = _torch()
+    act = x if x is not None else xq
+    if ncols is None:
+        ncols = act.shape[0] if act.dim() == 2 else 1
+    if y is None:
+        y = torch.empty((ncols, rows), dtype=torch.float32, device=W.device)
+    d = mv_desc(W, rows, K, y, x=x, xq=xq, xq_out=xq_out, ncols=ncols, y_ld=y.shape[-1])
+    _check(mq_check_mv_desc(d), "mq_check_mv_desc")
+    dd = upload_struct(d, W.device)
+    _check(mq_matvec_q4K_q8_0(_ptr(dd), rows, K, ncols, _stream(stream)), "mq_matvec_q4K_q8_0")
+    return y, dd
+
+
+def block_sums(W, rows: int, K: int, x=None, xq=None, ncols: Optional[int] = None, stream=None):
+    """Test export: (sumi int32 [ncols, rows, K/32], sumq int32 [ncols, K/32])."""
+    torch = _torch()
+    act = x if x is not None else xq
+    if ncols is None:
+        ncols = act.shape[0] if act.dim() == 2 else 1
+    y = torch.empty((ncols, rows), dtype=torch.float32, device=W.device)
+    d = mv_desc(W, rows, K, y, x=x, xq=xq, ncols=ncols)
+    _check(mq_check_mv_desc(d), "mq_check_mv_desc")
+    dd = upload_struct(d, W.device)
+    sumi = torch.empty((ncols, rows, K // 32), dtype=torch.int32, device=W.device)
+    sumq = torch.empty((ncols, K // 32), dtype=torch.int32, device=W.device)
+    _check(mq_debug_block_sums_q4K_q8_0(_ptr(dd), rows, K, ncols, _ptr(sumi), _ptr(sumq), _stream(stream)),
+           "mq_debug_block_sums_q4K_q8_0")
+    return sumi, sumq
+
+
+def ffn_desc(W_gu, W_down, H: int, I: int, h_q8, y, x=None, xq=None, gu_dbg=None, h_dbg=None, ncols: int = 1,
+             y_ld: Optional[int] = None) -> FfnDesc:
+    return FfnDesc(_ptr(W_gu), _ptr(W_down), _ptr(x), _ptr(xq), _ptr(h_q8), _ptr(gu_dbg), _ptr(h_dbg), _ptr(y),
+                   H, I, ncols, H if y_ld is None else y_ld)
+
+
+def ffn_gu_silu_down(W_gu, W_down, H: int, I: int, x=None, xq=None, debug: bool = False, stream=None):
+    """Fused FFN.  Returns dict with y [ncols, H], h_q8 and (debug) gu, h, plus the descriptor buffer."""
+    torch = _torch()
+    act = x if x is not None else xq
+    ncols = act.shape[0] if act.dim() == 2 else 1
+    dev = W_gu.device
+    out = {
+        "y": torch.empty((ncols, H), dtype=torch.float32, device=dev),
+        "h_q8": torch.empty((ncols, I // 32 * 34), dtype=torch.uint8, device=dev),
+    }
+    if debug:
+        out["gu"] = torch.empty((ncols, 2 * I), dtype=torch.float32, device=dev)
+        out["h"] = torch.empty((ncols, I), dtype=torch.float32, device=dev)
+    d = ffn_desc(W_gu, W_down, H, I, out["h_q8"], out["y"], x=x, xq=xq, gu_dbg=out.get("gu"), h_dbg=out.get("h"),
+                 ncols=ncols)
+    _check(mq_check_ffn_desc(d), "mq_check_ffn_desc")
+    out["desc"] = upload_struct(d, dev)
+    _check(mq_ffn_gu_silu_down(_ptr(out["desc"]), H, I, ncols, _stream(stream)), "mq_ffn_gu_silu_down")
+    return out
+
+
+class StepBuffers:
+    """Device buffers and the descriptor table of one layer stack for mq_step.
+
+    weights: per layer dict with 'qkv' (concatenated q|k|v rows), 'o', 'gu', 'down'
+    (uint8 cuda tensors).  Inputs a/b/c and outputs are allocated here, one buffer
+    per layer, so a captured graph reads fresh inputs from the same addresses on
+    every replay.
+    """
+
+    def __init__(self, weights: List[Dict[str, "torch.Tensor"]], H: int, I: int, qkv_rows: int, o_rows: int,
+                 o_K: int, ncols: int = 1, device=None, debug: bool = False):
+        torch = _torch()
+        self.n_layers = len(weights)
+        self.H, self.I, self.qkv_rows, self.o_rows, self.o_K, self.ncols = H, I, qkv_rows, o_rows, o_K, ncols
+        dev = device if device is not None else weights[0]["qkv"].device
+        self.device = dev
+        n = self.n_layers
+        self.weights = weights
+        # inputs [layer, ncols, K]
+        self.a = torch.zeros((n, ncols, H), dtype=torch.float32, device=dev)
+        self.b = torch.zeros((n, ncols, o_K), dtype=torch.float32, device=dev)
+        self.c = torch.zeros((n, ncols, H), dtype=torch.float32, device=dev)
+        # outputs
+        self.y_qkv = torch.zeros((n, ncols, qkv_rows), dtype=torch.float32, device=dev)
+        self.y_o = torch.zeros((n, ncols, o_rows), dtype=torch.float32, device=dev)
+        self.y_ffn = torch.zeros((n, ncols, H), dtype=torch.float32, device=dev)
+        self.h_q8 = torch.zeros((n, ncols, I // 32 * 34), dtype=torch.uint8, device=dev)
+        self.debug = debug
+        if debug:
+            self.xq_a = torch.zeros((n, ncols, H // 32 * 34), dtype=torch.uint8, device=dev)
+            self.xq_b = torch.zeros((n, ncols, o_K // 32 * 34), dtype=torch.uint8, device=dev)
+        table = (LayerDesc * n)()
+        for l, w in enumerate(weights):
+            table[l].qkv = mv_desc(w["qkv"], qkv_rows, H, self.y_qkv[l], x=self.a[l],
+                                   xq_out=self.xq_a[l] if debug else None, ncols=ncols, y_ld=qkv_rows)
+            table[l].o = mv_desc(w["o"], o_rows, o_K, self.y_o[l], x=self.b[l],
+                                 xq_out=self.xq_b[l] if debug else None, ncols=ncols, y_ld=o_rows)
+            table[l].ffn = ffn_desc(w["gu"], w["down"], H, I, self.h_q8[l], self.y_ffn[l], x=self.c[l],
+                                    ncols=ncols, y_ld=H)
+            for part in (table[l].qkv, table[l].o):
+                _check(mq_check_mv_desc(part), "mq_check_mv_desc")
+            _check(mq_check_ffn_desc(table[l].ffn), "mq_check_ffn_desc")
+        self.table_host = table
+        self.table = upload_struct(bytes(table), dev)
+
+    def shape(self, flags: int = 0) -> StepShape:
+        return StepShape(self.n_layers, self.H, self.I, self.qkv_rows, self.o_rows, self.o_K, self.ncols, flags)
+
+    def step(self, stream=None, flags: int = 0) -> None:
+        _check(mq_step(_ptr(self.table), self.shape(flags), _stream(stream)), "mq_step")

@@ -9,7 +9,8 @@ Recipe (every tensor gets its own stream, ``PCG64(SeedSequence([seed, tag]))``):
 
 * q4_K weight matrix [rows, K] (K a multiple of 256): ``rows * K/256``
   super-blocks of 144 bytes.  First the whole byte image is drawn uniformly
-  (``Generator.bytes``), then bytes 0-1 of every super-block are overwritten
+  (the raw 64-bit PCG64 outputs, ``bit_generator.random_raw``, read as
+  little-endian bytes), then bytes 0-1 of every super-block are overwritten
   with the binary16 value of ``|N(0, 2e-3)|`` (the super-block scale d) and
   bytes 2-3 with binary16 ``|N(0, 1e-3)|`` (dmin), both converted by numpy's
   ``astype(float16)``.  Because the twelve scale bytes carry exactly sixteen
@@ -61,7 +62,8 @@ def q4K_matrix(rows: int, K: int, seed: int, tag: int = TAG_W, layer: int = 0,
     nb = K // QK_K
     rng = stream(seed, tag, layer)
     nbytes = rows * nb * Q4K_BLOCK_BYTES
-    img = np.frombuffer(bytearray(rng.bytes(nbytes)), dtype=np.uint8).reshape(rows * nb, Q4K_BLOCK_BYTES)
+    raw = rng.bit_generator.random_raw((nbytes + 7) // 8).astype("<u8", copy=False)
+    img = raw.view(np.uint8)[:nbytes].reshape(rows * nb, Q4K_BLOCK_BYTES)
     d = np.abs(rng.standard_normal(rows * nb)) * d_sigma
     dmin = np.abs(rng.standard_normal(rows * nb)) * dmin_sigma
     img[:, 0:2] = d.astype(np.float16).view(np.uint8).reshape(-1, 2)

@@ -18,8 +18,8 @@ def mq_lib():
     """The C-ABI library, built in-tree if missing or stale."""
     from quantized_decode_matvec_gb300 import build as mqbuild
     mqbuild.build()
-    from quantized_decode_matvec_gb300 import _binding
-    return _binding
+    from quantized_decode_matvec_gb300 import mq
+    return mq
 
 
 @pytest.fixture(scope="session")
@@ -28,6 +28,5 @@ def cuda_ready(mq_lib):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     torch.cuda.init()
-    st = mq_lib.mq_init(torch.cuda.current_device())
-    assert st == 0, mq_lib.status_string(st)
+    mq_lib.init(torch.cuda.current_device())
     return mq_lib

@@ -1,0 +1,216 @@
+"""The whole decode step of a layer stack (mq_step), eager and as a CUDA graph.
+
+Graph tests follow "Part 4 . Lecture 08 -- Graph-Resident Decode": capture
+plus at least seven replays, each with different inputs, each byte-compared
+with an eager run on the same inputs (section 4); an A/A control before any
+A/B (section 5); a deliberately frozen input that must go stale from replay 2
+on (section 4); a failed capture that degrades to eager (section 3).
+"""
+import numpy as np
+import pytest
+
+import oracle
+from quantized_decode_matvec_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+SMALL = synth.StepCase("step_small", n_layers=3, H=512, I=1024, q_rows=512, kv_rows=128, ncols=1, seed=5)
+
+
+def _weights(case, device="cuda"):
+    import torch
+    out, host = [], []
+    for l in range(case.n_layers):
+        w = synth.step_layer_weights(case, l)
+        qkv = np.concatenate([w["q"], w["k"], w["v"]])          # row concatenation q|k|v
+        host.append({"qkv": qkv, "o": w["o"], "gu": w["gu"], "down": w["down"]})
+        out.append({k: torch.from_numpy(v).to(device) for k, v in host[-1].items()})
+    return out, host
+
+
+def _inputs(case, replay):
+    a = np.stack([synth.step_layer_inputs(case, l, replay)["a"] for l in range(case.n_layers)])
+    b = np.stack([synth.step_layer_inputs(case, l, replay)["b"] for l in range(case.n_layers)])
+    c = np.stack([synth.step_layer_inputs(case, l, replay)["c"] for l in range(case.n_layers)])
+    return a, b, c
+
+
+def _bufs(mq, case, wdev, debug=False):
+    return mq.StepBuffers(wdev, case.H, case.I, case.qkv_rows, case.H, case.q_rows, case.ncols, debug=debug)
+
+
+def _outputs(bufs):
+    import torch
+    torch.cuda.synchronize()
+    return {k: getattr(bufs, k).cpu().numpy().copy() for k in ("y_qkv", "y_o", "y_ffn", "h_q8")}
+
+
+def _set_inputs(bufs, a, b, c):
+    import torch
+    bufs.a.copy_(torch.from_numpy(a))
+    bufs.b.copy_(torch.from_numpy(b))
+    bufs.c.copy_(torch.from_numpy(c))
+
+
+def _check_layer_oracle(case, host, outs, a, b, c, l, rows=None):
+    """Layer l of a step against the oracle (sampled rows if given); FFN teacher-forced on h_q8."""
+    H, I = case.H, case.I
+    rs = lambda n: None if rows is None else np.sort(np.unique(np.concatenate([rows % n, [0, n - 1]])))
+    for name, W, x, K, y in (("qkv", host[l]["qkv"], a[l], H, outs["y_qkv"][l]),
+                             ("o", host[l]["o"], b[l], case.q_rows, outs["y_o"][l])):
+        ids = rs(W.shape[0])
+        y_ref, T = oracle.matvec(W, oracle.quantize_q8_0(x), W.shape[0], K, row_ids=ids)
+        yg = y if ids is None else y[:, ids]
+        assert oracle.within_tolerance(yg, y_ref, T).all(), (name, l)
+    ids = rs(H)
+    y_ref, T = oracle.matvec(host[l]["down"], outs["h_q8"][l], H, I, row_ids=ids)
+    yg = outs["y_ffn"][l] if ids is None else outs["y_ffn"][l][:, ids]
+    assert oracle.within_tolerance(yg, y_ref, T).all(), ("down", l)
+
+
+def test_step_small_eager_matches_oracle(cuda_ready):
+    mq = cuda_ready
+    wdev, host = _weights(SMALL)
+    bufs = _bufs(mq, SMALL, wdev, debug=True)
+    a, b, c = _inputs(SMALL, 0)
+    _set_inputs(bufs, a, b, c)
+    bufs.step()
+    outs = _outputs(bufs)
+    for l in range(SMALL.n_layers):
+        _check_layer_oracle(SMALL, host, outs, a, b, c, l)
+        assert np.array_equal(bufs.xq_a[l].cpu().numpy(), oracle.quantize_q8_0(a[l]))
+        # h_q8 against the whole oracle FFN chain: codes may differ only where h sits on a rounding edge
+        _, hq_ref = oracle.ffn(host[l]["gu"], host[l]["down"], c[l], SMALL.H, SMALL.I)
+        assert np.mean(outs["h_q8"][l] == hq_ref) > 0.99
+
+
+def test_step_graph_replays_byte_identical(cuda_ready):
+    import torch
+    from quantized_decode_matvec_gb300.graph import StepGraph
+    mq = cuda_ready
+    wdev, host = _weights(SMALL)
+    eager = _bufs(mq, SMALL, wdev)
+    graphed = _bufs(mq, SMALL, wdev)
+    g = StepGraph(graphed)
+    assert g.captured, g.capture_error
+    # A/A first: eager vs eager on the same inputs
+    a, b, c = _inputs(SMALL, 100)
+    _set_inputs(eager, a, b, c)
+    eager.step()
+    first = _outputs(eager)
+    eager.step()
+    again = _outputs(eager)
+    for k in first:
+        assert np.array_equal(first[k], again[k])
+    # capture + 7 replays with fresh inputs each, byte-compared with eager
+    for r in range(8):
+        a, b, c = _inputs(SMALL, r)
+        _set_inputs(eager, a, b, c)
+        eager.step()
+        e = _outputs(eager)
+        _set_inputs(graphed, a, b, c)
+        g.run()
+        torch.cuda.synchronize()
+        gr = _outputs(graphed)
+        for k in e:
+            assert np.array_equal(e[k].view(np.uint8), gr[k].view(np.uint8)), (r, k)
+        if r in (0, 7):
+            for l in (0, SMALL.n_layers - 1):
+                _check_layer_oracle(SMALL, host, gr, a, b, c, l)
+
+
+def test_frozen_input_goes_stale_from_replay_2(cuda_ready):
+    # Negative control: a runner that captures its input copy from the staging slot
+    # chosen at capture time.  Replay 1 reuses that slot and is right; from replay 2
+    # the inputs sit in other slots and the graph keeps reading the frozen one.
+    import torch
+    mq = cuda_ready
+    wdev, host = _weights(SMALL)
+    bufs = _bufs(mq, SMALL, wdev)
+    eager = _bufs(mq, SMALL, wdev)
+    slots = [torch.empty((3,) + tuple(bufs.a.shape), dtype=torch.float32, device="cuda") for _ in range(4)]
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        bufs.step(s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    frozen = slots[0]
+    with torch.cuda.graph(g, stream=s):
+        bufs.a.copy_(frozen[0])
+        bufs.b.copy_(frozen[1])
+        bufs.c.copy_(frozen[2])
+        bufs.step(s)
+    mism = []
+    for r in range(4):
+        a, b, c = _inputs(SMALL, r)
+        slot = slots[r % len(slots)] if r > 0 else slots[0]
+        slot[0].copy_(torch.from_numpy(a))
+        slot[1].copy_(torch.from_numpy(b))
+        slot[2].copy_(torch.from_numpy(c))
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        _set_inputs(eager, a, b, c)
+        eager.step()
+        e = _outputs(eager)
+        gr = _outputs(bufs)
+        mism.append(not np.array_equal(e["y_ffn"], gr["y_ffn"]))
+    assert mism == [False, True, True, True]
+
+
+def test_capture_failure_falls_back_to_eager(cuda_ready):
+    import torch
+    from quantized_decode_matvec_gb300.graph import StepGraph
+    mq = cuda_ready
+    wdev, host = _weights(SMALL)
+    bufs = _bufs(mq, SMALL, wdev)
+    # a synchronizing host call inside the capture window is illegal during capture
+    g = StepGraph(bufs, capture_hook=lambda: torch.cuda.synchronize())
+    assert not g.captured and g.capture_error
+    a, b, c = _inputs(SMALL, 3)
+    _set_inputs(bufs, a, b, c)
+    g.run()
+    outs = _outputs(bufs)
+    _check_layer_oracle(SMALL, host, outs, a, b, c, 0)
+    _check_layer_oracle(SMALL, host, outs, a, b, c, SMALL.n_layers - 1)
+
+
+def test_step_pdl_matches_plain(cuda_ready):
+    mq = cuda_ready
+    wdev, host = _weights(SMALL)
+    p = _bufs(mq, SMALL, wdev)
+    q = _bufs(mq, SMALL, wdev)
+    a, b, c = _inputs(SMALL, 4)
+    _set_inputs(p, a, b, c)
+    _set_inputs(q, a, b, c)
+    p.step()
+    q.step(flags=mq.MQ_STEP_PDL)
+    x, y = _outputs(p), _outputs(q)
+    for k in x:
+        assert np.array_equal(x[k].view(np.uint8), y[k].view(np.uint8)), k
+
+
+@pytest.mark.slow
+def test_step_7b_full_size_sampled(cuda_ready):
+    # the 28-layer 7B-class step at full size, as the benchmark runs it (graph replay),
+    # every layer checked on sampled rows (FFN teacher-forced on the kernel's h_q8)
+    import torch
+    from quantized_decode_matvec_gb300.graph import StepGraph
+    mq = cuda_ready
+    case = synth.STEP_7B
+    wdev, host = _weights(case)
+    bufs = _bufs(mq, case, wdev)
+    g = StepGraph(bufs)
+    assert g.captured, g.capture_error
+    rng = np.random.default_rng(0)
+    rows = rng.choice(1 << 20, 48, replace=False)
+    for r in (0, 1, 2):
+        a, b, c = _inputs(case, r)
+        _set_inputs(bufs, a, b, c)
+        g.run()
+        outs = _outputs(bufs)
+        layers = range(case.n_layers) if r == 0 else (0, case.n_layers - 1)
+        for l in layers:
+            _check_layer_oracle(case, host, outs, a, b, c, l, rows=rows)
+    del wdev, bufs, g
+    torch.cuda.empty_cache()
