@@ -313,8 +313,8 @@ def run_ours(args):
     fill_inputs(bufs, case, 0)
     flags = mq.MQ_STEP_PDL if args.pdl else 0
     g = StepGraph(bufs, flags=flags)
-    g_alt = StepGraph(bufs, flags=(0 if args.pdl else mq.MQ_STEP_PDL))
     stream = g.stream
+    g_alt = StepGraph(bufs, flags=(0 if args.pdl else mq.MQ_STEP_PDL), stream=stream)
 
     # warm-up (untimed)
     for _ in range(args.warmup):

@@ -30,10 +30,11 @@ class StepGraph:
     """
 
     def __init__(self, bufs: "mq.StepBuffers", flags: int = 0, use_graph: bool = True,
-                 capture_hook: Optional[Callable[[], None]] = None, warmup: int = 1):
+                 capture_hook: Optional[Callable[[], None]] = None, warmup: int = 1,
+                 stream: Optional[torch.cuda.Stream] = None):
         self.bufs = bufs
         self.flags = flags
-        self.stream = torch.cuda.Stream(device=bufs.device)
+        self.stream = stream if stream is not None else torch.cuda.Stream(device=bufs.device)
         self.graph: Optional[torch.cuda.CUDAGraph] = None
         self.captured = False
         self.capture_error: Optional[str] = None
@@ -67,11 +68,14 @@ class StepGraph:
         self.captured = True
 
     def run(self) -> None:
-        """One decode step on self.stream: graph replay, or eager launches after a failed capture."""
-        if self.captured:
-            self.graph.replay()
-        else:
-            with torch.cuda.stream(self.stream):
+        """One decode step on self.stream: graph replay, or eager launches after a failed capture.
+
+        CUDAGraph.replay() launches on torch's current stream, so make self.stream current.
+        """
+        with torch.cuda.stream(self.stream):
+            if self.captured:
+                self.graph.replay()
+            else:
                 self.bufs.step(self.stream, self.flags)
 
     def node_count(self) -> Optional[int]:
