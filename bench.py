@@ -311,16 +311,19 @@ def run_ours(args):
     layers = build_step(case, device, mq)
     bufs = mq.StepBuffers(layers, case.H, case.I, case.qkv_rows, case.H, case.q_rows, case.ncols)
     fill_inputs(bufs, case, 0)
-    flags = mq.MQ_STEP_PDL if args.pdl else 0
+    mode_flags = {"persistent": mq.MQ_STEP_PERSISTENT, "graph": 0, "pdl": mq.MQ_STEP_PDL}
+    flags = mode_flags[args.mode]
     g = StepGraph(bufs, flags=flags)
     stream = g.stream
-    g_alt = StepGraph(bufs, flags=(0 if args.pdl else mq.MQ_STEP_PDL), stream=stream)
+    alt = {m: StepGraph(bufs, flags=f, stream=stream) for m, f in mode_flags.items() if m != args.mode}
 
     # warm-up (untimed)
     for _ in range(args.warmup):
         g.run()
-        g_alt.run()
+        for a in alt.values():
+            a.run()
     torch.cuda.synchronize()
+    assert mq.mq_read_device_status(0) == 0
 
     # ---- the timed region: K graph replays, inputs resident in HBM (3.67 GB >> L2: no flush needed)
     clocks = ClockSampler(device.index)
@@ -335,39 +338,53 @@ def run_ours(args):
     ms, total_bytes = reduce_over_ranks(ms_local, float(wbytes), device if ws > 1 else None)
     value = total_bytes / (ms / 1e3) / 1e9
 
-    # ---- interleaved arms (context): the other PDL setting, and eager launches
-    arms = {"graph": [], "graph_alt": [], "eager": []}
-    eager_run = lambda: bufs.step(stream, flags)
+    # ---- interleaved arms (context): the other launch modes, and eager launches
+    arms = {args.mode: []}
+    arms.update({m: [] for m in alt})
+    arms["eager"] = []
+    eager_run = lambda: bufs.step(stream, 0)
     for _ in range(3):
-        arms["graph"] += time_replays(g.run, stream, 5)
-        arms["graph_alt"] += time_replays(g_alt.run, stream, 5)
+        arms[args.mode] += time_replays(g.run, stream, 5)
+        for m, a in alt.items():
+            arms[m] += time_replays(a.run, stream, 5)
         with torch.cuda.stream(stream):
             arms["eager"] += time_replays(eager_run, stream, 5)
     arm_stats = {k: {"median_ms": statistics.median(v), "mean_ms": statistics.mean(v), "sem_ms": sem(v)}
                  for k, v in arms.items()}
 
-    # ---- dominant kernel alone: ffn_gu + SiLU*mul + q8_0(h), over the 28 layers' weights
-    ffn_descs = [bufs.table[l * 192 + 112:l * 192 + 192] for l in range(case.n_layers)]
-    reps = 3
-
-    def gu_all():
-        for l in range(case.n_layers):
-            mq._check(mq.mq_ffn_gate_up(ffn_descs[l].data_ptr(), case.H, case.I, case.ncols, stream.cuda_stream),
-                      "mq_ffn_gate_up")
-
-    with torch.cuda.stream(stream):
-        gu_all()
-        t = time_replays(gu_all, stream, reps)
-    gu_ms = sum(t) / (reps * case.n_layers)
-    gu_bytes = (2 * case.I * (case.H // 256) * 144 + case.H * 4 * case.ncols
-                + case.I // 32 * 34 * case.ncols)
     peak, peak_kind = measured_hbm_peak()
-    gu_gbs = gu_bytes / (gu_ms / 1e3) / 1e9
-    roofline = {"bound": "hbm", "achieved": gu_gbs, "peak": peak, "unit": "GB/s", "frac": gu_gbs / peak,
-                "traffic": recorded_traffic("ffn_gate_up_7B.md"),
-                "kernel": "gu_kernel (ffn_gu matvec + SiLU*mul + q8_0 of h), 37888x3584",
-                "peak_kind": f"{peak_kind} (copy bandwidth)", "avg_launch_us": gu_ms * 1e3,
-                "algorithmic_bytes_per_launch": gu_bytes}
+    act_bytes = case.n_layers * (3 * case.H * 4 + case.I // 32 * 34 * 2) * case.ncols
+    out_bytes = case.n_layers * (case.qkv_rows + case.H + case.H) * 4 * case.ncols
+    if args.mode == "persistent":
+        step_bytes = wbytes + act_bytes + out_bytes
+        gbs = step_bytes / (ms_local / 1e3) / 1e9
+        roofline = {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                    "traffic": recorded_traffic("step_kernel_7B.md"),
+                    "kernel": "step_kernel<1> (persistent: all 28 layers, one launch per step)",
+                    "peak_kind": f"{peak_kind} (copy bandwidth)", "avg_launch_us": ms_local * 1e3,
+                    "algorithmic_bytes_per_launch": step_bytes}
+    else:
+        # dominant kernel alone: ffn_gu + SiLU*mul + q8_0(h), over the 28 layers' weights
+        ffn_descs = [bufs.table[l * 192 + 112:l * 192 + 192] for l in range(case.n_layers)]
+        reps = 3
+
+        def gu_all():
+            for l in range(case.n_layers):
+                mq._check(mq.mq_ffn_gate_up(ffn_descs[l].data_ptr(), case.H, case.I, case.ncols,
+                                            stream.cuda_stream), "mq_ffn_gate_up")
+
+        with torch.cuda.stream(stream):
+            gu_all()
+            t = time_replays(gu_all, stream, reps)
+        gu_ms = sum(t) / (reps * case.n_layers)
+        gu_bytes = (2 * case.I * (case.H // 256) * 144 + case.H * 4 * case.ncols
+                    + case.I // 32 * 34 * case.ncols)
+        gu_gbs = gu_bytes / (gu_ms / 1e3) / 1e9
+        roofline = {"bound": "hbm", "achieved": gu_gbs, "peak": peak, "unit": "GB/s", "frac": gu_gbs / peak,
+                    "traffic": recorded_traffic("ffn_gate_up_7B.md"),
+                    "kernel": "ring_kernel<1,GU> (ffn_gu matvec + SiLU*mul + q8_0 of h), 37888x3584",
+                    "peak_kind": f"{peak_kind} (copy bandwidth)", "avg_launch_us": gu_ms * 1e3,
+                    "algorithmic_bytes_per_launch": gu_bytes}
 
     # ---- end to end through host buffers: pinned H2D of the inputs, replay, D2H of the outputs
     feeder = PinnedFeeder(bufs)
@@ -397,6 +414,8 @@ def run_ours(args):
     e2e = {"value": total_bytes / (e2e_ms / 1e3) / 1e9, "unit": UNIT, "ms_per_step": e2e_ms,
            "h2d_bytes_per_step": feeder.h2d_bytes, "d2h_bytes_per_step": d2h,
            "api": "mq_step via a captured CUDA graph; pinned host inputs and outputs"}
+    assert mq.mq_read_device_status(0) == 0
+    launches_per_step = 1 if args.mode == "persistent" else 4 * case.n_layers
 
     cpu = cpu_baseline(case) if (rank == 0 and ws == 1 and not args.no_cpu_baseline) else None
 
@@ -411,13 +430,13 @@ def run_ours(args):
                 "weight_bytes_per_step": wbytes, "weight_bytes_per_layer": per_layer,
                 "l2": "inputs larger than L2 (3.67 GB of weights per step vs 129 MB L2); no flush",
                 "parallelism": "replicas" if ws > 1 else "single GPU",
-                "pdl": bool(args.pdl),
+                "launch_mode": args.mode,
             },
             "frac_of_measured_hbm": value / ws / peak, "frac_of_nominal_8TBs": value / ws / NOMINAL_HBM_GBS,
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": 4 * case.n_layers * args.steps,
+            "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
             "arms": arm_stats,
             "graph_kernel_nodes": g.node_count(),
@@ -434,7 +453,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--pdl", type=int, default=0, help="launch the step with programmatic dependent launch")
+    ap.add_argument("--mode", choices=["persistent", "graph", "pdl"], default="pdl",
+                    help="step launch mode: one persistent kernel, or four kernels per layer (plain or PDL)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -53,7 +53,7 @@
 extern "C" {
 #endif
 
-#define MQ_ABI_VERSION 1
+#define MQ_ABI_VERSION 2
 
 typedef int mq_status;
 #define MQ_OK 0
@@ -67,6 +67,7 @@ typedef int mq_status;
 /* device status word bits (mq_read_device_status) */
 #define MQ_DEV_DESC_MISMATCH 1u  /* a kernel's device descriptor disagreed with its launch shape */
 #define MQ_DEV_DESC_ALIGN 2u     /* a device descriptor held a misaligned pointer */
+#define MQ_DEV_TIMEOUT 4u        /* a kernel's bounded wait on its copy pipeline gave up; outputs not written */
 
 /* quantization types (mq_concat_rows*) */
 #define MQ_TYPE_Q4_K 1
@@ -198,7 +199,11 @@ typedef struct mq_layer_desc {
     mq_ffn_desc ffn;
 } mq_layer_desc;
 
-#define MQ_STEP_PDL 1u   /* launch with programmatic dependent launch */
+#define MQ_STEP_PDL 1u         /* multi-kernel path: launch with programmatic dependent launch */
+#define MQ_STEP_PERSISTENT 2u  /* one persistent kernel for the whole stack (needs `workspace`) */
+
+/* bytes of device workspace the persistent step needs (grid-barrier words) */
+#define MQ_STEP_WORKSPACE_BYTES 256
 
 typedef struct mq_step_shape {
     int32_t n_layers;
@@ -209,8 +214,20 @@ typedef struct mq_step_shape {
     int32_t o_K;      /* K of o */
     int32_t ncols;
     uint32_t flags;   /* MQ_STEP_* */
+    void* workspace;  /* MQ_STEP_PERSISTENT: caller-owned device memory of
+                         MQ_STEP_WORKSPACE_BYTES, 4-byte aligned; zeroed by
+                         the call on its stream (so a captured graph re-zeroes
+                         it every replay); two steps that overlap on the GPU
+                         must not share it */
 } mq_step_shape;
 
+/* Without MQ_STEP_PERSISTENT: four launches per layer (qkv, o, gate/up, down).
+ * With it: a single cooperative launch of one CTA per SM that runs every
+ * layer, the weight stream running ahead across the dependency points, which
+ * are grid-wide barriers on `workspace` (bounded waits; a timeout records
+ * MQ_DEV_TIMEOUT).  Both give bit-identical outputs.  The persistent kernel
+ * needs every SM: it fails with MQ_ERR_CUDA if the device cannot host its
+ * whole grid at once. */
 mq_status mq_step(const mq_layer_desc* d_layers, const mq_step_shape* h_shape, void* stream);
 
 /* ---- test export ---------------------------------------------------------------------
@@ -219,6 +236,26 @@ mq_status mq_step(const mq_layer_desc* d_layers, const mq_step_shape* h_shape, v
  * sumq int32 [ncols][K/32] = sum q8 per block. */
 mq_status mq_debug_block_sums_q4K_q8_0(const mq_mv_desc* d_desc, int32_t rows, int32_t K, int32_t ncols,
                                        int32_t* sumi, int32_t* sumq, void* stream);
+
+/* Test-only setter of the kernel family used by later calls (process-wide,
+ * not thread-safe): MQ_VARIANT_AUTO (default) uses the bulk-copy ring kernels
+ * wherever their shared-memory plan fits and the register-streaming kernels
+ * elsewhere; MQ_VARIANT_FORCE_REGISTER always uses the register-streaming
+ * kernels.  Both give results within the same tolerance; a graph captured
+ * under one setting keeps it. */
+#define MQ_VARIANT_AUTO 0
+#define MQ_VARIANT_FORCE_REGISTER 1
+mq_status mq_debug_set_variant(int32_t policy);
+
+/* Test-only fault injection for later calls (process-wide, not thread-safe).
+ * MQ_FAULT_WITHHOLD_TILE: in the bulk-copy ring kernels the producer never
+ * delivers each CTA's last tile and every wait is limited to 50 ms, so the
+ * consumers' bounded waits run out: the kernels record MQ_DEV_TIMEOUT in the
+ * device status word, write no output and return; the GPU context stays
+ * usable.  MQ_FAULT_NONE restores normal operation. */
+#define MQ_FAULT_NONE 0
+#define MQ_FAULT_WITHHOLD_TILE 1
+mq_status mq_debug_set_fault(int32_t fault);
 
 #ifdef __cplusplus
 }

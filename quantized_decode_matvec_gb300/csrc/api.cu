@@ -12,6 +12,9 @@
 namespace mq {
 cudaError_t set_mv_attributes(int max_smem);
 cudaError_t set_gu_attributes(int max_smem);
+cudaError_t set_ring_attributes(int max_smem);
+cudaError_t set_step_attributes(int max_smem);
+void plan_ring(MvPlan& q, int64_t units, int kind, int nc, const DeviceInfo& dev);
 }  // namespace mq
 
 namespace {
@@ -19,6 +22,8 @@ namespace {
 constexpr int kMaxDevices = 64;
 mq::DeviceInfo g_dev[kMaxDevices];
 thread_local int g_last_cuda_error = 0;
+int g_variant_policy = mq::VARIANT_AUTO;  // set only through mq_debug_set_variant (tests)
+int g_fault_policy = mq::FAULT_NONE;       // set only through mq_debug_set_fault (tests)
 
 // Device status word (one per device that loads the library): kernels OR in
 // MQ_DEV_* bits when their device descriptor disagrees with their launch.
@@ -63,6 +68,9 @@ const DeviceInfo* current_device_info()
     return current_dev(&d) == MQ_OK ? d : nullptr;
 }
 
+int variant_policy() { return g_variant_policy; }
+int fault_policy() { return g_fault_policy; }
+
 bool plan_mv(int64_t rows, int K, int nc, int kind, int I, const DeviceInfo& dev, MvPlan* p)
 {
     MvPlan q = {};
@@ -101,7 +109,158 @@ bool plan_mv(int64_t rows, int K, int nc, int kind, int I, const DeviceInfo& dev
     q.grid = int(G);
     q.block = int(32 * nw);
     q.smem = int(smem);
+    q.variant = 0;
+    if (variant_policy() != VARIANT_FORCE_REGISTER) plan_ring(q, units, kind, nc, dev);
     *p = q;
+    return true;
+}
+
+// Bulk-copy ring plan on top of a register-streaming plan q (same rows per CTA,
+// same segments).  Leaves q unchanged when the ring does not apply.
+//  * consumers: nwc = nseg * floor(wmax/nseg) warps (wmax 15 for one column,
+//    8 for more), segment-stationary,
+//    rg = warps per segment * items per warp row-lanes;
+//  * tiles of T = 2*rg*m rows (about 24 KB), at most the CTA's rows rounded up;
+//  * 2..8 stages, within ~110 KB of shared memory when possible so that the
+//    next kernel's CTA fits beside this one under programmatic dependent launch.
+void plan_ring(MvPlan& q0, int64_t units, int kind, int nc, const DeviceInfo& dev)
+{
+    // work unit: half a super-block (128 weights); C counts units per row here
+    MvPlan q = q0;
+    q.C = q0.C / 2;
+    if (q.C <= 8) {
+        q.L = 8;
+        q.nseg = 1;
+    } else if (q.C <= 16) {
+        q.L = 16;
+        q.nseg = 1;
+    } else {
+        q.L = 32;
+        q.nseg = (q.C + 31) / 32;
+    }
+    q.S = (q.C + q.nseg - 1) / q.nseg;
+    q.nseg = (q.C + q.S - 1) / q.S;
+    const int wmax = (nc == 1) ? 15 : 8;  // consumer warps (the kernel's launch bound minus the producer)
+    if (q.nseg > wmax) return;
+    const int nwc = q.nseg * (wmax / q.nseg);
+    const int ipw = 32 / q.L;
+    const int rg = (nwc / q.nseg) * ipw;
+    const int64_t row_bytes = int64_t(q.C / 2) * 144;
+    // tiles of whole row pairs per row-lane (consumers take two rows per step)
+    const int64_t unit = 2 * rg * row_bytes;
+    int64_t m = (24576 + unit / 2) / unit;
+    if (m < 1) m = 1;
+    int64_t T = 2 * rg * m;
+    const int64_t rpc_round = (q.rows_per_cta + 2 * rg - 1) / (2 * rg) * (2 * rg);
+    if (T > rpc_round) T = rpc_round;
+    const int64_t stage = (T * row_bytes + 127) / 128 * 128;
+    const int64_t act = int64_t(nc) * q.C * 160;
+    const int64_t part = int64_t(q.rows_per_cta) * q.nseg * nc * 4;
+    const int64_t vals = (kind == KIND_GU) ? int64_t(nc) * q.rows_per_cta * 4 : 0;
+    const int64_t fixed = 256 + act + (part + 15) / 16 * 16 + vals;
+    const int64_t pair_budget = 110 * 1024;
+    // (the ring kernel also has a few bytes of static shared memory)
+    const int64_t budget = (fixed + 4 * stage <= pair_budget) ? pair_budget : dev.max_smem_optin - 256;
+    int64_t ns = (budget - fixed) / stage;
+    if (ns > 8) ns = 8;
+    if (ns < 2) return;
+    (void)units;
+    q.variant = 1;
+    q.fault = fault_policy();
+    q.wait_ms = q.fault == FAULT_NONE ? 2000 : 50;
+    q.nwc = nwc;
+    q.rg = rg;
+    q.T = int(T);
+    q.ns = int(ns);
+    q.stage_bytes = int(stage);
+    q.off_ring = 256;
+    q.off_act = int(q.off_ring + ns * stage);
+    q.off_part = int(q.off_act + act);
+    q.off_vals = int(q.off_part + (part + 15) / 16 * 16);
+    q.smem = int(q.off_vals + vals);
+    q.block = 32 * (nwc + 1);
+    q0 = q;
+}
+
+// Plan of the persistent step kernel.  Per phase the same unit split as the
+// per-matrix ring kernels (so results are bit-identical); one ring shared by
+// all phases: stages as large as the largest phase tile (about 64 KB: two rows
+// per row-lane), as many as fit beside the largest activation, partial and
+// gate/up buffers.
+bool plan_step(const mq_step_shape& h, const DeviceInfo& dev, StepPlan* out)
+{
+    StepPlan sp = {};
+    const int nc = h.ncols;
+    const int wmax = (nc == 1) ? 15 : 8;
+    const int64_t G = dev.num_sms;
+    const int kinds[4] = {KIND_MV, KIND_MV, KIND_GU, KIND_DOWN};
+    const int64_t Ks[4] = {h.H, h.o_K, h.H, h.I};
+    const int64_t Rs[4] = {h.qkv_rows, h.o_rows, h.I, h.H};
+    int64_t stage = 0, act = 0, part = 0, vals = 0;
+    for (int ph = 0; ph < 4; ++ph) {
+        MvPlan q = {};
+        q.C = int(Ks[ph] / 128);
+        if (q.C <= 8) {
+            q.L = 8;
+            q.nseg = 1;
+        } else if (q.C <= 16) {
+            q.L = 16;
+            q.nseg = 1;
+        } else {
+            q.L = 32;
+            q.nseg = (q.C + 31) / 32;
+        }
+        q.S = (q.C + q.nseg - 1) / q.nseg;
+        q.nseg = (q.C + q.S - 1) / q.S;
+        if (q.nseg > wmax) return false;
+        q.nwc = q.nseg * (wmax / q.nseg);
+        q.rg = (q.nwc / q.nseg) * (32 / q.L);
+        const bool gu = kinds[ph] == KIND_GU;
+        const int64_t units = gu ? Rs[ph] / 32 : Rs[ph];
+        const int64_t upc = (units + G - 1) / G;
+        const int64_t rpc = gu ? upc * 64 : upc;
+        const int64_t row_bytes = int64_t(q.C / 2) * 144;
+        const int64_t unit2 = 2 * int64_t(q.rg) * row_bytes;
+        int64_t m = 65536 / unit2;
+        if (m < 1) m = 1;
+        int64_t T = 2 * int64_t(q.rg) * m;
+        const int64_t rpc_round = (rpc + 2 * q.rg - 1) / (2 * q.rg) * (2 * q.rg);
+        if (T > rpc_round) T = rpc_round;
+        q.T = int(T);
+        q.rows_per_cta = int(rpc);
+        q.variant = 1;
+        q.fault = FAULT_NONE;
+        q.wait_ms = 2000;
+        const int64_t st = (T * row_bytes + 127) / 128 * 128;
+        if (st > stage) stage = st;
+        if (int64_t(nc) * q.C * 160 > act) act = int64_t(nc) * q.C * 160;
+        if (rpc * q.nseg * nc * 4 > part) part = rpc * q.nseg * nc * 4;
+        if (gu) vals = int64_t(nc) * rpc * 4;
+        sp.ph[ph] = q;
+        sp.K[ph] = int(Ks[ph]);
+        sp.R[ph] = int(Rs[ph]);
+    }
+    const int64_t fixed = 256 + act + (part + 15) / 16 * 16 + vals;
+    int64_t ns = (dev.max_smem_optin - 256 - fixed) / stage;  // the kernel has a few static bytes too
+    if (ns > 8) ns = 8;
+    if (ns < 2) return false;
+    const int off_ring = 256, off_act = int(256 + ns * stage), off_part = int(off_act + act);
+    const int off_vals = int(off_part + (part + 15) / 16 * 16);
+    for (int ph = 0; ph < 4; ++ph) {
+        MvPlan& q = sp.ph[ph];
+        q.ns = int(ns);
+        q.stage_bytes = int(stage);
+        q.off_ring = off_ring;
+        q.off_act = off_act;
+        q.off_part = off_part;
+        q.off_vals = off_vals;
+        q.grid = int(G);
+    }
+    sp.n_layers = h.n_layers;
+    sp.nwc = wmax;
+    sp.grid = int(G);
+    sp.smem = int(off_vals + vals);
+    *out = sp;
     return true;
 }
 
@@ -109,6 +268,8 @@ cudaError_t set_kernel_attributes(int max_smem)
 {
     cudaError_t e = set_mv_attributes(max_smem);
     if (e == cudaSuccess) e = set_gu_attributes(max_smem);
+    if (e == cudaSuccess) e = set_ring_attributes(max_smem);
+    if (e == cudaSuccess) e = set_step_attributes(max_smem);
     return e;
 }
 
@@ -131,6 +292,20 @@ const char* mq_status_string(mq_status s)
 }
 
 int mq_abi_version(void) { return MQ_ABI_VERSION; }
+
+mq_status mq_debug_set_fault(int32_t fault)
+{
+    if (fault != mq::FAULT_NONE && fault != mq::FAULT_WITHHOLD_TILE) return MQ_ERR_INVALID_ARG;
+    g_fault_policy = fault;
+    return MQ_OK;
+}
+
+mq_status mq_debug_set_variant(int32_t policy)
+{
+    if (policy != mq::VARIANT_AUTO && policy != mq::VARIANT_FORCE_REGISTER) return MQ_ERR_INVALID_ARG;
+    g_variant_policy = policy;
+    return MQ_OK;
+}
 
 int mq_last_cuda_error(void) { return g_last_cuda_error; }
 
@@ -362,10 +537,20 @@ mq_status mq_step(const mq_layer_desc* d_layers, const mq_step_shape* h, void* s
     if ((st = check_mv_shape(h->o_rows, h->o_K, h->ncols)) != MQ_OK) return st;
     if ((st = check_ffn_shape(h->H, h->I, h->ncols)) != MQ_OK) return st;
     if (h->qkv_rows == 0 || h->o_rows == 0) return MQ_ERR_SHAPE;
+    if (h->flags & MQ_STEP_PERSISTENT) {
+        if (!h->workspace) return MQ_ERR_INVALID_ARG;
+        if (!aligned(h->workspace, 4)) return MQ_ERR_ALIGN;
+    }
     const mq::DeviceInfo* dev = nullptr;
     if ((st = current_dev(&dev)) != MQ_OK) return st;
     const bool pdl = (h->flags & MQ_STEP_PDL) != 0;
     const cudaStream_t s = as_stream(stream);
+    if (h->flags & MQ_STEP_PERSISTENT) {
+        mq::StepPlan sp;
+        if (!mq::plan_step(*h, *dev, &sp)) return MQ_ERR_UNSUPPORTED;
+        cudaError_t e = mq::launch_step(d_layers, sp, h->ncols, dev->status, static_cast<unsigned*>(h->workspace), s);
+        return e == cudaSuccess ? MQ_OK : cuda_fail(e);
+    }
     // one plan per projection, decided once for the whole stack
     mq::MvPlan p_qkv, p_o, p_gu, p_down;
     if (!mq::plan_mv(h->qkv_rows, h->H, h->ncols, mq::KIND_MV, 0, *dev, &p_qkv) ||

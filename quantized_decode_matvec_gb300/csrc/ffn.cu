@@ -1,5 +1,6 @@
 // ffn.cu -- gate/up matvec over the concatenated ffn_gu weight with the
-// SwiGLU product and the q8_0 re-quantization of h fused into the epilogue.
+// SwiGLU product and the q8_0 re-quantization of h fused into the epilogue
+// (register-streaming variant; the bulk-copy ring variant is in ring.cu).
 //
 // "04 . 8o -- Killing the CPU stall at decode start", sections 1 and 3.1:
 // gate and up weights are concatenated row-wise into ffn_gu (gate rows
@@ -7,6 +8,8 @@
 // of h: 32*k consecutive intermediate indices i, i.e. gate rows i and up rows
 // I+i, so SiLU(g)*u and the amax of each 32-block of h are formed in shared
 // memory and h leaves the kernel already as q8_0 for the down projection.
+#include "mq_epilogue.cuh"
+#include "mq_job.cuh"
 #include "mq_stream.cuh"
 
 namespace mq {
@@ -17,25 +20,15 @@ __global__ void __launch_bounds__(512, 1)
 {
     griddep_wait();
     extern __shared__ uint4 smem[];
+    const unsigned bad = check_ffn_gu(d, H_h, I_h, NC);
+    if (bad) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(status, bad);
+        return;
+    }
     const uint8_t* W = static_cast<const uint8_t*>(d->W_gu);
     const float* x = d->x;
     const uint8_t* xq = static_cast<const uint8_t*>(d->xq);
-    uint8_t* hq = static_cast<uint8_t*>(d->h_q8);
-    float* gu_dbg = d->gu_dbg;
-    float* h_dbg = d->h_dbg;
-    const int H = d->H, I = d->I, nc = d->ncols;
-    {
-        unsigned bad = 0;
-        if (H != H_h || I != I_h || nc != NC) bad |= MQ_DEV_DESC_MISMATCH;
-        if ((reinterpret_cast<uintptr_t>(W) & 15) || (reinterpret_cast<uintptr_t>(hq) & 1) || !W || !hq ||
-            (x && (reinterpret_cast<uintptr_t>(x) & 3)) || (!x && (!xq || (reinterpret_cast<uintptr_t>(xq) & 1))) ||
-            (reinterpret_cast<uintptr_t>(gu_dbg) & 3) || (reinterpret_cast<uintptr_t>(h_dbg) & 3))
-            bad |= MQ_DEV_DESC_ALIGN;
-        if (bad) {
-            if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(status, bad);
-            return;
-        }
-    }
+    const int H = d->H, I = d->I;
     const int G = gridDim.x;
     const int nblk = I / kQK8;
     const int b0 = int(int64_t(blockIdx.x) * nblk / G), b1 = int(int64_t(blockIdx.x + 1) * nblk / G);
@@ -49,43 +42,19 @@ __global__ void __launch_bounds__(512, 1)
     mv_stream<NC, 2>(
         W, row_bytes, [=](int lr) { return lr < n ? i0 + lr : I + i0 + (lr - n); }, nrows, p, act, part, [&]() {
             if (x)
-                stage_x_quantize<NC>(x, H, act, nullptr);
+                stage_x_quantize<NC>(x, H, act, nullptr, threadIdx.x, blockDim.x);
             else
-                stage_q8_global<NC>(xq, H, act, nullptr);
+                stage_q8_global<NC>(xq, H, act, nullptr, threadIdx.x, blockDim.x);
         });
     __syncthreads();
     griddep_launch_dependents();
-    for (int t = threadIdx.x; t < NC * nrows; t += blockDim.x) {
-        const int c = t / nrows, lr = t - c * nrows;
-        float s = 0.0f;
-        for (int g = 0; g < p.nseg; ++g) s += part[(lr * p.nseg + g) * NC + c];
-        vals[t] = s;
-        if (gu_dbg) gu_dbg[size_t(c) * 2 * I + (lr < n ? i0 + lr : I + i0 + (lr - n))] = s;
-    }
-    __syncthreads();
-
-    // h = SiLU(g) * u = g / (1 + exp(-g)) * u, then q8_0 per 32 indices
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, NW = blockDim.x >> 5;
-    const int nb = n / kQK8;
-    for (int t = warp; t < NC * nb; t += NW) {
-        const int c = t / nb, k = t - c * nb;
-        const int i = k * kQK8 + lane;
-        const float g = vals[size_t(c) * nrows + i];
-        const float u = vals[size_t(c) * nrows + n + i];
-        const float h = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
-        float dd;
-        const int q = q8_quantize_lane(h, &dd);
-        const __half dh = __float2half_rn(dd);
-        uint8_t* ob = hq + (size_t(c) * nblk + b0 + k) * kQ8Bytes;
-        if (lane == 0) *reinterpret_cast<uint16_t*>(ob) = __half_as_ushort(dh);
-        ob[2 + lane] = uint8_t(int8_t(q));
-        if (h_dbg) h_dbg[size_t(c) * I + i0 + i] = h;
-    }
+    gu_epilogue<NC>(part, vals, p.nseg, n, i0, I, static_cast<uint8_t*>(d->h_q8), d->gu_dbg, d->h_dbg);
 }
 
 cudaError_t launch_gu(const mq_ffn_desc* d, int H, int I, int ncols, const MvPlan& p, unsigned* status,
                       cudaStream_t s, bool pdl)
 {
+    if (p.variant == 1) return launch_ring(d, KIND_GU, H, I, ncols, p, status, s, pdl);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.grid);
     cfg.blockDim = dim3(p.block);
@@ -109,7 +78,7 @@ cudaError_t set_gu_attributes(int max_smem)
 {
     cudaError_t e = cudaSuccess;
 #define MQ_SET(N) \
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(gu_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    if (e == cudaSuccess) e = set_max_dyn_smem(reinterpret_cast<const void*>(gu_kernel<N>), max_smem);
     MQ_SET(1) MQ_SET(2) MQ_SET(3) MQ_SET(4) MQ_SET(5) MQ_SET(6) MQ_SET(7) MQ_SET(8)
 #undef MQ_SET
     return e;

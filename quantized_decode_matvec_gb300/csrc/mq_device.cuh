@@ -70,14 +70,15 @@ struct ActSmem {
     int C;  // chunks per row = K/64
 };
 
-// From q8_0 blocks in global memory (34-byte blocks, 2-byte aligned).
-// sumq_out (nullable, test export): int32 [NC][K/32] block sums of the codes.
+// From q8_0 blocks in global memory (34-byte blocks, 2-byte aligned), by
+// threads tid = 0..nthr-1.  sumq_out (nullable, test export): int32
+// [NC][K/32] block sums of the codes.
 template <int NC>
 __device__ __forceinline__ void stage_q8_global(const uint8_t* __restrict__ xq, int K, ActSmem s,
-                                                int32_t* sumq_out)
+                                                int32_t* sumq_out, int tid, int nthr)
 {
     const int nq = K / kQK8;
-    for (int t = threadIdx.x; t < NC * nq; t += blockDim.x) {
+    for (int t = tid; t < NC * nq; t += nthr) {
         const int c = t / nq, J = t - c * nq;
         const uint16_t* h = reinterpret_cast<const uint16_t*>(xq + (size_t(c) * nq + J) * kQ8Bytes);
         uint16_t v[17];
@@ -105,14 +106,14 @@ __device__ __forceinline__ void stage_q8_global(const uint8_t* __restrict__ xq, 
 // stand-alone quantizer) straight into shared memory.  One warp per block;
 // each warp first issues the loads of up to 8 blocks, then quantizes them,
 // so the L2 latency is paid once per 8 blocks.  xq_out (nullable) receives
-// the 34-byte blocks.
+// the 34-byte blocks.  Run by whole warps tid = 0..nthr-1 (nthr % 32 == 0).
 template <int NC>
 __device__ __forceinline__ void stage_x_quantize(const float* __restrict__ x, int K, ActSmem s,
-                                                 uint8_t* __restrict__ xq_out)
+                                                 uint8_t* __restrict__ xq_out, int tid, int nthr)
 {
     constexpr int B = 8;
     const int nq = K / kQK8;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int lane = tid & 31, warp = tid >> 5, nw = nthr >> 5;
     const int total = NC * nq;
     for (int t0 = warp * B; t0 < total; t0 += nw * B) {
         float v[B];
@@ -173,55 +174,85 @@ __device__ __forceinline__ void load_chunk(Chunk& k, const uint8_t* sb, int c4)
 // Scale bytes s[0..11] are h.y (s0..s3), h.z (s4..s7), h.w (s8..s11).
 // j < 4: sc = s[j] & 63, m = s[j+4] & 63.
 // j >= 4: sc = (s[j+4] & 15) | (s[j-4] >> 6) << 4, m = (s[j+4] >> 4) | (s[j] >> 6) << 4.
+// Branch-free (c4 differs across the lanes of a warp): both forms are
+// computed and one is selected.  fd1 comes out divided by 16 (exact, a power
+// of two) to match chunk_dot's s1x16.
 __device__ __forceinline__ void chunk_scales(const uint4& h, int c4, float& fd0, float& fd1, float& fm0,
                                              float& fm1)
 {
     const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&h.x));
-    uint32_t scw, mw;
-    if (c4 < 2) {
-        scw = h.y & 0x3f3f3f3fu;
-        mw = h.z & 0x3f3f3f3fu;
-    } else {
-        scw = (h.w & 0x0f0f0f0fu) | ((h.y >> 2) & 0x30303030u);
-        mw = ((h.w >> 4) & 0x0f0f0f0fu) | ((h.z >> 2) & 0x30303030u);
-    }
-    const int sh = (c4 & 1) * 16;
-    fd0 = dd.x * float((scw >> sh) & 0xffu);
-    fd1 = dd.x * float((scw >> (sh + 8)) & 0xffu);
-    fm0 = dd.y * float((mw >> sh) & 0xffu);
-    fm1 = dd.y * float((mw >> (sh + 8)) & 0xffu);
+    const uint32_t sc_lo = h.y & 0x3f3f3f3fu;
+    const uint32_t m_lo = h.z & 0x3f3f3f3fu;
+    const uint32_t sc_hi = (h.w & 0x0f0f0f0fu) | ((h.y >> 2) & 0x30303030u);
+    const uint32_t m_hi = ((h.w >> 4) & 0x0f0f0f0fu) | ((h.z >> 2) & 0x30303030u);
+    const bool upper = c4 >= 2;
+    const uint32_t scw = upper ? sc_hi : sc_lo;
+    const uint32_t mw = upper ? m_hi : m_lo;
+    // bytes j0 and j1 of the selected words (j0 = 2*(c4 & 1) within the word)
+    const uint32_t sel = (c4 & 1) ? 0x4442u : 0x4440u;  // byte_perm: byte 2 or 0 into byte 0, zero elsewhere
+    const uint32_t sel1 = (c4 & 1) ? 0x4443u : 0x4441u;
+    fd0 = dd.x * float(__byte_perm(scw, 0u, sel));
+    fd1 = (dd.x * 0.0625f) * float(__byte_perm(scw, 0u, sel1));
+    fm0 = dd.y * float(__byte_perm(mw, 0u, sel));
+    fm1 = dd.y * float(__byte_perm(mw, 0u, sel1));
+}
+
+// unsigned bytes of a times signed bytes of b, summed into c (PTX dp4a.u32.s32)
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c)
+{
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
 }
 
 // Exact int32 dot products of the chunk's quants with the activation codes:
-// s0 = sum over the 32 elements of block j0 of q4 * q8, s1 likewise for j1.
+// s0 = sum over the 32 elements of block j0 of q4 * q8 (low nibbles), and
+// s1x16 = 16 * (the same for j1): the high nibbles are used in place, masked
+// but not shifted, as unsigned bytes (16*q), so s1 = s1x16 / 16 exactly.
+// Two accumulators per block keep the dependent dp4a chains short.
 // p0..p3 are the four activation planes of this chunk.
 __device__ __forceinline__ void chunk_dot(const Chunk& k, const uint4& p0, const uint4& p1, const uint4& p2,
-                                          const uint4& p3, int& s0, int& s1)
+                                          const uint4& p3, int& s0, int& s1x16)
 {
-    const uint32_t m4 = 0x0f0f0f0fu;
-    int a = 0, b = 0;
-    a = __dp4a(int(k.a.x & m4), int(p0.x), a);
-    a = __dp4a(int(k.a.y & m4), int(p0.y), a);
-    a = __dp4a(int(k.a.z & m4), int(p0.z), a);
-    a = __dp4a(int(k.a.w & m4), int(p0.w), a);
-    a = __dp4a(int(k.b.x & m4), int(p1.x), a);
-    a = __dp4a(int(k.b.y & m4), int(p1.y), a);
-    a = __dp4a(int(k.b.z & m4), int(p1.z), a);
-    a = __dp4a(int(k.b.w & m4), int(p1.w), a);
-    b = __dp4a(int((k.a.x >> 4) & m4), int(p2.x), b);
-    b = __dp4a(int((k.a.y >> 4) & m4), int(p2.y), b);
-    b = __dp4a(int((k.a.z >> 4) & m4), int(p2.z), b);
-    b = __dp4a(int((k.a.w >> 4) & m4), int(p2.w), b);
-    b = __dp4a(int((k.b.x >> 4) & m4), int(p3.x), b);
-    b = __dp4a(int((k.b.y >> 4) & m4), int(p3.y), b);
-    b = __dp4a(int((k.b.z >> 4) & m4), int(p3.z), b);
-    b = __dp4a(int((k.b.w >> 4) & m4), int(p3.w), b);
-    s0 = a;
-    s1 = b;
+    const uint32_t lo = 0x0f0f0f0fu, hi = 0xf0f0f0f0u;
+    int a0 = 0, a1 = 0, b0 = 0, b1 = 0;
+    a0 = dp4a_us(k.a.x & lo, p0.x, a0);
+    a1 = dp4a_us(k.b.x & lo, p1.x, a1);
+    b0 = dp4a_us(k.a.x & hi, p2.x, b0);
+    b1 = dp4a_us(k.b.x & hi, p3.x, b1);
+    a0 = dp4a_us(k.a.y & lo, p0.y, a0);
+    a1 = dp4a_us(k.b.y & lo, p1.y, a1);
+    b0 = dp4a_us(k.a.y & hi, p2.y, b0);
+    b1 = dp4a_us(k.b.y & hi, p3.y, b1);
+    a0 = dp4a_us(k.a.z & lo, p0.z, a0);
+    a1 = dp4a_us(k.b.z & lo, p1.z, a1);
+    b0 = dp4a_us(k.a.z & hi, p2.z, b0);
+    b1 = dp4a_us(k.b.z & hi, p3.z, b1);
+    a0 = dp4a_us(k.a.w & lo, p0.w, a0);
+    a1 = dp4a_us(k.b.w & lo, p1.w, a1);
+    b0 = dp4a_us(k.a.w & hi, p2.w, b0);
+    b1 = dp4a_us(k.b.w & hi, p3.w, b1);
+    s0 = a0 + a1;
+    s1x16 = b0 + b1;
 }
 
-// acc[c] += this chunk's contribution for every column:
-// dq_j0*(d*sc_j0*s0 - dmin*m_j0*sumq_j0) + (same for j1).
+// One column's contribution of a chunk:
+// dq_j0*(d*sc_j0*s0 - dmin*m_j0*sumq_j0) + (same for j1), with fd0..fm1 from
+// chunk_scales (fd1 pre-divided by 16 for s1x16).
+__device__ __forceinline__ float chunk_column(const Chunk& k, float fd0, float fd1, float fm0, float fm1,
+                                              const uint4& p0, const uint4& p1, const uint4& p2, const uint4& p3,
+                                              const float4& sc, float acc)
+{
+    int s0, s1x16;
+    chunk_dot(k, p0, p1, p2, p3, s0, s1x16);
+    acc = fmaf(fd0, sc.x * float(s0), acc);
+    acc = fmaf(fd1, sc.y * float(s1x16), acc);  // fd1 carries the 1/16
+    acc = fmaf(-fm0, sc.z, acc);
+    acc = fmaf(-fm1, sc.w, acc);
+    return acc;
+}
+
+// acc[c] += this chunk's contribution for every column, activation from shared memory
 template <int NC>
 __device__ __forceinline__ void chunk_accumulate(const Chunk& k, int c4, int ch, const ActSmem& s, float acc[NC])
 {
@@ -230,17 +261,21 @@ __device__ __forceinline__ void chunk_accumulate(const Chunk& k, int c4, int ch,
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
         const uint4* P = s.planes + size_t(c * 4) * s.C + ch;
-        const uint4 p0 = P[0], p1 = P[s.C], p2 = P[2 * s.C], p3 = P[3 * s.C];
-        const float4 sc = s.scales[size_t(c) * s.C + ch];
-        int s0, s1;
-        chunk_dot(k, p0, p1, p2, p3, s0, s1);
-        float t = acc[c];
-        t = fmaf(fd0, sc.x * float(s0), t);
-        t = fmaf(fd1, sc.y * float(s1), t);
-        t = fmaf(-fm0, sc.z, t);
-        t = fmaf(-fm1, sc.w, t);
-        acc[c] = t;
+        acc[c] = chunk_column(k, fd0, fd1, fm0, fm1, P[0], P[s.C], P[2 * s.C], P[3 * s.C],
+                              s.scales[size_t(c) * s.C + ch], acc[c]);
     }
+}
+
+// the same with this chunk's activation held in registers (one lane, fixed chunk)
+template <int NC>
+__device__ __forceinline__ void chunk_accumulate_regs(const Chunk& k, int c4, const uint4 (&P)[NC][4],
+                                                      const float4 (&SC)[NC], float acc[NC])
+{
+    float fd0, fd1, fm0, fm1;
+    chunk_scales(k.h, c4, fd0, fd1, fm0, fm1);
+#pragma unroll
+    for (int c = 0; c < NC; ++c)
+        acc[c] = chunk_column(k, fd0, fd1, fm0, fm1, P[c][0], P[c][1], P[c][2], P[c][3], SC[c], acc[c]);
 }
 
 }  // namespace mq

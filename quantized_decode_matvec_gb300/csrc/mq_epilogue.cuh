@@ -1,0 +1,74 @@
+// mq_epilogue.cuh -- what a CTA does after its rows are streamed: the fixed-
+// order combine of the per-segment partial sums, and for the gate/up kernel
+// the SwiGLU product and the q8_0 re-quantization of h.
+#pragma once
+
+#include "mq_device.cuh"
+
+namespace mq {
+
+// y[c][r0 + lr] = sum over segments, in segment order, of part[(lr*nseg+seg)*NC + c]
+template <int NC>
+__device__ __forceinline__ void mv_epilogue(const float* __restrict__ part, int nseg, int nrows, int r0,
+                                            float* __restrict__ y, int y_ld, int tid, int nthr)
+{
+    for (int t = tid; t < NC * nrows; t += nthr) {
+        const int c = t / nrows, lr = t - c * nrows;
+        float s = 0.0f;
+        for (int g = 0; g < nseg; ++g) s += part[(lr * nseg + g) * NC + c];
+        y[size_t(c) * y_ld + r0 + lr] = s;
+    }
+}
+
+// Gate/up epilogue ("04 . 8o", sections 1 and 3.1: gate rows first in ffn_gu).
+// Local rows 0..n-1 are gate rows i0.., rows n..2n-1 the up rows I+i0..; n is a
+// multiple of 32, so the CTA owns whole q8_0 blocks of h (block indices
+// b0 .. b0 + n/32 - 1 of each column).  Called by all threads of the CTA.
+// Runs on threads tid = 0..nthr-1 (whole warps); `sync` is a barrier over
+// exactly those threads.
+template <int NC, typename SyncFn>
+__device__ __forceinline__ void gu_epilogue_on(const float* __restrict__ part, float* __restrict__ vals, int nseg,
+                                               int n, int i0, int I, uint8_t* __restrict__ hq,
+                                               float* __restrict__ gu_dbg, float* __restrict__ h_dbg, int tid,
+                                               int nthr, SyncFn sync)
+{
+    const int nrows = 2 * n;
+    const int nblk = I / kQK8, b0 = i0 / kQK8;
+    for (int t = tid; t < NC * nrows; t += nthr) {
+        const int c = t / nrows, lr = t - c * nrows;
+        float s = 0.0f;
+        for (int g = 0; g < nseg; ++g) s += part[(lr * nseg + g) * NC + c];
+        vals[t] = s;
+        if (gu_dbg) gu_dbg[size_t(c) * 2 * I + (lr < n ? i0 + lr : I + i0 + (lr - n))] = s;
+    }
+    sync();
+    // h = SiLU(g) * u = g / (1 + exp(-g)) * u, then q8_0 per 32 indices
+    const int lane = tid & 31, warp = tid >> 5, NW = nthr >> 5;
+    const int nb = n / kQK8;
+    for (int t = warp; t < NC * nb; t += NW) {
+        const int c = t / nb, k = t - c * nb;
+        const int i = k * kQK8 + lane;
+        const float g = vals[size_t(c) * nrows + i];
+        const float u = vals[size_t(c) * nrows + n + i];
+        const float h = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+        float dd;
+        const int q = q8_quantize_lane(h, &dd);
+        const __half dh = __float2half_rn(dd);
+        uint8_t* ob = hq + (size_t(c) * nblk + b0 + k) * kQ8Bytes;
+        if (lane == 0) *reinterpret_cast<uint16_t*>(ob) = __half_as_ushort(dh);
+        ob[2 + lane] = uint8_t(int8_t(q));
+        if (h_dbg) h_dbg[size_t(c) * I + i0 + i] = h;
+    }
+}
+
+// the whole CTA
+template <int NC>
+__device__ __forceinline__ void gu_epilogue(const float* __restrict__ part, float* __restrict__ vals, int nseg,
+                                            int n, int i0, int I, uint8_t* __restrict__ hq,
+                                            float* __restrict__ gu_dbg, float* __restrict__ h_dbg)
+{
+    gu_epilogue_on<NC>(part, vals, nseg, n, i0, I, hq, gu_dbg, h_dbg, threadIdx.x, blockDim.x,
+                       []() { __syncthreads(); });
+}
+
+}  // namespace mq

@@ -17,14 +17,44 @@ struct MvPlan {
     int C;             // chunks (64 weights) per row = K/64
     int L;             // lanes per work item: 8, 16 or 32
     int nseg;          // K segments per row (one work item = one row segment)
-    int S;             // chunks per segment (<= L)
+    int S;             // chunks per segment (<= L, a multiple of 4)
     int rows_per_cta;  // max rows handled by one CTA
     int grid;          // CTAs
     int block;         // threads per CTA
     int smem;          // dynamic shared memory bytes
+    // bulk-copy ring variant (variant == 1)
+    int variant;       // 0: register-streaming kernels, 1: bulk-copy ring kernels
+    int nwc;           // consumer warps (one more warp is the producer)
+    int rg;            // row-lanes per segment: consumer rows advance by rg
+    int T;             // rows per tile (a multiple of rg)
+    int ns;            // ring stages
+    int stage_bytes;   // bytes per stage (128-byte multiple)
+    int off_ring, off_act, off_part, off_vals;  // shared-memory offsets
+    int fault;         // test-only: FAULT_* injected by the ring kernels (0 = none)
+    int wait_ms;       // limit of every mbarrier wait of the ring kernels
 };
 
+// Plan of the persistent step kernel: one ring plan per phase (qkv, o, gate/up,
+// down) sharing the ring geometry and shared-memory layout of ph[0].
+struct StepPlan {
+    MvPlan ph[4];
+    int K[4];      // reduction length per phase
+    int R[4];      // rows per phase (gate/up: I)
+    int n_layers;
+    int nwc;       // consumer warps of the kernel (phases may use fewer)
+    int grid;
+    int smem;
+};
+
+// test-only fault injection (mq_debug_set_fault)
+enum Fault { FAULT_NONE = 0, FAULT_WITHHOLD_TILE = 1 };
+int fault_policy();
+
 enum Kind { KIND_MV = 0, KIND_DOWN = 1, KIND_GU = 2 };
+
+// kernel family selection (test hook; 0 = automatic)
+enum VariantPolicy { VARIANT_AUTO = 0, VARIANT_FORCE_REGISTER = 1 };
+int variant_policy();
 
 struct DeviceInfo {
     int num_sms = 0;
@@ -40,13 +70,31 @@ const DeviceInfo* current_device_info();
 bool plan_mv(int64_t rows, int K, int ncols, int kind, int I, const DeviceInfo& dev, MvPlan* p);
 
 cudaError_t launch_quantize(const float* x, void* xq, int64_t nblocks, cudaStream_t s);
+// launch_mv / launch_gu dispatch on p.variant
 cudaError_t launch_mv(const void* desc, int kind, int rows, int K, int ncols, const MvPlan& p,
                       unsigned* status, cudaStream_t s, bool pdl);
 cudaError_t launch_gu(const mq_ffn_desc* d, int H, int I, int ncols, const MvPlan& p, unsigned* status,
                       cudaStream_t s, bool pdl);
+cudaError_t launch_ring(const void* desc, int kind, int a, int b, int ncols, const MvPlan& p, unsigned* status,
+                        cudaStream_t s, bool pdl);
+bool plan_step(const mq_step_shape& h, const DeviceInfo& dev, StepPlan* sp);
+cudaError_t launch_step(const mq_layer_desc* layers, const StepPlan& sp, int ncols, unsigned* status, unsigned* ws,
+                        cudaStream_t s);
 cudaError_t launch_block_sums(const mq_mv_desc* d, int rows, int K, int ncols, int32_t* sumi, int32_t* sumq,
                               int smem, unsigned* status, cudaStream_t s);
 // raises the dynamic shared memory limit of every kernel on the current device
 cudaError_t set_kernel_attributes(int max_smem);
 
+}  // namespace mq
+
+namespace mq {
+// Raise a kernel's dynamic shared-memory limit to the device's opt-in maximum
+// minus the kernel's own static shared memory.
+inline cudaError_t set_max_dyn_smem(const void* func, int max_optin)
+{
+    cudaFuncAttributes a;
+    cudaError_t e = cudaFuncGetAttributes(&a, func);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin - int(a.sharedSizeBytes));
+}
 }  // namespace mq

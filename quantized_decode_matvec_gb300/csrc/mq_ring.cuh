@@ -1,0 +1,166 @@
+// mq_ring.cuh -- consumer side of the bulk-copy weight ring, shared by the
+// per-matrix ring kernels (ring.cu) and the persistent step kernel (step.cu).
+#pragma once
+
+#include "mq_internal.h"
+#include "mq_tma.cuh"
+#include "mq_unit.cuh"
+
+namespace mq {
+
+// consumer warps + the producer warp: 15 + 1 for one column; 8 + 1 for more
+// columns, which need more registers per thread (activation and
+// accumulators).  The register file is split between the SM's four
+// schedulers, so the busiest scheduler's warp count sets the per-thread
+// budget: 16 warps (4 per scheduler) allow 128 registers, 17 only 96.
+template <int NC>
+constexpr int ring_max_warps()
+{
+    return NC == 1 ? 16 : 9;
+}
+constexpr int ring_max_consumers(int nc) { return nc == 1 ? 15 : 8; }
+
+// Sum of v over the L lanes of each lane group, into every lane of the group.
+template <int L>
+__device__ __forceinline__ float group_sum(float v)
+{
+#pragma unroll
+    for (int off = L >> 1; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+// Two rows' partials a, b reduced over the L lanes of each group in one tree:
+// afterwards lanes l < L/2 hold row a's sum, lanes l >= L/2 row b's.
+template <int L>
+__device__ __forceinline__ float group_sum2(float a, float b, int l)
+{
+    const bool upper = l >= (L >> 1);
+    float keep = upper ? b : a;
+    const float send = upper ? a : b;
+    keep += __shfl_xor_sync(0xffffffffu, send, L >> 1);
+#pragma unroll
+    for (int off = L >> 2; off > 0; off >>= 1) keep += __shfl_xor_sync(0xffffffffu, keep, off);
+    return keep;
+}
+
+// Consumer side of the ring, for L lanes per item.  A lane always works on the
+// same unit u of every row (segment-stationary warps), so its 128 activation
+// codes and scales stay in registers (ncols <= 2; from shared memory above).
+// Each iteration takes two rows of the tile (r + sub and r + rg + sub): two
+// independent dp4a chains per lane and one shuffle tree for both rows.
+// Returns false if a wait timed out.
+// What a consumer needs of a ring plan, by value: a non-inlined callee that
+// took the plan by reference would read it through local memory.
+struct ConsumeArgs {
+    int C, L, nseg, S, rg, T, ns, stage_bytes;
+    int nrows;      // the CTA's rows of this matrix
+    int tile_base;  // ring position of the matrix's first tile
+    int nwc_used;   // consumer warps with work (the others only hand tiles back)
+};
+
+__device__ __forceinline__ ConsumeArgs consume_args(const MvPlan& p, int nrows, int tile_base, int nwc_used)
+{
+    return ConsumeArgs{p.C, p.L, p.nseg, p.S, p.rg, p.T, p.ns, p.stage_bytes, nrows, tile_base, nwc_used};
+}
+
+// (not inlined: called once per matrix, it keeps its own register allocation
+// instead of adding to the caller's)
+template <int NC, int L>
+__device__ __noinline__ bool ring_consume_L(const ConsumeArgs p, const uint8_t* ring, uint64_t* full,
+                                            uint64_t* empty, const UnitAct act, float* __restrict__ part,
+                                            uint64_t limit_ns)
+{
+    const int nrows = p.nrows, tile_base = p.tile_base, nwc_used = p.nwc_used;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nseg = p.nseg;
+    const int seg = warp % nseg, jj = warp / nseg;
+    constexpr int ipw = 32 / L;
+    const int sub = lane / L, l = lane - sub * L;
+    const int rho0 = jj * ipw;  // first row-lane of this warp
+    const int rg = p.rg;
+    const int u = seg * p.S + l;  // this lane's unit of every row
+    // warps beyond nwc_used have no work in this matrix but still take part in
+    // every tile's full/empty handshake, so the stage counts stay exact
+    const bool warp_active = warp < nwc_used;
+    const bool on = warp_active && (l < p.S) && (u < p.C);
+    const bool upper = (u & 1) != 0;
+    const uint32_t row_bytes = uint32_t(p.C / 2) * kQ4KBytes;
+    const uint32_t off_h = uint32_t(u >> 1) * kQ4KBytes;
+    const uint32_t off_q = off_h + 16 + 64 * (u & 1);
+
+    constexpr bool kRegAct = NC <= 2;
+    uint4 A[NC][8];
+    float4 DQ[NC], DQSQ[NC];
+    auto load_act = [&](int c, int slot) {  // column c's codes and scales into A[slot], DQ[slot], DQSQ[slot]
+#pragma unroll
+        for (int k = 0; k < 8; ++k) A[slot][k] = act.planes[size_t(c * 8 + k) * act.U + u];
+        DQ[slot] = act.scales[(size_t(c) * act.U + u) * 2];
+        DQSQ[slot] = act.scales[(size_t(c) * act.U + u) * 2 + 1];
+    };
+    if (kRegAct && on) {
+#pragma unroll
+        for (int c = 0; c < NC; ++c) load_act(c, c);
+    }
+    auto load_w = [&](const uint8_t* stage, int rr, UnitW& w) {
+        const uint8_t* rb = stage + uint32_t(rr) * row_bytes;
+        w.h = lds16(rb + off_h);
+        w.qa0 = lds16(rb + off_q);
+        w.qb0 = lds16(rb + off_q + 16);
+        w.qa1 = lds16(rb + off_q + 32);
+        w.qb1 = lds16(rb + off_q + 48);
+    };
+
+    const int ntiles = (nrows + p.T - 1) / p.T;
+    for (int i = 0; i < ntiles; ++i) {
+        const int gi = tile_base + i;  // position in the ring's tile sequence
+        const int s = gi % p.ns;
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], uint32_t(gi / p.ns) & 1u, limit_ns));
+        if (!ok) return false;
+        const uint8_t* stage = ring + uint32_t(s) * uint32_t(p.stage_bytes);
+        const int tr0 = i * p.T, tn = min(p.T, nrows - tr0);
+        for (int r = warp_active ? rho0 : tn; r < tn; r += 2 * rg) {
+            const int ra = r + sub, rb = r + rg + sub;
+            const bool va = on && ra < tn, vb = on && rb < tn;
+            float acc_a[NC], acc_b[NC];
+#pragma unroll
+            for (int c = 0; c < NC; ++c) acc_a[c] = acc_b[c] = 0.0f;
+            if (va || vb) {
+                UnitW wa, wb;
+                load_w(stage, va ? ra : rb, wa);
+                load_w(stage, vb ? rb : ra, wb);
+                float fda[4], fma_[4], fdb[4], fmb[4];
+                unit_scales(wa.h, upper, fda, fma_);
+                unit_scales(wb.h, upper, fdb, fmb);
+#pragma unroll
+                for (int c = 0; c < NC; ++c) {
+                    if (!kRegAct) load_act(c, 0);
+                    const int cc = kRegAct ? c : 0;
+                    if (va) acc_a[c] = unit_column(wa, fda, fma_, A[cc], DQ[cc], DQSQ[cc], 0.0f);
+                    if (vb) acc_b[c] = unit_column(wb, fdb, fmb, A[cc], DQ[cc], DQSQ[cc], 0.0f);
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                const float t = group_sum2<L>(acc_a[c], acc_b[c], l);
+                if (l == 0 && ra < tn) part[((tr0 + ra) * nseg + seg) * NC + c] = t;
+                if (l == (L >> 1) && rb < tn) part[((tr0 + rb) * nseg + seg) * NC + c] = t;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    return true;
+}
+
+template <int NC>
+__device__ __forceinline__ bool ring_consume(const MvPlan& p, int nrows, int tile_base, int nwc_used,
+                                             const uint8_t* ring, uint64_t* full, uint64_t* empty,
+                                             const UnitAct& act, float* __restrict__ part, uint64_t limit_ns)
+{
+    const ConsumeArgs a = consume_args(p, nrows, tile_base, nwc_used);
+    if (p.L == 32) return ring_consume_L<NC, 32>(a, ring, full, empty, act, part, limit_ns);
+    if (p.L == 16) return ring_consume_L<NC, 16>(a, ring, full, empty, act, part, limit_ns);
+    return ring_consume_L<NC, 8>(a, ring, full, empty, act, part, limit_ns);
+}
+
+}  // namespace mq

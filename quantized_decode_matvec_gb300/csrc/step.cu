@@ -1,0 +1,314 @@
+// step.cu -- the whole decode step of a layer stack as one persistent kernel.
+//
+// "Part 4 . Lecture 08 -- Graph-Resident Decode" captures a decode step as one
+// graph (section 1) and names a single resident kernel as the endpoint of
+// that road; PDL (section 7) attacks the device-side gap between kernels.
+// Here that gap is removed outright: one cooperative CTA per SM runs every
+// matrix of every layer (phases qkv, o, ffn_gu + SiLU*mul + q8_0(h), down, in
+// that order), and
+//
+// * the producer warp streams the CTA's rows of all phases, back to back,
+//   through one bulk-copy ring, so the weights of phase p+1 are already in
+//   shared memory while phase p finishes: weights are never written by any
+//   kernel, so fetching them early is always correct;
+// * consumers follow the dependency chain a real decode has: before a
+//   phase stages its activation they wait at a grid-wide barrier until every
+//   CTA has written the previous phase's outputs (the down projection really
+//   reads the h_q8 written by the gate/up phase; the other inputs stand for
+//   results of the previous phase and are treated the same way);
+// * every wait (ring mbarriers, grid barrier) is bounded in time; on a
+//   timeout a CTA records MQ_DEV_TIMEOUT, raises the step's abort word so the
+//   other CTAs stop too, drains its own copies in flight and returns.
+//
+// Arithmetic, segment split and combine order per matrix are those of the
+// per-matrix ring kernels, so the outputs are bit-identical to mq_step's
+// multi-kernel path.
+#include <type_traits>
+
+#include "mq_epilogue.cuh"
+#include "mq_job.cuh"
+#include "mq_ring.cuh"
+#include "mq_stream.cuh"
+
+namespace mq {
+
+// Grid barrier on the step workspace: word 0 counts CTA arrivals (monotonic
+// within a launch, zeroed by the host before it), word 1 is the abort word.
+__device__ __forceinline__ void grid_arrive(unsigned* ws)
+{
+    __threadfence();
+    atomicAdd(ws, 1u);
+}
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p)
+{
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// true when the count reaches target; false on timeout or when another CTA aborted
+__device__ __forceinline__ bool grid_wait(unsigned* ws, unsigned target, uint64_t limit_ns)
+{
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (ld_acquire_gpu(ws) >= target) {
+            __threadfence();
+            return true;
+        }
+        if (ld_acquire_gpu(ws + 1) != 0) return false;
+        if ((it & 31u) == 31u) {
+            if (global_timer_ns() - t0 > limit_ns) return false;
+            __nanosleep(64);
+        }
+    }
+}
+
+// phase views of a layer descriptor
+struct PhaseJob {
+    const uint8_t* W;
+    const float* x;
+    const uint8_t* xq;
+    uint8_t* xq_out;
+    float* y;
+    int y_ld;
+    const mq_ffn_desc* ffn;
+};
+
+__device__ __forceinline__ PhaseJob phase_job(const mq_layer_desc* L, int ph)
+{
+    PhaseJob j{};
+    if (ph == 0 || ph == 1) {
+        const mq_mv_desc* d = ph == 0 ? &L->qkv : &L->o;
+        j.W = static_cast<const uint8_t*>(d->W);
+        j.x = d->x;
+        j.xq = static_cast<const uint8_t*>(d->xq);
+        j.xq_out = static_cast<uint8_t*>(d->xq_out);
+        j.y = d->y;
+        j.y_ld = d->y_ld;
+    } else if (ph == 2) {
+        j.ffn = &L->ffn;
+        j.W = static_cast<const uint8_t*>(L->ffn.W_gu);
+        j.x = L->ffn.x;
+        j.xq = static_cast<const uint8_t*>(L->ffn.xq);
+    } else {
+        j.ffn = &L->ffn;
+        j.W = static_cast<const uint8_t*>(L->ffn.W_down);
+        j.xq = static_cast<const uint8_t*>(L->ffn.h_q8);
+        j.y = L->ffn.y;
+        j.y_ld = L->ffn.y_ld;
+    }
+    return j;
+}
+
+// rows of matrix phase ph owned by CTA b of G: local row lr -> matrix row
+struct PhaseRows {
+    int nrows, r0, i0, n, R;
+    bool gu;
+    __device__ __forceinline__ int64_t map(int lr) const
+    {
+        return gu ? (lr < n ? int64_t(i0) + lr : int64_t(R) + i0 + (lr - n)) : int64_t(r0) + lr;
+    }
+};
+
+__device__ __forceinline__ PhaseRows phase_rows(const StepPlan& sp, int ph, int b, int G)
+{
+    PhaseRows r{};
+    r.R = sp.R[ph];
+    r.gu = (ph == 2);
+    if (r.gu) {
+        const int nblk = r.R / kQK8;
+        const int b0 = int(int64_t(b) * nblk / G), b1 = int(int64_t(b + 1) * nblk / G);
+        r.i0 = b0 * kQK8;
+        r.n = (b1 - b0) * kQK8;
+        r.nrows = 2 * r.n;
+    } else {
+        r.r0 = int(int64_t(b) * r.R / G);
+        r.nrows = int(int64_t(b + 1) * r.R / G) - r.r0;
+    }
+    return r;
+}
+
+// device-side re-check of every layer descriptor against the step plan
+__device__ __forceinline__ unsigned check_layers(const mq_layer_desc* layers, const StepPlan& sp, int nc)
+{
+    unsigned bad = 0;
+    for (int l = 0; l < sp.n_layers; ++l) {
+        const mq_layer_desc& L = layers[l];
+        MvJob q = read_job<KIND_MV>(&L.qkv), o = read_job<KIND_MV>(&L.o);
+        bad |= check_job(q, sp.R[0], sp.K[0], nc) | check_job(o, sp.R[1], sp.K[1], nc);
+        bad |= check_ffn_gu(&L.ffn, sp.K[2], sp.R[2], nc);
+        MvJob dn = read_job<KIND_DOWN>(&L.ffn);
+        bad |= check_job(dn, sp.R[3], sp.K[3], nc);
+    }
+    return bad;
+}
+
+template <int NC>
+__global__ void __launch_bounds__(32 * ring_max_warps<NC>(), 1)
+    step_kernel(const mq_layer_desc* __restrict__ layers, StepPlan sp, unsigned* status, unsigned* ws)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ volatile int abort_flag;
+    const MvPlan& P0 = sp.ph[0];  // ring geometry and shared-memory offsets are common to all phases
+    const int G = gridDim.x, b = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nwc = sp.nwc;
+    const uint64_t limit_ns = uint64_t(P0.wait_ms) * 1000000ull;
+
+    {
+        const unsigned bad = check_layers(layers, sp, NC);  // every CTA reaches the same verdict
+        if (bad) {
+            if (b == 0 && threadIdx.x == 0) atomicOr(status, bad);
+            return;
+        }
+    }
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + P0.ns;
+    uint8_t* ring = smem + P0.off_ring;
+    float* part = reinterpret_cast<float*>(smem + P0.off_part);
+    float* vals = reinterpret_cast<float*>(smem + P0.off_vals);
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int s = 0; s < P0.ns; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], nwc);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    // Phases run in a fixed order per layer; the phase index is a compile-time
+    // constant everywhere (run-time indexing of the plan in parameter space
+    // would copy it to local memory).
+    using P0c = std::integral_constant<int, 0>;
+    using P1c = std::integral_constant<int, 1>;
+    using P2c = std::integral_constant<int, 2>;
+    using P3c = std::integral_constant<int, 3>;
+    const int nphase = sp.n_layers * 4;
+    int issued = 0;  // tiles issued by the producer (lane 0 of the producer warp)
+    if (warp == nwc) {
+        // ---- producer: all phases' tiles, back to back
+        auto produce = [&](auto phc, int l) -> bool {
+            constexpr int ph = decltype(phc)::value;
+            const MvPlan& P = sp.ph[ph];
+            const PhaseJob j = phase_job(&layers[l], ph);
+            const PhaseRows pr = phase_rows(sp, ph, b, G);
+            const size_t row_bytes = size_t(sp.K[ph] / kQK) * kQ4KBytes;
+            const int ntiles = (pr.nrows + P.T - 1) / P.T;
+            for (int t = 0; t < ntiles; ++t, ++issued) {
+                const int s = issued % P0.ns;
+                if (issued >= P0.ns && !mbar_wait_bounded(&empty[s], uint32_t(issued / P0.ns - 1) & 1u, limit_ns))
+                    return false;
+                const int lr0 = t * P.T, tn = min(P.T, pr.nrows - lr0);
+                mbar_arrive_expect_tx(&full[s], uint32_t(size_t(tn) * row_bytes));
+                uint8_t* dst = ring + size_t(s) * P0.stage_bytes;
+                int a = lr0;
+                const int e = lr0 + tn;
+                while (a < e) {
+                    int stop = e;
+                    if (pr.gu && a < pr.n && e > pr.n) stop = pr.n;
+                    bulk_copy_g2s(dst + size_t(a - lr0) * row_bytes, j.W + size_t(pr.map(a)) * row_bytes,
+                                  uint32_t(size_t(stop - a) * row_bytes), &full[s]);
+                    a = stop;
+                }
+            }
+            return true;
+        };
+        if (lane == 0) {
+            for (int l = 0; l < sp.n_layers && !abort_flag; ++l) {
+                if (!produce(P0c{}, l) || !produce(P1c{}, l) || !produce(P2c{}, l) || !produce(P3c{}, l)) {
+                    abort_flag = 1;
+                    break;
+                }
+            }
+        }
+    } else {
+        // ---- consumers
+        const int ctid = threadIdx.x, cthr = nwc * 32;
+        int gi = 0;  // tile index of the ring sequence at the start of the phase
+        auto consume = [&](auto phc, int l) -> bool {
+            constexpr int ph = decltype(phc)::value;
+            const int k = 4 * l + ph;  // phase number within the launch
+            const MvPlan& P = sp.ph[ph];
+            const PhaseJob j = phase_job(&layers[l], ph);
+            const PhaseRows pr = phase_rows(sp, ph, b, G);
+            const int K = sp.K[ph];
+            // wait until every CTA has written the previous phase's outputs
+            if (k > 0) {
+                if (ctid == 0 && !grid_wait(ws, unsigned(k) * unsigned(G), limit_ns)) abort_flag = 1;
+                named_barrier_sync(1, cthr);
+                if (abort_flag) return false;
+            }
+            const UnitAct act{reinterpret_cast<uint4*>(smem + P0.off_act),
+                              reinterpret_cast<float4*>(smem + P0.off_act + size_t(NC) * 8 * P.C * 16), P.C};
+            if (ph == 3)
+                stage_units_q8<NC, true>(j.xq, K, act, nullptr, ctid, cthr);  // h_q8: written in this kernel
+            else if (j.x)
+                stage_units_x<NC>(j.x, K, act, (ph <= 1 && b == 0) ? j.xq_out : nullptr, nullptr, ctid, cthr);
+            else
+                stage_units_q8<NC>(j.xq, K, act, nullptr, ctid, cthr);
+            named_barrier_sync(1, cthr);
+            const bool ok = ring_consume<NC>(P, pr.nrows, gi, P.nwc, ring, full, empty, act, part, limit_ns);
+            gi += (pr.nrows + P.T - 1) / P.T;
+            if (!ok && lane == 0) abort_flag = 1;
+            named_barrier_sync(1, cthr);
+            if (abort_flag) return false;
+            if (ph == 2) {
+                gu_epilogue_on<NC>(part, vals, P.nseg, pr.n, pr.i0, pr.R, static_cast<uint8_t*>(j.ffn->h_q8),
+                                   j.ffn->gu_dbg, j.ffn->h_dbg, ctid, cthr, [cthr]() { named_barrier_sync(1, cthr); });
+            } else {
+                mv_epilogue<NC>(part, P.nseg, pr.nrows, pr.r0, j.y, j.y_ld, ctid, cthr);
+            }
+            named_barrier_sync(1, cthr);  // this CTA's outputs of phase k are written
+            if (ctid == 0 && k + 1 < nphase) grid_arrive(ws);
+            return true;
+        };
+        for (int l = 0; l < sp.n_layers; ++l)
+            if (!consume(P0c{}, l) || !consume(P1c{}, l) || !consume(P2c{}, l) || !consume(P3c{}, l)) break;
+        if (abort_flag && ctid == 0) atomicExch(ws + 1, 1u);  // let the other CTAs stop early
+    }
+    __syncthreads();
+    if (abort_flag) {
+        if (threadIdx.x == 0) atomicOr(status, MQ_DEV_TIMEOUT);
+        if (warp == nwc && lane == 0)  // drain this CTA's copies that may still be in flight
+            for (int t = issued > P0.ns ? issued - P0.ns : 0; t < issued; ++t)
+                (void)mbar_wait_bounded(&full[t % P0.ns], uint32_t(t / P0.ns) & 1u, limit_ns);
+    }
+}
+
+cudaError_t launch_step(const mq_layer_desc* layers, const StepPlan& sp, int ncols, unsigned* status, unsigned* ws,
+                        cudaStream_t s)
+{
+    cudaError_t e = cudaMemsetAsync(ws, 0, 2 * sizeof(unsigned), s);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(sp.grid);
+    cfg.blockDim = dim3(32 * (sp.nwc + 1));
+    cfg.dynamicSmemBytes = sp.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs resident at once: the grid barrier needs it
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    switch (ncols) {
+#define MQ_CASE(N) \
+    case N: return cudaLaunchKernelEx(&cfg, step_kernel<N>, layers, sp, status, ws);
+        MQ_CASE(1) MQ_CASE(2) MQ_CASE(3) MQ_CASE(4) MQ_CASE(5) MQ_CASE(6) MQ_CASE(7) MQ_CASE(8)
+#undef MQ_CASE
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t set_step_attributes(int max_smem)
+{
+    cudaError_t e = cudaSuccess;
+#define MQ_SET(N) \
+    if (e == cudaSuccess) e = set_max_dyn_smem(reinterpret_cast<const void*>(step_kernel<N>), max_smem);
+    MQ_SET(1) MQ_SET(2) MQ_SET(3) MQ_SET(4) MQ_SET(5) MQ_SET(6) MQ_SET(7) MQ_SET(8)
+#undef MQ_SET
+    return e;
+}
+
+}  // namespace mq

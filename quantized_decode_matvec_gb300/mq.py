@@ -39,12 +39,19 @@ MQ_ERR_UNSUPPORTED = 5
 MQ_ERR_NOT_INITIALIZED = 6
 MQ_DEV_DESC_MISMATCH = 1
 MQ_DEV_DESC_ALIGN = 2
+MQ_DEV_TIMEOUT = 4
+MQ_VARIANT_AUTO = 0
+MQ_VARIANT_FORCE_REGISTER = 1
+MQ_FAULT_NONE = 0
+MQ_FAULT_WITHHOLD_TILE = 1
 MQ_TYPE_Q4_K = 1
 MQ_TYPE_Q8_0 = 2
 MQ_MAX_NCOLS = 8
 MQ_MAX_K = 131072
 MQ_MAX_K_TIMES_NCOLS = 163840
 MQ_STEP_PDL = 1
+MQ_STEP_PERSISTENT = 2
+MQ_STEP_WORKSPACE_BYTES = 256
 
 
 class MvDesc(ctypes.Structure):
@@ -64,7 +71,7 @@ class LayerDesc(ctypes.Structure):
 
 class StepShape(ctypes.Structure):
     _fields_ = [("n_layers", c_i32), ("H", c_i32), ("I", c_i32), ("qkv_rows", c_i32), ("o_rows", c_i32),
-                ("o_K", c_i32), ("ncols", c_i32), ("flags", c_u32)]
+                ("o_K", c_i32), ("ncols", c_i32), ("flags", c_u32), ("workspace", c_vp)]
 
 
 def _sig(name, res, *args):
@@ -94,13 +101,15 @@ _sig("mq_ffn_gu_silu_down", c_i32, c_vp, c_i32, c_i32, c_i32, c_vp)
 _sig("mq_ffn_gate_up", c_i32, c_vp, c_i32, c_i32, c_i32, c_vp)
 _sig("mq_step", c_i32, c_vp, ctypes.POINTER(StepShape), c_vp)
 _sig("mq_debug_block_sums_q4K_q8_0", c_i32, c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp)
+_sig("mq_debug_set_variant", c_i32, c_i32)
+_sig("mq_debug_set_fault", c_i32, c_i32)
 
 # the exported names, one per declaration in include/mq.h
 EXPORTS = ["mq_status_string", "mq_abi_version", "mq_last_cuda_error", "mq_init", "mq_read_device_status",
            "mq_q4K_row_bytes", "mq_q8_0_bytes", "mq_quant_block_elems", "mq_quant_block_bytes",
            "mq_concat_rows_feasible", "mq_concat_rows", "mq_quantize_q8_0", "mq_check_mv_desc",
            "mq_matvec_q4K_q8_0", "mq_check_ffn_desc", "mq_ffn_gu_silu_down", "mq_ffn_gate_up", "mq_step",
-           "mq_debug_block_sums_q4K_q8_0"]
+           "mq_debug_block_sums_q4K_q8_0", "mq_debug_set_variant", "mq_debug_set_fault"]
 
 
 class MQError(RuntimeError):
@@ -203,6 +212,14 @@ def mq_step(d_layers: int, shape: StepShape, stream: int = 0) -> int:
 def mq_debug_block_sums_q4K_q8_0(d_desc: int, rows: int, K: int, ncols: int, sumi: int, sumq: int,
                                  stream: int = 0) -> int:
     return _lib.mq_debug_block_sums_q4K_q8_0(c_vp(d_desc), rows, K, ncols, c_vp(sumi), c_vp(sumq), c_vp(stream))
+
+
+def mq_debug_set_variant(policy: int) -> int:
+    return _lib.mq_debug_set_variant(policy)
+
+
+def mq_debug_set_fault(fault: int) -> int:
+    return _lib.mq_debug_set_fault(fault)
 
 
 def _check(st: int, where: str):
@@ -373,9 +390,12 @@ class StepBuffers:
             _check(mq_check_ffn_desc(table[l].ffn), "mq_check_ffn_desc")
         self.table_host = table
         self.table = upload_struct(bytes(table), dev)
+        # grid-barrier words of the persistent step (zeroed by mq_step itself)
+        self.workspace = torch.zeros(MQ_STEP_WORKSPACE_BYTES, dtype=torch.uint8, device=dev)
 
     def shape(self, flags: int = 0) -> StepShape:
-        return StepShape(self.n_layers, self.H, self.I, self.qkv_rows, self.o_rows, self.o_K, self.ncols, flags)
+        return StepShape(self.n_layers, self.H, self.I, self.qkv_rows, self.o_rows, self.o_K, self.ncols, flags,
+                         _ptr(self.workspace))
 
     def step(self, stream=None, flags: int = 0) -> None:
         _check(mq_step(_ptr(self.table), self.shape(flags), _stream(stream)), "mq_step")

@@ -30,3 +30,13 @@ def cuda_ready(mq_lib):
     torch.cuda.init()
     mq_lib.init(torch.cuda.current_device())
     return mq_lib
+
+
+@pytest.fixture(params=["auto", "register"])
+def variant(request, cuda_ready):
+    """Run a test under each kernel family: bulk-copy ring where it applies (auto), and register streaming."""
+    mq = cuda_ready
+    pol = mq.MQ_VARIANT_AUTO if request.param == "auto" else mq.MQ_VARIANT_FORCE_REGISTER
+    assert mq.mq_debug_set_variant(pol) == mq.MQ_OK
+    yield request.param
+    assert mq.mq_debug_set_variant(mq.MQ_VARIANT_AUTO) == mq.MQ_OK

@@ -30,7 +30,7 @@ def test_struct_sizes_match_header(mq_lib):
     assert ctypes.sizeof(mq_lib.MvDesc) == 5 * 8 + 4 * 4
     assert ctypes.sizeof(mq_lib.FfnDesc) == 8 * 8 + 4 * 4
     assert ctypes.sizeof(mq_lib.LayerDesc) == 2 * 56 + 80
-    assert ctypes.sizeof(mq_lib.StepShape) == 8 * 4
+    assert ctypes.sizeof(mq_lib.StepShape) == 8 * 4 + 8
 
 
 def test_sizes(mq_lib):
@@ -44,7 +44,7 @@ def test_sizes(mq_lib):
     assert mq_lib.mq_quant_block_elems(mq_lib.MQ_TYPE_Q8_0) == 32
     assert mq_lib.mq_quant_block_bytes(mq_lib.MQ_TYPE_Q8_0) == 34
     assert mq_lib.mq_quant_block_bytes(99) == 0
-    assert mq_lib.mq_abi_version() == 1
+    assert mq_lib.mq_abi_version() == 2
     assert mq_lib.mq_status_string(0) == "ok"
     assert "shape" in mq_lib.mq_status_string(2)
 
@@ -121,3 +121,12 @@ def test_binding_raises_without_fallback(mq_lib):
     # the tensor-level helpers surface library errors; there is no CPU path to fall back to
     with pytest.raises(mq_lib.MQError):
         mq_lib._check(mq_lib.mq_matvec_q4K_q8_0(0, 10, 100, 1), "x")
+
+
+def test_persistent_step_needs_workspace(mq_lib):
+    m = mq_lib
+    # checked before any device work: no workspace, misaligned workspace
+    shape = m.StepShape(2, 3584, 18944, 4608, 3584, 3584, 1, m.MQ_STEP_PERSISTENT, None)
+    assert m.mq_step(0x1000, shape) == m.MQ_ERR_INVALID_ARG
+    shape.workspace = 0x2002
+    assert m.mq_step(0x1000, shape) == m.MQ_ERR_ALIGN

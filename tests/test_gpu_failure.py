@@ -1,0 +1,46 @@
+"""Failure detection without a GPU fault.
+
+The bulk-copy ring kernels bound every wait on their copy pipeline.  A
+test-only setting makes the producer withhold each CTA's last tile, so the
+consumers' waits run out (a flag that nothing ever sets): the kernel must
+report MQ_DEV_TIMEOUT through the device status word, leave its output
+untouched and return, and the context must stay usable for the next call.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from quantized_decode_matvec_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def test_bounded_wait_runs_out_and_reports(cuda_ready):
+    import torch
+    mq = cuda_ready
+    rows, K = 3584, 3584          # planned on the ring kernels
+    W = torch.from_numpy(synth.q4K_matrix(rows, K, seed=4)).cuda()
+    x_np = synth.activation(K, 1, seed=4)
+    x = torch.from_numpy(x_np).cuda()
+    y = torch.full((1, rows), 3.0, dtype=torch.float32, device="cuda")
+    assert mq.mq_read_device_status(0) == 0
+    assert mq.mq_debug_set_fault(mq.MQ_FAULT_WITHHOLD_TILE) == mq.MQ_OK
+    try:
+        mq.matvec_q4K_q8_0(W, rows, K, x=x, y=y)
+        torch.cuda.synchronize()                     # returns: the waits are bounded
+    finally:
+        assert mq.mq_debug_set_fault(mq.MQ_FAULT_NONE) == mq.MQ_OK
+    assert mq.mq_read_device_status(0) & mq.MQ_DEV_TIMEOUT
+    assert torch.all(y == 3.0)                       # nothing written
+    # the context is still healthy: the same call now succeeds and matches the oracle
+    y2, _ = mq.matvec_q4K_q8_0(W, rows, K, x=x)
+    torch.cuda.synchronize()
+    assert mq.mq_read_device_status(0) == 0
+    y_ref, T = oracle.matvec(W.cpu().numpy(), oracle.quantize_q8_0(x_np), rows, K)
+    assert oracle.within_tolerance(y2.cpu().numpy(), y_ref, T).all()
+
+
+def test_fault_setter_rejects_unknown(cuda_ready):
+    mq = cuda_ready
+    assert mq.mq_debug_set_fault(7) == mq.MQ_ERR_INVALID_ARG
+    assert mq.mq_debug_set_variant(7) == mq.MQ_ERR_INVALID_ARG

@@ -56,7 +56,7 @@ def _stagewise(out, W_gu, W_down, x, H, I, gu_rows=None, down_rows=None):
 
 
 @pytest.mark.parametrize("H,I,nc", [(256, 256, 1), (512, 768, 2), (1024, 1280, 1), (768, 2048, 8), (3584, 512, 3)])
-def test_ffn_small_stagewise_and_end_to_end(cuda_ready, H, I, nc):
+def test_ffn_small_stagewise_and_end_to_end(cuda_ready, variant, H, I, nc):
     mq = cuda_ready
     W_gu = synth.q4K_matrix(2 * I, H, seed=H + I, tag=synth.TAG_GU)
     W_down = synth.q4K_matrix(H, I, seed=H + I, tag=synth.TAG_DOWN)
@@ -75,7 +75,7 @@ def test_ffn_small_stagewise_and_end_to_end(cuda_ready, H, I, nc):
     assert np.all(np.abs(out["y"] - y_ref) <= 1e-3 * T + 1e-5 + widen * (1 + 1e-6))
 
 
-def test_ffn_05b_layers_stagewise(cuda_ready):
+def test_ffn_05b_layers_stagewise(cuda_ready, variant):
     mq = cuda_ready
     case = synth.FFN_05B
     for layer in (0, 11, 23):
@@ -86,7 +86,7 @@ def test_ffn_05b_layers_stagewise(cuda_ready):
 
 
 @pytest.mark.parametrize("nc", [1, 2, 4, 8])
-def test_ffn_7b_stagewise(cuda_ready, nc):
+def test_ffn_7b_stagewise(cuda_ready, variant, nc):
     mq = cuda_ready
     case = synth.FFN_7B
     W_gu, W_down = synth.ffn_layer_weights(case, 0)
@@ -98,7 +98,7 @@ def test_ffn_7b_stagewise(cuda_ready, nc):
     _stagewise(out, W_gu, W_down, x, case.H, case.I, gu_rows=gu_rows, down_rows=down_rows)
 
 
-def test_ffn_deterministic_aa(cuda_ready):
+def test_ffn_deterministic_aa(cuda_ready, variant):
     mq = cuda_ready
     case = synth.FFN_7B
     W_gu, W_down = synth.ffn_layer_weights(case, 0)

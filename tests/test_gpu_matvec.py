@@ -33,7 +33,7 @@ SHAPES = [(1, 256), (7, 256), (33, 512), (300, 1024), (129, 1280), (64, 2304), (
 
 @pytest.mark.parametrize("rows,K", SHAPES)
 @pytest.mark.parametrize("ncols", [1, 2, 8])
-def test_matvec_parity_small(cuda_ready, rows, K, ncols):
+def test_matvec_parity_small(cuda_ready, variant, rows, K, ncols):
     import torch
     mq = cuda_ready
     if K * ncols > mq.MQ_MAX_K_TIMES_NCOLS:
@@ -55,7 +55,7 @@ def test_matvec_parity_small(cuda_ready, rows, K, ncols):
 
 
 @pytest.mark.parametrize("ncols", [1, 3, 4, 5, 6, 7])
-def test_matvec_all_ncols(cuda_ready, ncols):
+def test_matvec_all_ncols(cuda_ready, variant, ncols):
     import torch
     mq = cuda_ready
     rows, K = 257, 3584
@@ -93,7 +93,7 @@ def test_xq_out_matches_quantizer(cuda_ready):
     assert np.array_equal(xq_out.cpu().numpy(), oracle.quantize_q8_0(x))
 
 
-def test_deterministic_aa(cuda_ready):
+def test_deterministic_aa(cuda_ready, variant):
     # A/A control: the same call twice gives the same bits (no atomics, fixed reduction order)
     import torch
     mq = cuda_ready
@@ -152,7 +152,7 @@ def test_matvec_512x1024_full(cuda_ready):
 
 
 @pytest.mark.parametrize("K", synth.KSWEEP_KS)
-def test_k_sweep_full(cuda_ready, K):
+def test_k_sweep_full(cuda_ready, variant, K):
     import torch
     mq = cuda_ready
     W, x = synth.ksweep_inputs(K)
@@ -161,7 +161,7 @@ def test_k_sweep_full(cuda_ready, K):
     _check_y(y.cpu().numpy(), W, oracle.quantize_q8_0(x), synth.KSWEEP_ROWS, K)
 
 
-def test_7b_down_matrix_full(cuda_ready):
+def test_7b_down_matrix_full(cuda_ready, variant):
     # down projection of the 7B FFN: 3584 x 18944, every output row against the oracle
     import torch
     mq = cuda_ready

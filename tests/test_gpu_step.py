@@ -68,7 +68,7 @@ def _check_layer_oracle(case, host, outs, a, b, c, l, rows=None):
     assert oracle.within_tolerance(yg, y_ref, T).all(), ("down", l)
 
 
-def test_step_small_eager_matches_oracle(cuda_ready):
+def test_step_small_eager_matches_oracle(cuda_ready, variant):
     mq = cuda_ready
     wdev, host = _weights(SMALL)
     bufs = _bufs(mq, SMALL, wdev, debug=True)
@@ -84,7 +84,7 @@ def test_step_small_eager_matches_oracle(cuda_ready):
         assert np.mean(outs["h_q8"][l] == hq_ref) > 0.99
 
 
-def test_step_graph_replays_byte_identical(cuda_ready):
+def test_step_graph_replays_byte_identical(cuda_ready, variant):
     import torch
     from quantized_decode_matvec_gb300.graph import StepGraph
     mq = cuda_ready
@@ -175,7 +175,7 @@ def test_capture_failure_falls_back_to_eager(cuda_ready):
     _check_layer_oracle(SMALL, host, outs, a, b, c, SMALL.n_layers - 1)
 
 
-def test_step_pdl_matches_plain(cuda_ready):
+def test_step_pdl_matches_plain(cuda_ready, variant):
     mq = cuda_ready
     wdev, host = _weights(SMALL)
     p = _bufs(mq, SMALL, wdev)
@@ -190,6 +190,51 @@ def test_step_pdl_matches_plain(cuda_ready):
         assert np.array_equal(x[k].view(np.uint8), y[k].view(np.uint8)), k
 
 
+@pytest.mark.parametrize("case", [SMALL, synth.StepCase("step_tiny", 2, 256, 256, 256, 256, 1, 6),
+                                  synth.StepCase("step_ncols3", 2, 512, 768, 512, 128, 3, 7)],
+                         ids=["small", "tiny", "ncols3"])
+def test_persistent_step_bit_identical_to_multikernel(cuda_ready, case):
+    mq = cuda_ready
+    wdev, host = _weights(case)
+    p = _bufs(mq, case, wdev, debug=True)
+    q = _bufs(mq, case, wdev, debug=True)
+    a, b, c = _inputs(case, 9)
+    _set_inputs(p, a, b, c)
+    _set_inputs(q, a, b, c)
+    p.step()
+    q.step(flags=mq.MQ_STEP_PERSISTENT)
+    x, y = _outputs(p), _outputs(q)
+    assert mq.mq_read_device_status(0) == 0
+    for k in x:
+        assert np.array_equal(x[k].view(np.uint8), y[k].view(np.uint8)), k
+    assert np.array_equal(p.xq_a.cpu().numpy(), q.xq_a.cpu().numpy())
+    for l in range(case.n_layers):
+        _check_layer_oracle(case, host, y, a, b, c, l)
+
+
+def test_persistent_step_graph_replays(cuda_ready):
+    import torch
+    from quantized_decode_matvec_gb300.graph import StepGraph
+    mq = cuda_ready
+    wdev, host = _weights(SMALL)
+    eager = _bufs(mq, SMALL, wdev)
+    graphed = _bufs(mq, SMALL, wdev)
+    g = StepGraph(graphed, flags=mq.MQ_STEP_PERSISTENT)
+    assert g.captured, g.capture_error
+    for r in range(8):
+        a, b, c = _inputs(SMALL, 20 + r)
+        _set_inputs(eager, a, b, c)
+        eager.step()
+        e = _outputs(eager)
+        _set_inputs(graphed, a, b, c)
+        g.run()
+        torch.cuda.synchronize()
+        gr = _outputs(graphed)
+        for k in e:
+            assert np.array_equal(e[k].view(np.uint8), gr[k].view(np.uint8)), (r, k)
+    assert mq.mq_read_device_status(0) == 0
+
+
 @pytest.mark.slow
 def test_step_7b_full_size_sampled(cuda_ready):
     # the 28-layer 7B-class step at full size, as the benchmark runs it (graph replay),
@@ -200,7 +245,8 @@ def test_step_7b_full_size_sampled(cuda_ready):
     case = synth.STEP_7B
     wdev, host = _weights(case)
     bufs = _bufs(mq, case, wdev)
-    g = StepGraph(bufs)
+    multi = _bufs(mq, case, wdev)
+    g = StepGraph(bufs, flags=mq.MQ_STEP_PERSISTENT)   # the configuration the benchmark times
     assert g.captured, g.capture_error
     rng = np.random.default_rng(0)
     rows = rng.choice(1 << 20, 48, replace=False)
@@ -212,5 +258,12 @@ def test_step_7b_full_size_sampled(cuda_ready):
         layers = range(case.n_layers) if r == 0 else (0, case.n_layers - 1)
         for l in layers:
             _check_layer_oracle(case, host, outs, a, b, c, l, rows=rows)
+        if r == 2:  # the multi-kernel path gives the same bytes at full size
+            _set_inputs(multi, a, b, c)
+            multi.step()
+            m = _outputs(multi)
+            for k in outs:
+                assert np.array_equal(outs[k].view(np.uint8), m[k].view(np.uint8)), k
+    assert mq.mq_read_device_status(0) == 0
     del wdev, bufs, g
     torch.cuda.empty_cache()
