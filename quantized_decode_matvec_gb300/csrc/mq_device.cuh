@@ -44,19 +44,27 @@ __device__ __forceinline__ uint4 ldg16(const uint8_t* p)
 // order-free.  d = amax/127 and x/d by IEEE division, round half away from
 // zero, clamp to +-127.  Returns this lane's code; *d_out is the fp32 d.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ int q8_quantize_lane(float x, float* d_out)
+// The two halves of the quantizer, shared by every caller:
+// d = amax/127 of a warp-held block (all lanes get it), and one lane's code.
+__device__ __forceinline__ float q8_block_scale(float x)
 {
     const unsigned ab = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(x)));
-    const float amax = __uint_as_float(ab);
-    const float d = __fdiv_rn(amax, 127.0f);
-    int q = 0;
-    if (d != 0.0f) {
-        float r = roundf(__fdiv_rn(x, d));
-        r = fminf(fmaxf(r, -127.0f), 127.0f);
-        q = static_cast<int>(r);
-    }
+    return __fdiv_rn(__uint_as_float(ab), 127.0f);
+}
+
+__device__ __forceinline__ int q8_code(float x, float d)
+{
+    if (d == 0.0f) return 0;
+    float r = roundf(__fdiv_rn(x, d));
+    r = fminf(fmaxf(r, -127.0f), 127.0f);
+    return static_cast<int>(r);
+}
+
+__device__ __forceinline__ int q8_quantize_lane(float x, float* d_out)
+{
+    const float d = q8_block_scale(x);
     *d_out = d;
-    return q;
+    return q8_code(x, d);
 }
 
 // ---------------------------------------------------------------------------

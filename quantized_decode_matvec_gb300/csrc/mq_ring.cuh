@@ -128,15 +128,13 @@ __device__ __noinline__ bool ring_consume_L(const ConsumeArgs p, const uint8_t* 
                 UnitW wa, wb;
                 load_w(stage, va ? ra : rb, wa);
                 load_w(stage, vb ? rb : ra, wb);
-                float fda[4], fma_[4], fdb[4], fmb[4];
-                unit_scales(wa.h, upper, fda, fma_);
-                unit_scales(wb.h, upper, fdb, fmb);
+                const UnitScales ka = unit_scales(wa.h, upper), kb = unit_scales(wb.h, upper);
 #pragma unroll
                 for (int c = 0; c < NC; ++c) {
                     if (!kRegAct) load_act(c, 0);
                     const int cc = kRegAct ? c : 0;
-                    if (va) acc_a[c] = unit_column(wa, fda, fma_, A[cc], DQ[cc], DQSQ[cc], 0.0f);
-                    if (vb) acc_b[c] = unit_column(wb, fdb, fmb, A[cc], DQ[cc], DQSQ[cc], 0.0f);
+                    if (va) acc_a[c] = unit_column(wa, ka, A[cc], DQ[cc], DQSQ[cc], 0.0f);
+                    if (vb) acc_b[c] = unit_column(wb, kb, A[cc], DQ[cc], DQSQ[cc], 0.0f);
                 }
             }
 #pragma unroll

@@ -61,9 +61,11 @@ __device__ __forceinline__ void stage_units_q8(const uint8_t* __restrict__ xq, i
     }
 }
 
-// From fp32 x: q8_0 quantization (the same warp-level quantizer as the
+// From fp32 x: q8_0 quantization (the same warp-level quantizer halves as the
 // stand-alone kernel, hence bit-identical) straight into the unit layout.
-// Whole warps tid = 0..nthr-1; each warp first loads up to 8 blocks.
+// Whole warps tid = 0..nthr-1.  Each warp takes B blocks at a time and runs
+// their quantizations in lockstep (independent chains), since a single
+// block's amax -> divide -> round -> sum chain is mostly latency.
 template <int NC>
 __device__ __forceinline__ void stage_units_x(const float* __restrict__ x, int K, UnitAct s,
                                               uint8_t* __restrict__ xq_out, int32_t* sumq_out, int tid, int nthr)
@@ -73,7 +75,8 @@ __device__ __forceinline__ void stage_units_x(const float* __restrict__ x, int K
     const int lane = tid & 31, warp = tid >> 5, nw = nthr >> 5;
     const int total = NC * nq;
     for (int t0 = warp * B; t0 < total; t0 += nw * B) {
-        float v[B];
+        float v[B], d[B];
+        int q[B], sq[B];
 #pragma unroll
         for (int b = 0; b < B; ++b) {
             const int t = t0 + b;
@@ -84,28 +87,32 @@ __device__ __forceinline__ void stage_units_x(const float* __restrict__ x, int K
             }
         }
 #pragma unroll
+        for (int b = 0; b < B; ++b) d[b] = q8_block_scale(v[b]);
+#pragma unroll
+        for (int b = 0; b < B; ++b) q[b] = q8_code(v[b], d[b]);
+#pragma unroll
+        for (int b = 0; b < B; ++b) sq[b] = __reduce_add_sync(0xffffffffu, q[b]);
+#pragma unroll
         for (int b = 0; b < B; ++b) {
             const int t = t0 + b;
-            if (t >= total) break;  // warp-uniform
-            const int c = t / nq, J = t - c * nq;
-            float d;
-            const int q = q8_quantize_lane(v[b], &d);
-            const __half dh = __float2half_rn(d);
-            const float dq = __half2float(dh);
-            const int sq = __reduce_add_sync(0xffffffffu, q);
-            const int u = J >> 2, slot = J & 3;
-            uint8_t* P = reinterpret_cast<uint8_t*>(s.planes + size_t(c * 8 + 2 * slot + (lane >> 4)) * s.U + u);
-            P[lane & 15] = uint8_t(int8_t(q));
-            if (lane == 0) {
-                float* S = reinterpret_cast<float*>(s.scales + (size_t(c) * s.U + u) * 2);
-                S[slot] = dq;
-                S[4 + slot] = dq * float(sq);
-                if (sumq_out) sumq_out[size_t(c) * nq + J] = sq;
-            }
-            if (xq_out) {
-                uint8_t* ob = xq_out + (size_t(c) * nq + J) * kQ8Bytes;
-                if (lane == 0) *reinterpret_cast<uint16_t*>(ob) = __half_as_ushort(dh);
-                ob[2 + lane] = uint8_t(int8_t(q));
+            if (t < total) {
+                const int c = t / nq, J = t - c * nq;
+                const __half dh = __float2half_rn(d[b]);
+                const float dq = __half2float(dh);
+                const int u = J >> 2, slot = J & 3;
+                uint8_t* P = reinterpret_cast<uint8_t*>(s.planes + size_t(c * 8 + 2 * slot + (lane >> 4)) * s.U + u);
+                P[lane & 15] = uint8_t(int8_t(q[b]));
+                if (lane == 0) {
+                    float* S = reinterpret_cast<float*>(s.scales + (size_t(c) * s.U + u) * 2);
+                    S[slot] = dq;
+                    S[4 + slot] = dq * float(sq[b]);
+                    if (sumq_out) sumq_out[size_t(c) * nq + J] = sq[b];
+                }
+                if (xq_out) {
+                    uint8_t* ob = xq_out + (size_t(c) * nq + J) * kQ8Bytes;
+                    if (lane == 0) *reinterpret_cast<uint16_t*>(ob) = __half_as_ushort(dh);
+                    ob[2 + lane] = uint8_t(int8_t(q[b]));
+                }
             }
         }
     }
@@ -123,27 +130,35 @@ __device__ __forceinline__ float byte_as_float(uint32_t w, int b)
     return __int_as_float(__byte_perm(w, 0x4B000000u, 0x7540u | uint32_t(b))) - 8388608.0f;
 }
 
-// Float scales of the unit's four sub-blocks j = 4h..4h+3: fd[j] = d*sc_j,
-// fm[j] = dmin*m_j; fd[1] and fd[3] pre-divided by 16 (exact) to match the
-// in-place high nibbles of unit_dot.
+// Scales of the unit's four sub-blocks j = 4h..4h+3 as floats: sc[j], m[j]
+// (sc[1], sc[3] pre-divided by 16, exact, to match the in-place high nibbles
+// of unit_dot), and the block's d and dmin.
 //   h = 0: sc_j = s[j] & 63, m_j = s[j+4] & 63                     (j = 0..3)
 //   h = 1: sc_j = (s[j+4] & 15) | (s[j-4] >> 6) << 4,
 //          m_j  = (s[j+4] >> 4) | (s[j] >> 6) << 4                  (j = 4..7)
-__device__ __forceinline__ void unit_scales(const uint4& hd, bool upper, float fd[4], float fm[4])
+struct UnitScales {
+    float sc[4], m[4];
+    float d, dmin;
+};
+
+__device__ __forceinline__ UnitScales unit_scales(const uint4& hd, bool upper)
 {
+    UnitScales r;
     const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&hd.x));
     const uint32_t S0 = hd.y, S1 = hd.z, S2 = hd.w;
     const uint32_t mlo = upper ? 0x0f0f0f0fu : 0x3f3f3f3fu;
     const uint32_t mhi = upper ? 0x30303030u : 0u;
     const uint32_t sc = ((upper ? S2 : S0) & mlo) | ((S0 >> 2) & mhi);
     const uint32_t m = ((upper ? (S2 >> 4) : S1) & mlo) | ((S1 >> 2) & mhi);
-    const float d16 = dd.x * 0.0625f;
-    fd[0] = dd.x * byte_as_float(sc, 0);
-    fd[1] = d16 * byte_as_float(sc, 1);
-    fd[2] = dd.x * byte_as_float(sc, 2);
-    fd[3] = d16 * byte_as_float(sc, 3);
+    r.sc[0] = byte_as_float(sc, 0);
+    r.sc[1] = 0.0625f * byte_as_float(sc, 1);
+    r.sc[2] = byte_as_float(sc, 2);
+    r.sc[3] = 0.0625f * byte_as_float(sc, 3);
 #pragma unroll
-    for (int b = 0; b < 4; ++b) fm[b] = dd.y * byte_as_float(m, b);
+    for (int b = 0; b < 4; ++b) r.m[b] = byte_as_float(m, b);
+    r.d = dd.x;
+    r.dmin = dd.y;
+    return r;
 }
 
 __device__ __forceinline__ int dot16_lo(const uint4& w, const uint4& a, int acc)
@@ -179,20 +194,22 @@ __device__ __forceinline__ void unit_dot(const UnitW& w, const uint4 (&A)[8], in
 
 // acc + the unit's contribution for one column:
 // sum_j dq_j*(d*sc_j*s_j - dmin*m_j*sumq_j)
-__device__ __forceinline__ float unit_column(const UnitW& w, const float fd[4], const float fm[4],
-                                             const uint4 (&A)[8], const float4& dq, const float4& dqsq, float acc)
+//   = d * sum_j sc_j*(dq_j*s_j) - dmin * sum_j m_j*(dq_j*sumq_j)
+__device__ __forceinline__ float unit_column(const UnitW& w, const UnitScales& k, const uint4 (&A)[8],
+                                             const float4& dq, const float4& dqsq, float acc)
 {
     int s[4];
     unit_dot(w, A, s);
-    acc = fmaf(fd[0], dq.x * float(s[0]), acc);
-    acc = fmaf(fd[1], dq.y * float(s[1]), acc);
-    acc = fmaf(fd[2], dq.z * float(s[2]), acc);
-    acc = fmaf(fd[3], dq.w * float(s[3]), acc);
-    acc = fmaf(-fm[0], dqsq.x, acc);
-    acc = fmaf(-fm[1], dqsq.y, acc);
-    acc = fmaf(-fm[2], dqsq.z, acc);
-    acc = fmaf(-fm[3], dqsq.w, acc);
-    return acc;
+    float t = k.sc[0] * (dq.x * float(s[0]));
+    t = fmaf(k.sc[1], dq.y * float(s[1]), t);
+    t = fmaf(k.sc[2], dq.z * float(s[2]), t);
+    t = fmaf(k.sc[3], dq.w * float(s[3]), t);
+    float u = k.m[0] * dqsq.x;
+    u = fmaf(k.m[1], dqsq.y, u);
+    u = fmaf(k.m[2], dqsq.z, u);
+    u = fmaf(k.m[3], dqsq.w, u);
+    acc = fmaf(k.d, t, acc);
+    return fmaf(-k.dmin, u, acc);
 }
 
 }  // namespace mq

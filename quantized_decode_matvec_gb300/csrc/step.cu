@@ -36,8 +36,9 @@ namespace mq {
 // within a launch, zeroed by the host before it), word 1 is the abort word.
 __device__ __forceinline__ void grid_arrive(unsigned* ws)
 {
-    __threadfence();
-    atomicAdd(ws, 1u);
+    // release at GPU scope: orders this CTA's earlier writes (gathered by the
+    // preceding CTA barrier) before the arrival
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ws) : "memory");
 }
 
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p)
@@ -52,14 +53,10 @@ __device__ __forceinline__ bool grid_wait(unsigned* ws, unsigned target, uint64_
 {
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 0;; ++it) {
-        if (ld_acquire_gpu(ws) >= target) {
-            __threadfence();
-            return true;
-        }
-        if (ld_acquire_gpu(ws + 1) != 0) return false;
-        if ((it & 31u) == 31u) {
+        if (ld_acquire_gpu(ws) >= target) return true;
+        if ((it & 15u) == 15u) {
+            if (ld_acquire_gpu(ws + 1) != 0) return false;
             if (global_timer_ns() - t0 > limit_ns) return false;
-            __nanosleep(64);
         }
     }
 }
