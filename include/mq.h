@@ -230,6 +230,40 @@ typedef struct mq_step_shape {
  * whole grid at once. */
 mq_status mq_step(const mq_layer_desc* d_layers, const mq_step_shape* h_shape, void* stream);
 
+/* ---- the FFN without caller scratch --------------------------------------------------
+ * No counterpart in the pages: they describe the FFN kernels, not how a
+ * caller supplies their scratch.  This entry point exists for callers that
+ * cannot allocate device memory for the h_q8 scratch (and the descriptor)
+ * that mq_ffn_gu_silu_down takes: a plugin or custom-op hook inside a host
+ * runtime that owns every device allocation, or an engine that has handed
+ * all free HBM to its cache pool.  It computes the same result as
+ * mq_ffn_gu_silu_down with the same kernels (bit-identical y), taking plain
+ * device pointers instead of a device descriptor:
+ *   W_gu q4_K [2I][H], W_down q4_K [H][I], x fp32 [ncols][H] or NULL (then
+ *   xq q8_0 [ncols][H/32] is read), y fp32 [ncols][y_ld], y_ld >= H;
+ *   the same shape and alignment rules as mq_check_ffn_desc.
+ * Scratch: a fixed device array inside the library, one per device, holding
+ * the descriptor and h_q8.  The call allocates nothing (no cudaMalloc, no
+ * allocating library routine); it launches three kernels on `stream`: one
+ * that writes the descriptor into that array, then the gate/up and the down
+ * kernels.  Nothing in the array has to start at zero: every call rewrites
+ * the descriptor, and the gate/up kernel writes every h_q8 byte that the down
+ * kernel reads.
+ * Limit: ncols * (I/32) * 34 bytes of h_q8 must not exceed
+ * MQ_NOALLOC_HQ8_MAX_BYTES; larger calls return MQ_ERR_UNSUPPORTED before
+ * any device work (use mq_ffn_gu_silu_down with caller scratch for them).
+ * Setup: the first call on each device looks up that device's copy of the
+ * array (the device must be current); make that first call before any stream
+ * capture.  Needs mq_init for the device.
+ * Races: every call on one device uses the same array, so two calls that
+ * overlap on the GPU (two streams, two host threads, or a call in flight
+ * while another runs) race on it and give wrong results; order them on one
+ * stream or by events. */
+#define MQ_NOALLOC_HQ8_MAX_BYTES 131072
+mq_status mq_ffn_gu_silu_down_noalloc(const void* W_gu, const void* W_down, const float* x, const void* xq,
+                                      float* y, int32_t H, int32_t I, int32_t ncols, int32_t y_ld,
+                                      void* stream);
+
 /* ---- test export ---------------------------------------------------------------------
  * The per-32-block integer sums of a matvec, computed by the same device code
  * as the matvec kernel: sumi int32 [ncols][rows][K/32] = sum q4*q8 per block,

@@ -68,6 +68,8 @@ const DeviceInfo* current_device_info()
     return current_dev(&d) == MQ_OK ? d : nullptr;
 }
 
+mq_status record_cuda_error(cudaError_t e) { return cuda_fail(e); }
+
 int variant_policy() { return g_variant_policy; }
 int fault_policy() { return g_fault_policy; }
 

@@ -65,6 +65,8 @@ struct DeviceInfo {
 
 // the calling thread's current device, initialised by mq_init (nullptr otherwise)
 const DeviceInfo* current_device_info();
+// records e for mq_last_cuda_error on the calling thread; returns MQ_ERR_CUDA
+mq_status record_cuda_error(cudaError_t e);
 
 // returns false if the shapes cannot be planned within the device limits
 bool plan_mv(int64_t rows, int K, int ncols, int kind, int I, const DeviceInfo& dev, MvPlan* p);

@@ -52,6 +52,7 @@ MQ_MAX_K_TIMES_NCOLS = 163840
 MQ_STEP_PDL = 1
 MQ_STEP_PERSISTENT = 2
 MQ_STEP_WORKSPACE_BYTES = 256
+MQ_NOALLOC_HQ8_MAX_BYTES = 131072
 
 
 class MvDesc(ctypes.Structure):
@@ -100,6 +101,7 @@ _sig("mq_check_ffn_desc", c_i32, ctypes.POINTER(FfnDesc))
 _sig("mq_ffn_gu_silu_down", c_i32, c_vp, c_i32, c_i32, c_i32, c_vp)
 _sig("mq_ffn_gate_up", c_i32, c_vp, c_i32, c_i32, c_i32, c_vp)
 _sig("mq_step", c_i32, c_vp, ctypes.POINTER(StepShape), c_vp)
+_sig("mq_ffn_gu_silu_down_noalloc", c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_vp)
 _sig("mq_debug_block_sums_q4K_q8_0", c_i32, c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp)
 _sig("mq_debug_set_variant", c_i32, c_i32)
 _sig("mq_debug_set_fault", c_i32, c_i32)
@@ -109,6 +111,7 @@ EXPORTS = ["mq_status_string", "mq_abi_version", "mq_last_cuda_error", "mq_init"
            "mq_q4K_row_bytes", "mq_q8_0_bytes", "mq_quant_block_elems", "mq_quant_block_bytes",
            "mq_concat_rows_feasible", "mq_concat_rows", "mq_quantize_q8_0", "mq_check_mv_desc",
            "mq_matvec_q4K_q8_0", "mq_check_ffn_desc", "mq_ffn_gu_silu_down", "mq_ffn_gate_up", "mq_step",
+           "mq_ffn_gu_silu_down_noalloc",
            "mq_debug_block_sums_q4K_q8_0", "mq_debug_set_variant", "mq_debug_set_fault"]
 
 
@@ -207,6 +210,12 @@ def mq_ffn_gate_up(d_desc: int, H: int, I: int, ncols: int, stream: int = 0) -> 
 
 def mq_step(d_layers: int, shape: StepShape, stream: int = 0) -> int:
     return _lib.mq_step(c_vp(d_layers), ctypes.byref(shape), c_vp(stream))
+
+
+def mq_ffn_gu_silu_down_noalloc(W_gu: int, W_down: int, x: int, xq: int, y: int, H: int, I: int, ncols: int,
+                                y_ld: int, stream: int = 0) -> int:
+    return _lib.mq_ffn_gu_silu_down_noalloc(c_vp(W_gu), c_vp(W_down), c_vp(x), c_vp(xq), c_vp(y), H, I, ncols,
+                                            y_ld, c_vp(stream))
 
 
 def mq_debug_block_sums_q4K_q8_0(d_desc: int, rows: int, K: int, ncols: int, sumi: int, sumq: int,
@@ -344,6 +353,20 @@ def ffn_gu_silu_down(W_gu, W_down, H: int, I: int, x=None, xq=None, debug: bool 
     out["desc"] = upload_struct(d, dev)
     _check(mq_ffn_gu_silu_down(_ptr(out["desc"]), H, I, ncols, _stream(stream)), "mq_ffn_gu_silu_down")
     return out
+
+
+def ffn_gu_silu_down_noalloc(W_gu, W_down, H: int, I: int, x=None, xq=None, y=None, stream=None):
+    """mq_ffn_gu_silu_down_noalloc: the fused FFN with the library's own fixed
+    scratch instead of a caller-owned h_q8 and descriptor.  Returns y [ncols, H]
+    (allocated here by torch unless given)."""
+    torch = _torch()
+    act = x if x is not None else xq
+    ncols = act.shape[0] if act.dim() == 2 else 1
+    if y is None:
+        y = torch.empty((ncols, H), dtype=torch.float32, device=W_gu.device)
+    _check(mq_ffn_gu_silu_down_noalloc(_ptr(W_gu), _ptr(W_down), _ptr(x), _ptr(xq), _ptr(y), H, I, ncols,
+                                       y.shape[-1], _stream(stream)), "mq_ffn_gu_silu_down_noalloc")
+    return y
 
 
 class StepBuffers:
