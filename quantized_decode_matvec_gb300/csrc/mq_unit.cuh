@@ -29,13 +29,34 @@ struct UnitAct {
     int U;  // units per row = K/128
 };
 
-// From q8_0 blocks in global memory (34-byte blocks, 2-byte aligned), threads
-// tid = 0..nthr-1.  sumq_out (nullable, test export): int32 [NC][K/32].
-// kL2Only: read through L2 only (ld.global.cg), for blocks written earlier in
-// the same kernel by other CTAs (the read-only path may hold stale lines).
-template <int NC, bool kL2Only = false>
-__device__ __forceinline__ void stage_units_q8(const uint8_t* __restrict__ xq, int K, UnitAct s, int32_t* sumq_out,
-                                               int tid, int nthr)
+// Staging works one warp per unit: lane l holds codes 4l..4l+3 of the unit,
+// i.e. values 4g..4g+3 (g = l % 8) of the unit's q8_0 block l / 8, which is
+// one 32-bit word of plane l / 4.  The eight lanes of a block reduce its
+// amax / code sum with three xor-shuffles.  tid = 0..nthr-1 are whole warps.
+
+// Stores one lane's four codes (packed, code 4g in the low byte) and, from
+// lane g == 0 of each block, the block's scale pair.
+__device__ __forceinline__ void put_unit_lane(UnitAct s, int c, int u, int lane, uint32_t codes, float dq, int sq)
+{
+    reinterpret_cast<uint32_t*>(s.planes + size_t(c * 8 + (lane >> 2)) * s.U + u)[lane & 3] = codes;
+    if ((lane & 7) == 0) {
+        float* S = reinterpret_cast<float*>(s.scales + (size_t(c) * s.U + u) * 2);
+        S[lane >> 3] = dq;
+        S[4 + (lane >> 3)] = dq * float(sq);
+    }
+}
+
+__device__ __forceinline__ int group8_sum(int v)
+{
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    v += __shfl_xor_sync(0xffffffffu, v, 2);
+    return v + __shfl_xor_sync(0xffffffffu, v, 4);
+}
+
+// q8_0 blocks, one thread per block: the form for a 2-byte aligned xq.
+template <int NC, bool kL2Only>
+__device__ __forceinline__ void stage_units_q8_by_block(const uint8_t* __restrict__ xq, int K, UnitAct s,
+                                                        int32_t* sumq_out, int tid, int nthr)
 {
     const int nq = K / kQK8;
     for (int t = tid; t < NC * nq; t += nthr) {
@@ -61,58 +82,114 @@ __device__ __forceinline__ void stage_units_q8(const uint8_t* __restrict__ xq, i
     }
 }
 
-// From fp32 x: q8_0 quantization (the same warp-level quantizer halves as the
-// stand-alone kernel, hence bit-identical) straight into the unit layout.
-// Whole warps tid = 0..nthr-1.  Each warp takes B blocks at a time and runs
-// their quantizations in lockstep (independent chains), since a single
-// block's amax -> divide -> round -> sum chain is mostly latency.
+// 32-bit load; kL2Only: a plain coherent load (not the read-only path), for
+// blocks written earlier in the same kernel by other CTAs and published by
+// the grid barrier's acquire.
+template <bool kL2Only>
+__device__ __forceinline__ uint32_t ld_word(const uint32_t* p)
+{
+    if (kL2Only) {
+        uint32_t v;
+        asm volatile("ld.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+        return v;
+    }
+    return __ldg(p);
+}
+
+// From q8_0 blocks in global memory (34-byte blocks; column c starts at byte
+// c*K/32*34).  sumq_out (nullable, test export): int32 [NC][K/32].
+// A unit's four blocks are 136 contiguous bytes at byte 136u of its column,
+// 34 words when xq is 4-byte aligned (K % 256 == 0 keeps every column and
+// unit on a word boundary): lanes load words 0..31 and lanes 0, 1 words 32,
+// 33, and each lane gathers its four codes and its block's scale by shuffles.
+template <int NC, bool kL2Only = false>
+__device__ __forceinline__ void stage_units_q8(const uint8_t* __restrict__ xq, int K, UnitAct s, int32_t* sumq_out,
+                                               int tid, int nthr)
+{
+    if (reinterpret_cast<uintptr_t>(xq) & 3) {
+        stage_units_q8_by_block<NC, kL2Only>(xq, K, s, sumq_out, tid, nthr);
+        return;
+    }
+    const int lane = tid & 31, warp = tid >> 5, nw = nthr >> 5;
+    const int nq = K / kQK8, U = s.U;
+    const int slot = lane >> 3, g = lane & 7;
+    const int cb = 34 * slot + 2 + 4 * g;                   // byte of my first code within the unit
+    const int cw = cb >> 2, cw1 = min(cw + 1, 33), csh = (cb & 3) * 8;
+    const int sw = (34 * slot) >> 2, ssh = ((34 * slot) & 3) * 8;  // the block's f16 scale
+    for (int c = 0; c < NC; ++c) {
+        const uint32_t* col = reinterpret_cast<const uint32_t*>(xq + size_t(c) * nq * kQ8Bytes);
+        for (int u = warp; u < U; u += nw) {
+            const uint32_t* p = col + size_t(u) * 34;
+            const uint32_t w0 = ld_word<kL2Only>(p + lane);
+            const uint32_t w1 = lane < 2 ? ld_word<kL2Only>(p + 32 + lane) : 0u;
+            const uint32_t a0 = __shfl_sync(0xffffffffu, w0, cw & 31), a1 = __shfl_sync(0xffffffffu, w1, cw & 31);
+            const uint32_t b0 = __shfl_sync(0xffffffffu, w0, cw1 & 31), b1 = __shfl_sync(0xffffffffu, w1, cw1 & 31);
+            const uint32_t s0 = __shfl_sync(0xffffffffu, w0, sw);
+            const uint32_t lo = cw < 32 ? a0 : a1, hi = cw1 < 32 ? b0 : b1;
+            const uint32_t codes = csh ? __funnelshift_r(lo, hi, csh) : lo;
+            const uint16_t sbits = uint16_t(s0 >> ssh);
+            const int sq = group8_sum(__dp4a(int(codes), 0x01010101, 0));
+            put_unit_lane(s, c, u, lane, codes, __half2float(__ushort_as_half(sbits)), sq);
+            if (sumq_out && g == 0) sumq_out[size_t(c) * nq + 4 * u + slot] = sq;
+        }
+    }
+}
+
+// From fp32 x: q8_0 quantization straight into the unit layout (the same
+// quantizer as the stand-alone kernel, hence bit-identical).  Optionally
+// also writes the q8_0 blocks to xq_out (2-byte aligned) and the code sums
+// to sumq_out.  Lane l loads values 4l..4l+3 of the unit (one 16-byte load
+// when x is 16-byte aligned).
 template <int NC>
 __device__ __forceinline__ void stage_units_x(const float* __restrict__ x, int K, UnitAct s,
                                               uint8_t* __restrict__ xq_out, int32_t* sumq_out, int tid, int nthr)
 {
-    constexpr int B = 8;
-    const int nq = K / kQK8;
     const int lane = tid & 31, warp = tid >> 5, nw = nthr >> 5;
-    const int total = NC * nq;
-    for (int t0 = warp * B; t0 < total; t0 += nw * B) {
-        float v[B], d[B];
-        int q[B], sq[B];
-#pragma unroll
-        for (int b = 0; b < B; ++b) {
-            const int t = t0 + b;
-            v[b] = 0.0f;
-            if (t < total) {
-                const int c = t / nq, J = t - c * nq;
-                v[b] = __ldg(x + size_t(c) * K + size_t(J) * kQK8 + lane);
+    const int nq = K / kQK8, U = s.U;
+    const int slot = lane >> 3, g = lane & 7;
+    const bool vec = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+    for (int c = 0; c < NC; ++c) {
+        const float* col = x + size_t(c) * K;
+        for (int u = warp; u < U; u += nw) {
+            const float* p = col + size_t(u) * kUnitElems + 4 * lane;
+            const float4 v = vec ? __ldg(reinterpret_cast<const float4*>(p))
+                                 : make_float4(__ldg(p), __ldg(p + 1), __ldg(p + 2), __ldg(p + 3));
+            unsigned m = max(max(__float_as_uint(fabsf(v.x)), __float_as_uint(fabsf(v.y))),
+                             max(__float_as_uint(fabsf(v.z)), __float_as_uint(fabsf(v.w))));
+            m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            m = max(m, __shfl_xor_sync(0xffffffffu, m, 4));
+            const Q8Scale sc = q8_scale_of(__uint_as_float(m));
+            int q0, q1, q2, q3;
+            bool ok = q8_code_fast(v.x, sc, &q0);
+            ok &= q8_code_fast(v.y, sc, &q1);
+            ok &= q8_code_fast(v.z, sc, &q2);
+            ok &= q8_code_fast(v.w, sc, &q3);
+            uint32_t codes = (uint32_t(q0) & 0xffu) | ((uint32_t(q1) & 0xffu) << 8) |
+                             ((uint32_t(q2) & 0xffu) << 16) | (uint32_t(q3) << 24);
+            int qs = q0 + q1 + q2 + q3;
+            if (!ok) {  // rare: redo the four codes with the IEEE division
+                codes = 0;
+                qs = 0;
+#pragma unroll 1
+                for (int i = 0; i < 4; ++i) {
+                    const float xi = i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+                    const int qi = q8_code_exact(xi, sc.d);
+                    codes |= (uint32_t(qi) & 0xffu) << (8 * i);
+                    qs += qi;
+                }
             }
-        }
-#pragma unroll
-        for (int b = 0; b < B; ++b) d[b] = q8_block_scale(v[b]);
-#pragma unroll
-        for (int b = 0; b < B; ++b) q[b] = q8_code(v[b], d[b]);
-#pragma unroll
-        for (int b = 0; b < B; ++b) sq[b] = __reduce_add_sync(0xffffffffu, q[b]);
-#pragma unroll
-        for (int b = 0; b < B; ++b) {
-            const int t = t0 + b;
-            if (t < total) {
-                const int c = t / nq, J = t - c * nq;
-                const __half dh = __float2half_rn(d[b]);
-                const float dq = __half2float(dh);
-                const int u = J >> 2, slot = J & 3;
-                uint8_t* P = reinterpret_cast<uint8_t*>(s.planes + size_t(c * 8 + 2 * slot + (lane >> 4)) * s.U + u);
-                P[lane & 15] = uint8_t(int8_t(q[b]));
-                if (lane == 0) {
-                    float* S = reinterpret_cast<float*>(s.scales + (size_t(c) * s.U + u) * 2);
-                    S[slot] = dq;
-                    S[4 + slot] = dq * float(sq[b]);
-                    if (sumq_out) sumq_out[size_t(c) * nq + J] = sq[b];
-                }
-                if (xq_out) {
-                    uint8_t* ob = xq_out + (size_t(c) * nq + J) * kQ8Bytes;
-                    if (lane == 0) *reinterpret_cast<uint16_t*>(ob) = __half_as_ushort(dh);
-                    ob[2 + lane] = uint8_t(int8_t(q[b]));
-                }
+            const int sq = group8_sum(qs);
+            const __half dh = __float2half_rn(sc.d);
+            put_unit_lane(s, c, u, lane, codes, __half2float(dh), sq);
+            const int J = 4 * u + slot;
+            if (sumq_out && g == 0) sumq_out[size_t(c) * nq + J] = sq;
+            if (xq_out) {
+                uint8_t* ob = xq_out + (size_t(c) * nq + J) * kQ8Bytes;
+                if (g == 0) *reinterpret_cast<uint16_t*>(ob) = __half_as_ushort(dh);
+                uint16_t* o = reinterpret_cast<uint16_t*>(ob + 2 + 4 * g);
+                o[0] = uint16_t(codes);
+                o[1] = uint16_t(codes >> 16);
             }
         }
     }

@@ -65,3 +65,39 @@ def test_empty_is_noop(cuda_ready):
     out = mq.quantize_q8_0(x)
     torch.cuda.synchronize()
     assert out.shape == (0, 68)
+
+
+def _near_tie_blocks(n_blocks: int, seed: int) -> np.ndarray:
+    """Blocks whose values sit within a few ulps of (k + 1/2) * d, d = fp32(amax/127):
+    the cases where an approximate quotient could round to the wrong code.  The
+    first value of each block is +-amax, so every block keeps its own scale."""
+    rng = np.random.default_rng(seed)
+    amax = (rng.uniform(0.5, 2.0, n_blocks) * 10.0 ** rng.integers(-12, 13, n_blocks)).astype(np.float32)
+    d = (amax / np.float32(127)).astype(np.float32)
+    k = rng.integers(-127, 127, (n_blocks, 31)).astype(np.float32) + np.float32(0.5)
+    c = (k * d[:, None]).astype(np.float32)
+    # half within 3 ulps (the exact division decides), half within 400 ulps (mostly the fast path)
+    span = np.where(rng.random(c.shape) < 0.5, 3, 400)
+    off = np.rint((rng.random(c.shape) * 2 - 1) * span).astype(np.int32)
+    nudged = (c.view(np.int32) + off).view(np.float32)
+    x = np.where(np.abs(nudged) <= amax[:, None], nudged, c)
+    x = np.where(np.abs(x) <= amax[:, None], x, np.float32(0))
+    sign = np.where(rng.random(n_blocks) < 0.5, np.float32(-1), np.float32(1))
+    return np.concatenate([(sign * amax)[:, None], x], axis=1).astype(np.float32)
+
+
+@pytest.mark.parametrize("seed", [1, 2])
+def test_near_tie_codes_bit_exact(cuda_ready, seed):
+    """Values next to code boundaries, through the stand-alone quantizer and
+    through the quantization fused into the matvec's staging (its q8_0 copy)."""
+    import torch
+    mq = cuda_ready
+    x = _near_tie_blocks(4096, seed).reshape(1, -1)       # K = 131072
+    ref = oracle.quantize_q8_0(x)
+    assert np.array_equal(_gpu_quant(mq, x), ref)
+    K = x.shape[1]
+    W = torch.from_numpy(synth.q4K_matrix(8, K, seed=seed)).cuda()
+    xq_out = torch.zeros((1, K // 32 * 34), dtype=torch.uint8, device="cuda")
+    mq.matvec_q4K_q8_0(W, 8, K, x=torch.from_numpy(x).cuda(), xq_out=xq_out)
+    torch.cuda.synchronize()
+    assert np.array_equal(xq_out.cpu().numpy(), ref)
