@@ -305,6 +305,9 @@ def run_ours(args):
     device = torch.device("cuda", torch.cuda.current_device())
     mq.init(device.index)
     case = synth.STEP_7B
+    if args.layers != case.n_layers:  # profiling aid: the same layers, fewer of them (not the bench workload)
+        import dataclasses
+        case = dataclasses.replace(case, name=f"{case.name}_slice{args.layers}L", n_layers=args.layers)
     wbytes = synth.weight_bytes_step(case)
     per_layer = wbytes // case.n_layers
 
@@ -425,7 +428,7 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": ms, "step_us": ms * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
             "config": {
-                "workload": f"{case.name}: 28 layers x (q|k|v 4608x3584, o 3584x3584, ffn_gu 37888x3584 + "
+                "workload": f"{case.name}: {case.n_layers} layers x (q|k|v 4608x3584, o 3584x3584, ffn_gu 37888x3584 + "
                             f"SiLU*mul + q8_0(h), down 3584x18944), batch 1, one CUDA graph replay per step",
                 "weight_bytes_per_step": wbytes, "weight_bytes_per_layer": per_layer,
                 "l2": "inputs larger than L2 (3.67 GB of weights per step vs 129 MB L2); no flush",
@@ -456,6 +459,8 @@ def main(argv=None):
     ap.add_argument("--mode", choices=["persistent", "graph", "pdl"], default="pdl",
                     help="step launch mode: one persistent kernel, or four kernels per layer (plain or PDL)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=28,
+                    help="layers of the 7B stack (28 = the bench workload; fewer only for small profiling runs)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
