@@ -259,6 +259,11 @@ bool plan_step(const mq_step_shape& h, const DeviceInfo& dev, StepPlan* out)
         q.grid = int(G);
     }
     sp.n_layers = h.n_layers;
+    // L2 prefetch window: the whole grid's prefetched tiles take at most a
+    // third of the L2 (wider windows measured slower on GB300: they evict
+    // prefetched tiles before use and crowd the critical path's loads)
+    int64_t pf = int64_t(dev.l2_bytes) / 3 / (G * stage);
+    sp.pf_tiles = int(pf < 0 ? 0 : (pf > 16 ? 16 : pf));
     sp.nwc = wmax;
     sp.grid = int(G);
     sp.smem = int(off_vals + vals);
@@ -322,6 +327,7 @@ mq_status mq_init(int device)
     mq_status st = MQ_OK;
     do {
         if ((e = cudaDeviceGetAttribute(&info.num_sms, cudaDevAttrMultiProcessorCount, device)) != cudaSuccess) break;
+        if ((e = cudaDeviceGetAttribute(&info.l2_bytes, cudaDevAttrL2CacheSize, device)) != cudaSuccess) break;
         if ((e = cudaDeviceGetAttribute(&info.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device)) !=
             cudaSuccess)
             break;

@@ -41,6 +41,7 @@ struct StepPlan {
     int K[4];      // reduction length per phase
     int R[4];      // rows per phase (gate/up: I)
     int n_layers;
+    int pf_tiles;  // tiles the producer prefetches into L2 beyond its next ring copy
     int nwc;       // consumer warps of the kernel (phases may use fewer)
     int grid;
     int smem;
@@ -59,6 +60,7 @@ int variant_policy();
 struct DeviceInfo {
     int num_sms = 0;
     int max_smem_optin = 0;
+    int l2_bytes = 0;
     unsigned* status = nullptr;  // device status word
     bool ready = false;
 };

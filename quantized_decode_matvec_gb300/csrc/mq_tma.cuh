@@ -95,6 +95,13 @@ __device__ __forceinline__ void bulk_copy_g2s_evict_first(void* dst, const void*
         : "memory");
 }
 
+// Hint: bring `bytes` (multiple of 16, 16-byte aligned) of global memory
+// into L2.  Nothing waits for it and it changes no result.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_first()
 {
     uint64_t pol;

@@ -111,26 +111,47 @@ __device__ __forceinline__ void stage_units_q8(const uint8_t* __restrict__ xq, i
         return;
     }
     const int lane = tid & 31, warp = tid >> 5, nw = nthr >> 5;
-    const int nq = K / kQK8, U = s.U;
+    const int nq = K / kQK8, U = s.U, total = NC * U;
     const int slot = lane >> 3, g = lane & 7;
     const int cb = 34 * slot + 2 + 4 * g;                   // byte of my first code within the unit
     const int cw = cb >> 2, cw1 = min(cw + 1, 33), csh = (cb & 3) * 8;
     const int sw = (34 * slot) >> 2, ssh = ((34 * slot) & 3) * 8;  // the block's f16 scale
-    for (int c = 0; c < NC; ++c) {
-        const uint32_t* col = reinterpret_cast<const uint32_t*>(xq + size_t(c) * nq * kQ8Bytes);
-        for (int u = warp; u < U; u += nw) {
-            const uint32_t* p = col + size_t(u) * 34;
-            const uint32_t w0 = ld_word<kL2Only>(p + lane);
-            const uint32_t w1 = lane < 2 ? ld_word<kL2Only>(p + 32 + lane) : 0u;
-            const uint32_t a0 = __shfl_sync(0xffffffffu, w0, cw & 31), a1 = __shfl_sync(0xffffffffu, w1, cw & 31);
-            const uint32_t b0 = __shfl_sync(0xffffffffu, w0, cw1 & 31), b1 = __shfl_sync(0xffffffffu, w1, cw1 & 31);
-            const uint32_t s0 = __shfl_sync(0xffffffffu, w0, sw);
+    // A warp takes kBatch units at a time and runs each step for all of them
+    // before the next (independent chains: the shuffle latencies overlap).
+    constexpr int kBatch = 4;
+    for (int base = warp; base < total; base += nw * kBatch) {
+        uint32_t w0[kBatch], w1[kBatch], codes[kBatch], sb[kBatch];
+        int sq[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int t = min(base + i * nw, total - 1);  // a tail batch repeats the last unit (stored once)
+            const uint32_t* p = reinterpret_cast<const uint32_t*>(xq) + size_t(t) * 34;  // units of all columns are contiguous
+            w0[i] = ld_word<kL2Only>(p + lane);
+            w1[i] = lane < 2 ? ld_word<kL2Only>(p + 32 + lane) : 0u;
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const uint32_t a0 = __shfl_sync(0xffffffffu, w0[i], cw & 31), a1 = __shfl_sync(0xffffffffu, w1[i], cw & 31);
+            const uint32_t b0 = __shfl_sync(0xffffffffu, w0[i], cw1 & 31), b1 = __shfl_sync(0xffffffffu, w1[i], cw1 & 31);
+            sb[i] = __shfl_sync(0xffffffffu, w0[i], sw);
             const uint32_t lo = cw < 32 ? a0 : a1, hi = cw1 < 32 ? b0 : b1;
-            const uint32_t codes = csh ? __funnelshift_r(lo, hi, csh) : lo;
-            const uint16_t sbits = uint16_t(s0 >> ssh);
-            const int sq = group8_sum(__dp4a(int(codes), 0x01010101, 0));
-            put_unit_lane(s, c, u, lane, codes, __half2float(__ushort_as_half(sbits)), sq);
-            if (sumq_out && g == 0) sumq_out[size_t(c) * nq + 4 * u + slot] = sq;
+            codes[i] = csh ? __funnelshift_r(lo, hi, csh) : lo;
+            sq[i] = __dp4a(int(codes[i]), 0x01010101, 0);
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) sq[i] += __shfl_xor_sync(0xffffffffu, sq[i], 1);
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) sq[i] += __shfl_xor_sync(0xffffffffu, sq[i], 2);
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) sq[i] += __shfl_xor_sync(0xffffffffu, sq[i], 4);
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int t = base + i * nw;
+            if (t < total) {
+                const int c = t / U, u = t - c * U;
+                put_unit_lane(s, c, u, lane, codes[i], __half2float(__ushort_as_half(uint16_t(sb[i] >> ssh))), sq[i]);
+                if (sumq_out && g == 0) sumq_out[size_t(c) * nq + 4 * u + slot] = sq[i];
+            }
         }
     }
 }
@@ -145,51 +166,84 @@ __device__ __forceinline__ void stage_units_x(const float* __restrict__ x, int K
                                               uint8_t* __restrict__ xq_out, int32_t* sumq_out, int tid, int nthr)
 {
     const int lane = tid & 31, warp = tid >> 5, nw = nthr >> 5;
-    const int nq = K / kQK8, U = s.U;
+    const int nq = K / kQK8, U = s.U, total = NC * U;
     const int slot = lane >> 3, g = lane & 7;
     const bool vec = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
-    for (int c = 0; c < NC; ++c) {
-        const float* col = x + size_t(c) * K;
-        for (int u = warp; u < U; u += nw) {
-            const float* p = col + size_t(u) * kUnitElems + 4 * lane;
-            const float4 v = vec ? __ldg(reinterpret_cast<const float4*>(p))
-                                 : make_float4(__ldg(p), __ldg(p + 1), __ldg(p + 2), __ldg(p + 3));
-            unsigned m = max(max(__float_as_uint(fabsf(v.x)), __float_as_uint(fabsf(v.y))),
-                             max(__float_as_uint(fabsf(v.z)), __float_as_uint(fabsf(v.w))));
-            m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-            m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-            m = max(m, __shfl_xor_sync(0xffffffffu, m, 4));
-            const Q8Scale sc = q8_scale_of(__uint_as_float(m));
+    // A warp takes kBatch units at a time and runs each step for all of them
+    // before the next (independent chains: the shuffle latencies overlap).
+    constexpr int kBatch = 2;
+    for (int base = warp; base < total; base += nw * kBatch) {
+        float4 v[kBatch];
+        unsigned m[kBatch];
+        Q8Scale sc[kBatch];
+        uint32_t codes[kBatch];
+        int qs[kBatch];
+        bool ok = true;
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int t = min(base + i * nw, total - 1);  // a tail batch repeats the last unit (stored once)
+            const float* p = x + size_t(t) * kUnitElems + 4 * lane;  // units of all columns are contiguous
+            v[i] = vec ? __ldg(reinterpret_cast<const float4*>(p))
+                       : make_float4(__ldg(p), __ldg(p + 1), __ldg(p + 2), __ldg(p + 3));
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i)
+            m[i] = max(max(__float_as_uint(fabsf(v[i].x)), __float_as_uint(fabsf(v[i].y))),
+                       max(__float_as_uint(fabsf(v[i].z)), __float_as_uint(fabsf(v[i].w))));
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) m[i] = max(m[i], __shfl_xor_sync(0xffffffffu, m[i], 1));
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) m[i] = max(m[i], __shfl_xor_sync(0xffffffffu, m[i], 2));
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) m[i] = max(m[i], __shfl_xor_sync(0xffffffffu, m[i], 4));
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            sc[i] = q8_scale_of(__uint_as_float(m[i]));
             int q0, q1, q2, q3;
-            bool ok = q8_code_fast(v.x, sc, &q0);
-            ok &= q8_code_fast(v.y, sc, &q1);
-            ok &= q8_code_fast(v.z, sc, &q2);
-            ok &= q8_code_fast(v.w, sc, &q3);
-            uint32_t codes = (uint32_t(q0) & 0xffu) | ((uint32_t(q1) & 0xffu) << 8) |
-                             ((uint32_t(q2) & 0xffu) << 16) | (uint32_t(q3) << 24);
-            int qs = q0 + q1 + q2 + q3;
-            if (!ok) {  // rare: redo the four codes with the IEEE division
-                codes = 0;
-                qs = 0;
+            ok &= q8_code_fast(v[i].x, sc[i], &q0);
+            ok &= q8_code_fast(v[i].y, sc[i], &q1);
+            ok &= q8_code_fast(v[i].z, sc[i], &q2);
+            ok &= q8_code_fast(v[i].w, sc[i], &q3);
+            codes[i] = (uint32_t(q0) & 0xffu) | ((uint32_t(q1) & 0xffu) << 8) | ((uint32_t(q2) & 0xffu) << 16) |
+                       (uint32_t(q3) << 24);
+            qs[i] = q0 + q1 + q2 + q3;
+        }
+        if (!ok) {  // rare: this lane redoes its codes with the IEEE division
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i) {
+                codes[i] = 0;
+                qs[i] = 0;
 #pragma unroll 1
-                for (int i = 0; i < 4; ++i) {
-                    const float xi = i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
-                    const int qi = q8_code_exact(xi, sc.d);
-                    codes |= (uint32_t(qi) & 0xffu) << (8 * i);
-                    qs += qi;
+                for (int e = 0; e < 4; ++e) {
+                    const float xe = e == 0 ? v[i].x : (e == 1 ? v[i].y : (e == 2 ? v[i].z : v[i].w));
+                    const int qe = q8_code_exact(xe, sc[i].d);
+                    codes[i] |= (uint32_t(qe) & 0xffu) << (8 * e);
+                    qs[i] += qe;
                 }
             }
-            const int sq = group8_sum(qs);
-            const __half dh = __float2half_rn(sc.d);
-            put_unit_lane(s, c, u, lane, codes, __half2float(dh), sq);
-            const int J = 4 * u + slot;
-            if (sumq_out && g == 0) sumq_out[size_t(c) * nq + J] = sq;
-            if (xq_out) {
-                uint8_t* ob = xq_out + (size_t(c) * nq + J) * kQ8Bytes;
-                if (g == 0) *reinterpret_cast<uint16_t*>(ob) = __half_as_ushort(dh);
-                uint16_t* o = reinterpret_cast<uint16_t*>(ob + 2 + 4 * g);
-                o[0] = uint16_t(codes);
-                o[1] = uint16_t(codes >> 16);
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) qs[i] += __shfl_xor_sync(0xffffffffu, qs[i], 1);
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) qs[i] += __shfl_xor_sync(0xffffffffu, qs[i], 2);
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) qs[i] += __shfl_xor_sync(0xffffffffu, qs[i], 4);
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int t = base + i * nw;
+            if (t < total) {
+                const int c = t / U, u = t - c * U;
+                const __half dh = __float2half_rn(sc[i].d);
+                put_unit_lane(s, c, u, lane, codes[i], __half2float(dh), qs[i]);
+                const int J = 4 * u + slot;
+                if (sumq_out && g == 0) sumq_out[size_t(c) * nq + J] = qs[i];
+                if (xq_out) {
+                    uint8_t* ob = xq_out + (size_t(c) * nq + J) * kQ8Bytes;
+                    if (g == 0) *reinterpret_cast<uint16_t*>(ob) = __half_as_ushort(dh);
+                    uint16_t* o = reinterpret_cast<uint16_t*>(ob + 2 + 4 * g);
+                    o[0] = uint16_t(codes[i]);
+                    o[1] = uint16_t(codes[i] >> 16);
+                }
             }
         }
     }

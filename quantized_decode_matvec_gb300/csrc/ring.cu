@@ -119,7 +119,8 @@ __global__ void __launch_bounds__(32 * ring_max_warps<NC>(), 1)
 
     int issued = 0;  // tiles issued (producer lane 0)
     if (warp == p.nwc) {
-        // ---- producer
+        // ---- producer; each weight byte is read once: evict-first in L2
+        const uint64_t wpolicy = l2_policy_evict_first();
         auto issue = [&](int i) {
             if (i == withheld) return;
             const int s = i % p.ns;
@@ -131,8 +132,8 @@ __global__ void __launch_bounds__(32 * ring_max_warps<NC>(), 1)
             while (a < e) {  // one copy per run of contiguous matrix rows (gate/up: at most two)
                 int stop = e;
                 if (KIND == KIND_GU && a < n && e > n) stop = n;
-                bulk_copy_g2s(dst + size_t(a - lr0) * row_bytes, W + size_t(rowmap(a)) * row_bytes,
-                              uint32_t(size_t(stop - a) * row_bytes), &full[s]);
+                bulk_copy_g2s_evict_first(dst + size_t(a - lr0) * row_bytes, W + size_t(rowmap(a)) * row_bytes,
+                                          uint32_t(size_t(stop - a) * row_bytes), &full[s], wpolicy);
                 a = stop;
             }
         };

@@ -126,6 +126,86 @@ __device__ __forceinline__ PhaseRows phase_rows(const StepPlan& sp, int ph, int 
     return r;
 }
 
+// plan values of a phase known only at run time, without indexing the plan
+// (a run-time index into the parameter struct would copy it to local memory)
+__device__ __forceinline__ int sel4(int ph, int a, int b, int c, int d)
+{
+    return ph == 0 ? a : (ph == 1 ? b : (ph == 2 ? c : d));
+}
+
+// The producer's L2 prefetcher: walks the CTA's tile sequence (layer, phase,
+// tile) ahead of the ring, so HBM keeps streaming while the ring is full
+// (barrier waits, staging, epilogues).  A prefetch is only a hint: it moves
+// data from HBM into L2 and changes nothing else.
+struct TileWalker {
+    int l, ph, t, ntiles, T;
+    int64_t g;  // position in the ring's tile sequence
+    PhaseRows pr;
+    const uint8_t* W;
+    uint32_t row_bytes;
+    bool done;
+
+    // settle on the first phase at or after (l, ph) that has tiles
+    __device__ __forceinline__ void enter(const mq_layer_desc* layers, const StepPlan& sp, int b, int G, int nc)
+    {
+        for (;;) {
+            if (l >= sp.n_layers) {
+                done = true;
+                return;
+            }
+            T = sel4(ph, sp.ph[0].T, sp.ph[1].T, sp.ph[2].T, sp.ph[3].T);
+            const int K = sel4(ph, sp.K[0], sp.K[1], sp.K[2], sp.K[3]);
+            const int R = sel4(ph, sp.R[0], sp.R[1], sp.R[2], sp.R[3]);
+            pr = PhaseRows{};
+            pr.R = R;
+            pr.gu = (ph == 2);
+            if (pr.gu) {
+                const int nblk = R / kQK8;
+                const int b0 = int(int64_t(b) * nblk / G), b1 = int(int64_t(b + 1) * nblk / G);
+                pr.i0 = b0 * kQK8;
+                pr.n = (b1 - b0) * kQK8;
+                pr.nrows = 2 * pr.n;
+            } else {
+                pr.r0 = int(int64_t(b) * R / G);
+                pr.nrows = int(int64_t(b + 1) * R / G) - pr.r0;
+            }
+            const PhaseJob j = phase_job(&layers[l], ph);
+            W = j.W;
+            row_bytes = uint32_t(K / kQK) * kQ4KBytes;
+            ntiles = (pr.nrows + T - 1) / T;
+            t = 0;
+            // the phase's activation too, where it is an fp32 input on a 16-byte boundary
+            if (ph < 3 && j.x && (reinterpret_cast<uintptr_t>(j.x) & 15) == 0) prefetch_l2(j.x, uint32_t(nc) * K * 4);
+            if (ntiles > 0) return;
+            if (++ph == 4) {
+                ph = 0;
+                ++l;
+            }
+        }
+    }
+
+    // prefetch the current tile and step to the next
+    __device__ __forceinline__ void step(const mq_layer_desc* layers, const StepPlan& sp, int b, int G, int nc)
+    {
+        const int lr0 = t * T, e = min(lr0 + T, pr.nrows);
+        int a = lr0;
+        while (a < e) {
+            int stop = e;
+            if (pr.gu && a < pr.n && e > pr.n) stop = pr.n;
+            prefetch_l2(W + size_t(pr.map(a)) * row_bytes, uint32_t(stop - a) * row_bytes);
+            a = stop;
+        }
+        ++g;
+        if (++t == ntiles) {
+            if (++ph == 4) {
+                ph = 0;
+                ++l;
+            }
+            enter(layers, sp, b, G, nc);
+        }
+    }
+};
+
 // device-side re-check of every layer descriptor against the step plan
 __device__ __forceinline__ unsigned check_layers(const mq_layer_desc* layers, const StepPlan& sp, int nc)
 {
@@ -186,6 +266,11 @@ __global__ void __launch_bounds__(32 * ring_max_warps<NC>(), 1)
     int issued = 0;  // tiles issued by the producer (lane 0 of the producer warp)
     if (warp == nwc) {
         // ---- producer: all phases' tiles, back to back
+        TileWalker pf{};
+        if (lane == 0) pf.enter(layers, sp, b, G, NC);
+        // each weight byte is read once per step: its ring copy marks it evict-first
+        // in L2, so prefetched tiles and activations stay
+        const uint64_t wpolicy = l2_policy_evict_first();
         auto produce = [&](auto phc, int l) -> bool {
             constexpr int ph = decltype(phc)::value;
             const MvPlan& P = sp.ph[ph];
@@ -195,6 +280,9 @@ __global__ void __launch_bounds__(32 * ring_max_warps<NC>(), 1)
             const int ntiles = (pr.nrows + P.T - 1) / P.T;
             for (int t = 0; t < ntiles; ++t, ++issued) {
                 const int s = issued % P0.ns;
+                // keep the L2 prefetch window pf_tiles ahead of this copy (it also
+                // runs ahead while the wait below blocks)
+                while (!pf.done && pf.g < int64_t(issued) + sp.pf_tiles) pf.step(layers, sp, b, G, NC);
                 if (issued >= P0.ns && !mbar_wait_bounded(&empty[s], uint32_t(issued / P0.ns - 1) & 1u, limit_ns))
                     return false;
                 const int lr0 = t * P.T, tn = min(P.T, pr.nrows - lr0);
@@ -205,8 +293,8 @@ __global__ void __launch_bounds__(32 * ring_max_warps<NC>(), 1)
                 while (a < e) {
                     int stop = e;
                     if (pr.gu && a < pr.n && e > pr.n) stop = pr.n;
-                    bulk_copy_g2s(dst + size_t(a - lr0) * row_bytes, j.W + size_t(pr.map(a)) * row_bytes,
-                                  uint32_t(size_t(stop - a) * row_bytes), &full[s]);
+                    bulk_copy_g2s_evict_first(dst + size_t(a - lr0) * row_bytes, j.W + size_t(pr.map(a)) * row_bytes,
+                                              uint32_t(size_t(stop - a) * row_bytes), &full[s], wpolicy);
                     a = stop;
                 }
             }
