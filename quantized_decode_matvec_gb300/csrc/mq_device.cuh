@@ -99,13 +99,15 @@ __device__ __forceinline__ int q8_code_exact(float x, float d)
 }
 
 // The code from the approximate quotient; false where it cannot be trusted
-// (then the caller takes q8_code_exact).
+// (then the caller takes q8_code_exact).  Away from a tie, adding +-1/2 and
+// truncating rounds half away from zero exactly (the sum cannot land on an
+// integer), and |x/d| <= 127.0001 keeps the result within +-127.
 __device__ __forceinline__ bool q8_code_fast(float x, const Q8Scale& s, int* q)
 {
-    const float qa = x * s.rd, a = fabsf(qa), fl = floorf(a), f = a - fl;
-    const float r = fminf(f > 0.5f ? fl + 1.0f : fl, 127.0f);
-    *q = qa < 0.0f ? -static_cast<int>(r) : static_cast<int>(r);
-    return !s.exact && fabsf(f - 0.5f) > 0x1p-14f;
+    const float qa = x * s.rd;
+    const float a = fabsf(qa);
+    *q = __float2int_rz(qa + copysignf(0.5f, qa));
+    return !s.exact && fabsf(a - floorf(a) - 0.5f) > 0x1p-14f;
 }
 
 // One 32-value block held one value per lane of the warp: returns this

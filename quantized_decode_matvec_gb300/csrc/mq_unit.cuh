@@ -34,17 +34,26 @@ struct UnitAct {
 // one 32-bit word of plane l / 4.  The eight lanes of a block reduce its
 // amax / code sum with three xor-shuffles.  tid = 0..nthr-1 are whole warps.
 
-// Stores one lane's four codes (packed, code 4g in the low byte) and, from
-// lane g == 0 of each block, the block's scale pair.
-__device__ __forceinline__ void put_unit_lane(UnitAct s, int c, int u, int lane, uint32_t codes, float dq, int sq)
-{
-    reinterpret_cast<uint32_t*>(s.planes + size_t(c * 8 + (lane >> 2)) * s.U + u)[lane & 3] = codes;
-    if ((lane & 7) == 0) {
-        float* S = reinterpret_cast<float*>(s.scales + (size_t(c) * s.U + u) * 2);
-        S[lane >> 3] = dq;
-        S[4 + (lane >> 3)] = dq * float(sq);
+// Where one lane's results of unit u go: its code word in plane l / 4, and
+// (lanes g == 0) its block's scale pair.  Lane constants, so the per-unit
+// address is one multiply-add.
+struct UnitLaneOut {
+    uint32_t* code;  // + 4u words
+    float* scale;    // + 8u floats: [slot] = dq, [4 + slot] = dq*sumq
+    __device__ __forceinline__ UnitLaneOut(UnitAct s, int c, int lane)
+    {
+        code = reinterpret_cast<uint32_t*>(s.planes + size_t(c * 8 + (lane >> 2)) * s.U) + (lane & 3);
+        scale = reinterpret_cast<float*>(s.scales + size_t(c) * s.U * 2) + (lane >> 3);
     }
-}
+    __device__ __forceinline__ void put(int u, int lane, uint32_t codes, float dq, int sq) const
+    {
+        code[4 * u] = codes;
+        if ((lane & 7) == 0) {
+            scale[8 * u] = dq;
+            scale[8 * u + 4] = dq * float(sq);
+        }
+    }
+};
 
 __device__ __forceinline__ int group8_sum(int v)
 {
@@ -111,46 +120,46 @@ __device__ __forceinline__ void stage_units_q8(const uint8_t* __restrict__ xq, i
         return;
     }
     const int lane = tid & 31, warp = tid >> 5, nw = nthr >> 5;
-    const int nq = K / kQK8, U = s.U, total = NC * U;
+    const int nq = K / kQK8, U = s.U;
     const int slot = lane >> 3, g = lane & 7;
     const int cb = 34 * slot + 2 + 4 * g;                   // byte of my first code within the unit
     const int cw = cb >> 2, cw1 = min(cw + 1, 33), csh = (cb & 3) * 8;
     const int sw = (34 * slot) >> 2, ssh = ((34 * slot) & 3) * 8;  // the block's f16 scale
-    // A warp takes kBatch units at a time and runs each step for all of them
-    // before the next (independent chains: the shuffle latencies overlap).
-    constexpr int kBatch = 4;
-    for (int base = warp; base < total; base += nw * kBatch) {
-        uint32_t w0[kBatch], w1[kBatch], codes[kBatch], sb[kBatch];
-        int sq[kBatch];
-#pragma unroll
-        for (int i = 0; i < kBatch; ++i) {
-            const int t = min(base + i * nw, total - 1);  // a tail batch repeats the last unit (stored once)
-            const uint32_t* p = reinterpret_cast<const uint32_t*>(xq) + size_t(t) * 34;  // units of all columns are contiguous
-            w0[i] = ld_word<kL2Only>(p + lane);
-            w1[i] = lane < 2 ? ld_word<kL2Only>(p + 32 + lane) : 0u;
-        }
-#pragma unroll
-        for (int i = 0; i < kBatch; ++i) {
-            const uint32_t a0 = __shfl_sync(0xffffffffu, w0[i], cw & 31), a1 = __shfl_sync(0xffffffffu, w1[i], cw & 31);
-            const uint32_t b0 = __shfl_sync(0xffffffffu, w0[i], cw1 & 31), b1 = __shfl_sync(0xffffffffu, w1[i], cw1 & 31);
-            sb[i] = __shfl_sync(0xffffffffu, w0[i], sw);
-            const uint32_t lo = cw < 32 ? a0 : a1, hi = cw1 < 32 ? b0 : b1;
-            codes[i] = csh ? __funnelshift_r(lo, hi, csh) : lo;
-            sq[i] = __dp4a(int(codes[i]), 0x01010101, 0);
-        }
-#pragma unroll
-        for (int i = 0; i < kBatch; ++i) sq[i] += __shfl_xor_sync(0xffffffffu, sq[i], 1);
-#pragma unroll
-        for (int i = 0; i < kBatch; ++i) sq[i] += __shfl_xor_sync(0xffffffffu, sq[i], 2);
-#pragma unroll
-        for (int i = 0; i < kBatch; ++i) sq[i] += __shfl_xor_sync(0xffffffffu, sq[i], 4);
-#pragma unroll
-        for (int i = 0; i < kBatch; ++i) {
-            const int t = base + i * nw;
-            if (t < total) {
-                const int c = t / U, u = t - c * U;
-                put_unit_lane(s, c, u, lane, codes[i], __half2float(__ushort_as_half(uint16_t(sb[i] >> ssh))), sq[i]);
-                if (sumq_out && g == 0) sumq_out[size_t(c) * nq + 4 * u + slot] = sq[i];
+    auto unit = [&](uint32_t w0, uint32_t w1, uint32_t& codes, float& dq) {
+        const uint32_t a0 = __shfl_sync(0xffffffffu, w0, cw & 31), a1 = __shfl_sync(0xffffffffu, w1, cw & 31);
+        const uint32_t b0 = __shfl_sync(0xffffffffu, w0, cw1 & 31), b1 = __shfl_sync(0xffffffffu, w1, cw1 & 31);
+        const uint32_t s0 = __shfl_sync(0xffffffffu, w0, sw);
+        const uint32_t lo = cw < 32 ? a0 : a1, hi = cw1 < 32 ? b0 : b1;
+        codes = csh ? __funnelshift_r(lo, hi, csh) : lo;
+        dq = __half2float(__ushort_as_half(uint16_t(s0 >> ssh)));
+    };
+    for (int c = 0; c < NC; ++c) {
+        const uint32_t* col = reinterpret_cast<const uint32_t*>(xq + size_t(c) * nq * kQ8Bytes);
+        const UnitLaneOut out(s, c, lane);
+        // two units per step, both loads first (a warp's last step may repeat its unit)
+        for (int u = warp; u < U; u += 2 * nw) {
+            const int u2 = u + nw < U ? u + nw : u;
+            const uint32_t* p = col + size_t(u) * 34;
+            const uint32_t* p2 = col + size_t(u2) * 34;
+            const uint32_t w0 = ld_word<kL2Only>(p + lane), v0 = ld_word<kL2Only>(p2 + lane);
+            const uint32_t w1 = lane < 2 ? ld_word<kL2Only>(p + 32 + lane) : 0u;
+            const uint32_t v1 = lane < 2 ? ld_word<kL2Only>(p2 + 32 + lane) : 0u;
+            uint32_t ca, cb2;
+            float da, db;
+            unit(w0, w1, ca, da);
+            unit(v0, v1, cb2, db);
+            int sa = __dp4a(int(ca), 0x01010101, 0), sb = __dp4a(int(cb2), 0x01010101, 0);
+            sa += __shfl_xor_sync(0xffffffffu, sa, 1);
+            sb += __shfl_xor_sync(0xffffffffu, sb, 1);
+            sa += __shfl_xor_sync(0xffffffffu, sa, 2);
+            sb += __shfl_xor_sync(0xffffffffu, sb, 2);
+            sa += __shfl_xor_sync(0xffffffffu, sa, 4);
+            sb += __shfl_xor_sync(0xffffffffu, sb, 4);
+            out.put(u, lane, ca, da, sa);
+            if (u2 != u) out.put(u2, lane, cb2, db, sb);
+            if (sumq_out && g == 0) {
+                sumq_out[size_t(c) * nq + 4 * u + slot] = sa;
+                if (u2 != u) sumq_out[size_t(c) * nq + 4 * u2 + slot] = sb;
             }
         }
     }
@@ -166,84 +175,72 @@ __device__ __forceinline__ void stage_units_x(const float* __restrict__ x, int K
                                               uint8_t* __restrict__ xq_out, int32_t* sumq_out, int tid, int nthr)
 {
     const int lane = tid & 31, warp = tid >> 5, nw = nthr >> 5;
-    const int nq = K / kQK8, U = s.U, total = NC * U;
+    const int nq = K / kQK8, U = s.U;
     const int slot = lane >> 3, g = lane & 7;
     const bool vec = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
-    // A warp takes kBatch units at a time and runs each step for all of them
-    // before the next (independent chains: the shuffle latencies overlap).
-    constexpr int kBatch = 2;
-    for (int base = warp; base < total; base += nw * kBatch) {
-        float4 v[kBatch];
-        unsigned m[kBatch];
-        Q8Scale sc[kBatch];
-        uint32_t codes[kBatch];
-        int qs[kBatch];
-        bool ok = true;
-#pragma unroll
-        for (int i = 0; i < kBatch; ++i) {
-            const int t = min(base + i * nw, total - 1);  // a tail batch repeats the last unit (stored once)
-            const float* p = x + size_t(t) * kUnitElems + 4 * lane;  // units of all columns are contiguous
-            v[i] = vec ? __ldg(reinterpret_cast<const float4*>(p))
-                       : make_float4(__ldg(p), __ldg(p + 1), __ldg(p + 2), __ldg(p + 3));
+    auto load = [&](const float* p) {
+        return vec ? __ldg(reinterpret_cast<const float4*>(p))
+                   : make_float4(__ldg(p), __ldg(p + 1), __ldg(p + 2), __ldg(p + 3));
+    };
+    auto amax8 = [](float4 v) {  // max |x| over the lane's 4 values, then its block's 8 lanes
+        float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        return fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+    };
+    // the lane's four codes, packed (code 4g in the low byte), and their sum
+    auto codes4 = [](float4 v, const Q8Scale& sc, uint32_t& codes, int& qs) {
+        int q0, q1, q2, q3;
+        bool ok = q8_code_fast(v.x, sc, &q0);
+        ok &= q8_code_fast(v.y, sc, &q1);
+        ok &= q8_code_fast(v.z, sc, &q2);
+        ok &= q8_code_fast(v.w, sc, &q3);
+        if (!ok) {  // rare: the IEEE division decides
+            q0 = q8_code_exact(v.x, sc.d);
+            q1 = q8_code_exact(v.y, sc.d);
+            q2 = q8_code_exact(v.z, sc.d);
+            q3 = q8_code_exact(v.w, sc.d);
         }
-#pragma unroll
-        for (int i = 0; i < kBatch; ++i)
-            m[i] = max(max(__float_as_uint(fabsf(v[i].x)), __float_as_uint(fabsf(v[i].y))),
-                       max(__float_as_uint(fabsf(v[i].z)), __float_as_uint(fabsf(v[i].w))));
-#pragma unroll
-        for (int i = 0; i < kBatch; ++i) m[i] = max(m[i], __shfl_xor_sync(0xffffffffu, m[i], 1));
-#pragma unroll
-        for (int i = 0; i < kBatch; ++i) m[i] = max(m[i], __shfl_xor_sync(0xffffffffu, m[i], 2));
-#pragma unroll
-        for (int i = 0; i < kBatch; ++i) m[i] = max(m[i], __shfl_xor_sync(0xffffffffu, m[i], 4));
-#pragma unroll
-        for (int i = 0; i < kBatch; ++i) {
-            sc[i] = q8_scale_of(__uint_as_float(m[i]));
-            int q0, q1, q2, q3;
-            ok &= q8_code_fast(v[i].x, sc[i], &q0);
-            ok &= q8_code_fast(v[i].y, sc[i], &q1);
-            ok &= q8_code_fast(v[i].z, sc[i], &q2);
-            ok &= q8_code_fast(v[i].w, sc[i], &q3);
-            codes[i] = (uint32_t(q0) & 0xffu) | ((uint32_t(q1) & 0xffu) << 8) | ((uint32_t(q2) & 0xffu) << 16) |
-                       (uint32_t(q3) << 24);
-            qs[i] = q0 + q1 + q2 + q3;
-        }
-        if (!ok) {  // rare: this lane redoes its codes with the IEEE division
-#pragma unroll
-            for (int i = 0; i < kBatch; ++i) {
-                codes[i] = 0;
-                qs[i] = 0;
-#pragma unroll 1
-                for (int e = 0; e < 4; ++e) {
-                    const float xe = e == 0 ? v[i].x : (e == 1 ? v[i].y : (e == 2 ? v[i].z : v[i].w));
-                    const int qe = q8_code_exact(xe, sc[i].d);
-                    codes[i] |= (uint32_t(qe) & 0xffu) << (8 * e);
-                    qs[i] += qe;
-                }
+        codes = (uint32_t(q0) & 0xffu) | ((uint32_t(q1) & 0xffu) << 8) | ((uint32_t(q2) & 0xffu) << 16) |
+                (uint32_t(q3) << 24);
+        qs = q0 + q1 + q2 + q3;
+    };
+    for (int c = 0; c < NC; ++c) {
+        const float* col = x + size_t(c) * K + 4 * lane;
+        const UnitLaneOut out(s, c, lane);
+        // two units per step, both loads first (a warp's last step may repeat its unit)
+        for (int u = warp; u < U; u += 2 * nw) {
+            const int u2 = u + nw < U ? u + nw : u;
+            const float4 va = load(col + size_t(u) * kUnitElems), vb = load(col + size_t(u2) * kUnitElems);
+            const float ma = amax8(va), mb = amax8(vb);
+            const Q8Scale sa = q8_scale_of(ma), sb = q8_scale_of(mb);
+            uint32_t ca, cb2;
+            int qa, qb;
+            codes4(va, sa, ca, qa);
+            codes4(vb, sb, cb2, qb);
+            qa += __shfl_xor_sync(0xffffffffu, qa, 1);
+            qb += __shfl_xor_sync(0xffffffffu, qb, 1);
+            qa += __shfl_xor_sync(0xffffffffu, qa, 2);
+            qb += __shfl_xor_sync(0xffffffffu, qb, 2);
+            qa += __shfl_xor_sync(0xffffffffu, qa, 4);
+            qb += __shfl_xor_sync(0xffffffffu, qb, 4);
+            const __half ha = __float2half_rn(sa.d), hb = __float2half_rn(sb.d);
+            out.put(u, lane, ca, __half2float(ha), qa);
+            if (u2 != u) out.put(u2, lane, cb2, __half2float(hb), qb);
+            if (sumq_out && g == 0) {
+                sumq_out[size_t(c) * nq + 4 * u + slot] = qa;
+                if (u2 != u) sumq_out[size_t(c) * nq + 4 * u2 + slot] = qb;
             }
-        }
-#pragma unroll
-        for (int i = 0; i < kBatch; ++i) qs[i] += __shfl_xor_sync(0xffffffffu, qs[i], 1);
-#pragma unroll
-        for (int i = 0; i < kBatch; ++i) qs[i] += __shfl_xor_sync(0xffffffffu, qs[i], 2);
-#pragma unroll
-        for (int i = 0; i < kBatch; ++i) qs[i] += __shfl_xor_sync(0xffffffffu, qs[i], 4);
-#pragma unroll
-        for (int i = 0; i < kBatch; ++i) {
-            const int t = base + i * nw;
-            if (t < total) {
-                const int c = t / U, u = t - c * U;
-                const __half dh = __float2half_rn(sc[i].d);
-                put_unit_lane(s, c, u, lane, codes[i], __half2float(dh), qs[i]);
-                const int J = 4 * u + slot;
-                if (sumq_out && g == 0) sumq_out[size_t(c) * nq + J] = qs[i];
-                if (xq_out) {
-                    uint8_t* ob = xq_out + (size_t(c) * nq + J) * kQ8Bytes;
-                    if (g == 0) *reinterpret_cast<uint16_t*>(ob) = __half_as_ushort(dh);
+            if (xq_out) {
+                auto put_q8 = [&](int uu, __half h, uint32_t cd) {
+                    uint8_t* ob = xq_out + (size_t(c) * nq + 4 * uu + slot) * kQ8Bytes;
+                    if (g == 0) *reinterpret_cast<uint16_t*>(ob) = __half_as_ushort(h);
                     uint16_t* o = reinterpret_cast<uint16_t*>(ob + 2 + 4 * g);
-                    o[0] = uint16_t(codes[i]);
-                    o[1] = uint16_t(codes[i] >> 16);
-                }
+                    o[0] = uint16_t(cd);
+                    o[1] = uint16_t(cd >> 16);
+                };
+                put_q8(u, ha, ca);
+                if (u2 != u) put_q8(u2, hb, cb2);
             }
         }
     }
