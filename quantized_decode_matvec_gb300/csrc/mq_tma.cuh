@@ -115,6 +115,12 @@ __device__ __forceinline__ void named_barrier_sync(int id, int nthreads)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// non-blocking arrival at a named barrier that other warps bar.sync on
+__device__ __forceinline__ void named_barrier_arrive(int id, int nthreads)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 __device__ __forceinline__ uint4 lds16(const uint8_t* p)
 {
     return *reinterpret_cast<const uint4*>(p);

@@ -32,6 +32,9 @@
 
 namespace mq {
 
+// ring tiles a CTA issues before its dependency wait (the rest follow the activation)
+constexpr int kEarlyTiles = 2;
+
 template <int NC, int KIND>
 __global__ void __launch_bounds__(32 * ring_max_warps<NC>(), 1)
     ring_kernel(const void* __restrict__ desc, int a_h, int b_h, MvPlan p, unsigned* status)
@@ -137,11 +140,16 @@ __global__ void __launch_bounds__(32 * ring_max_warps<NC>(), 1)
                 a = stop;
             }
         };
+        // One tile before the dependency wait; the rest only once the consumers
+        // have staged the activation, so the activation's loads are not queued
+        // behind a ring's worth of weight bytes on their way into this SM.
         if (lane == 0)
-            for (; issued < ntiles && issued < p.ns; ++issued) issue(issued);
+            for (; issued < ntiles && issued < kEarlyTiles && issued < p.ns; ++issued) issue(issued);
         __syncwarp();
         griddep_wait();
+        named_barrier_sync(2, (p.nwc + 1) * 32);  // the consumers' staging is done
         if (lane == 0) {
+            for (; issued < ntiles && issued < p.ns; ++issued) issue(issued);
             for (; issued < ntiles; ++issued) {
                 const int s = issued % p.ns;
                 if (abort_flag || !mbar_wait_bounded(&empty[s], uint32_t(issued / p.ns - 1) & 1u, limit_ns)) {
@@ -160,6 +168,7 @@ __global__ void __launch_bounds__(32 * ring_max_warps<NC>(), 1)
         else
             stage_units_q8<NC>(xq, K, act, nullptr, ctid, cthr);
         named_barrier_sync(1, cthr);
+        named_barrier_arrive(2, cthr + 32);  // release the producer's remaining ring tiles
         if (!ring_consume<NC>(p, nrows, 0, p.nwc, ring, full, empty, act, part, limit_ns) && lane == 0) abort_flag = 1;
     }
     __syncthreads();
