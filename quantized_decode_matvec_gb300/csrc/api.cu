@@ -155,6 +155,9 @@ void plan_ring(MvPlan& q0, int64_t units, int kind, int nc, const DeviceInfo& de
     int64_t T = 2 * rg * m;
     const int64_t rpc_round = (q.rows_per_cta + 2 * rg - 1) / (2 * rg) * (2 * rg);
     if (T > rpc_round) T = rpc_round;
+    // a CTA's few rows beyond one tile (q|k|v: 31 rows, tiles of 30) ride in
+    // that tile rather than in a tile of their own
+    if (q.rows_per_cta > T && q.rows_per_cta * row_bytes <= 65536) T = q.rows_per_cta;
     const int64_t stage = (T * row_bytes + 127) / 128 * 128;
     const int64_t act = int64_t(nc) * q.C * 160;
     const int64_t part = int64_t(q.rows_per_cta) * q.nseg * nc * 4;
@@ -228,6 +231,7 @@ bool plan_step(const mq_step_shape& h, const DeviceInfo& dev, StepPlan* out)
         int64_t T = 2 * int64_t(q.rg) * m;
         const int64_t rpc_round = (rpc + 2 * q.rg - 1) / (2 * q.rg) * (2 * q.rg);
         if (T > rpc_round) T = rpc_round;
+        if (rpc > T && rpc * row_bytes <= 65536) T = rpc;  // a few rows beyond one tile ride in it
         q.T = int(T);
         q.rows_per_cta = int(rpc);
         q.variant = 1;
