@@ -78,7 +78,7 @@ def barrier():
 class ClockSampler:
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,timestamp")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -90,11 +90,15 @@ class ClockSampler:
             fd, self.path = tempfile.mkstemp(prefix="mq_clocks_", suffix=".csv")
             self.fh = os.fdopen(fd, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
         time.sleep(0.3)
+
+    def mark(self):
+        """Host time of the timed region's start (first call) and end (second call)."""
+        self.window = getattr(self, "window", []) + [time.time()]
 
     def stop(self):
         if self.proc is None:
@@ -107,11 +111,20 @@ class ClockSampler:
         self.fh.close()
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        lo, hi = (self.window[0], self.window[-1]) if len(getattr(self, "window", [])) >= 2 else (None, None)
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
+                if lo is not None:  # keep the samples taken inside the timed region
+                    try:
+                        import datetime
+                        ts = datetime.datetime.strptime(parts[9], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                        if ts < lo - 0.05 or ts > hi + 0.05:
+                            continue
+                    except ValueError:
+                        pass
                 try:
                     sm.append(float(parts[1]))
                     smax.append(float(parts[2]))
@@ -333,8 +346,10 @@ def run_ours(args):
     clocks.start()
     barrier()
     torch.cuda.synchronize()
+    clocks.mark()
     per_step = time_replays(g.run, stream, args.steps)
     torch.cuda.synchronize()
+    clocks.mark()
     barrier()
     clk = clocks.stop()
     ms_local = sum(per_step) / len(per_step)
@@ -453,7 +468,7 @@ def run_ours(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--mode", choices=["persistent", "graph", "pdl"], default="pdl",
