@@ -303,6 +303,120 @@ def run_reference(args):
 # the GPU arm
 # ---------------------------------------------------------------------------------------------------------
 
+def config_suite(mq, device):
+    """The other workloads of the matvec, each timed on its own (context for the step's number).
+
+    Every call is captured in a CUDA graph and replayed; times are CUDA events around whole
+    replays (per-call = replay / calls).  Workloads smaller than twice the L2 are timed on
+    rotated device copies of the same weights, so each call streams its weights from HBM;
+    the single matvec is also reported warm (its 295 KB stay in L2).
+    """
+    import torch
+    from quantized_decode_matvec_gb300 import synth
+    l2 = 2 * 129 * 1024 * 1024
+    out = {}
+    stream = torch.cuda.Stream(device)
+
+    def timed(calls, reps=10):
+        """median per-call ms of a graph holding `calls` (a list of zero-arg launches)."""
+        with torch.cuda.stream(stream):
+            for c in calls:  # warm (lazy state, caches)
+                c()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for c in calls:
+                c()
+        for _ in range(2):
+            g.replay()
+        torch.cuda.synchronize()
+        t = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            t.append(e0.elapsed_time(e1))
+        return statistics.median(t) / len(calls)
+
+    def mv_calls(Ws, rows, K, x, y):
+        descs = [mq.upload_struct(mq.mv_desc(W, rows, K, y, x=x, ncols=x.shape[0]), device) for W in Ws]
+
+        def mk(d):
+            return lambda: mq._check(mq.mq_matvec_q4K_q8_0(d.data_ptr(), rows, K, x.shape[0],
+                                                           torch.cuda.current_stream().cuda_stream), "matvec")
+        return [mk(d) for d in descs], descs
+
+    def ffn_calls(pairs, H, I, x):
+        nc = x.shape[0]
+        y = torch.empty((nc, H), dtype=torch.float32, device=device)
+        h = torch.empty((nc, I // 32 * 34), dtype=torch.uint8, device=device)
+        descs = [mq.upload_struct(mq.ffn_desc(gu, dn, H, I, h, y, x=x, ncols=nc), device) for gu, dn in pairs]
+
+        def mk(d):
+            return lambda: mq._check(mq.mq_ffn_gu_silu_down(d.data_ptr(), H, I, nc,
+                                                            torch.cuda.current_stream().cuda_stream), "ffn")
+        return [mk(d) for d in descs], descs
+
+    peak, _ = measured_hbm_peak()
+
+    def rec(name, ms, wbytes, **extra):
+        gbs = wbytes / (ms / 1e3) / 1e9
+        out[name] = dict(us_per_call=round(ms * 1e3, 3), weight_bytes=wbytes, weight_gbs=round(gbs, 1),
+                         frac_of_measured_hbm=round(gbs / peak, 3), **extra)
+
+    # single matvec 512 x 1024 (seed 0): warm, and rotated copies (HBM)
+    c = synth.MATVEC_512x1024
+    W_np, x_np = synth.matvec_case_inputs(c)
+    W = torch.from_numpy(W_np).to(device)
+    x = torch.from_numpy(x_np).to(device)
+    y = torch.empty((1, c.rows), dtype=torch.float32, device=device)
+    calls, keep = mv_calls([W] * 64, c.rows, c.K, x, y)
+    rec("matvec_512x1024_warm_L2", timed(calls), W.numel(), note="weights L2-resident")
+    ncopy = l2 // W.numel() + 1
+    copies = [W.clone() for _ in range(ncopy)]
+    calls, keep = mv_calls(copies, c.rows, c.K, x, y)
+    rec("matvec_512x1024_hbm", timed(calls, 5), W.numel(), copies=ncopy)
+    del copies, keep
+
+    # 0.5B-class FFN, 24 layers (202 MB: larger than L2 as it is)
+    f = synth.FFN_05B
+    pairs = [tuple(torch.from_numpy(w).to(device) for w in synth.ffn_layer_weights(f, l)) for l in range(f.n_layers)]
+    x = torch.from_numpy(synth.ffn_layer_input(f, 0)).to(device)
+    calls, keep = ffn_calls(pairs, f.H, f.I, x)
+    ms = timed(calls)
+    wb = sum(a.numel() + b.numel() for a, b in pairs)
+    rec("ffn_0.5B_x24_per_layer", ms, wb // f.n_layers, total_us_24_layers=round(ms * 1e3 * f.n_layers, 2))
+    del pairs, keep
+
+    # 7B FFN (115 MB: rotated over 5 copies), batch 1 and 2/4/8 columns
+    f = synth.FFN_7B
+    gu, dn = (torch.from_numpy(w).to(device) for w in synth.ffn_layer_weights(f, 0))
+    pairs = [(gu, dn)] + [(gu.clone(), dn.clone()) for _ in range(4)]
+    wb = gu.numel() + dn.numel()
+    for nc in (1,) + tuple(synth.FFN_7B_NCOLS):
+        x = torch.from_numpy(synth.ffn_layer_input(f, 0, nc)).to(device)
+        calls, keep = ffn_calls(pairs, f.H, f.I, x)
+        rec(f"ffn_7B_ncols{nc}", timed(calls), wb, copies=len(pairs))
+    del pairs, gu, dn, keep
+
+    # K sweep, 4096 rows (rotated copies to exceed twice the L2)
+    for K in synth.KSWEEP_KS:
+        W_np, x_np = synth.ksweep_inputs(K)
+        W = torch.from_numpy(W_np).to(device)
+        x = torch.from_numpy(x_np).to(device)
+        y = torch.empty((1, synth.KSWEEP_ROWS), dtype=torch.float32, device=device)
+        ncopy = l2 // W.numel() + 1
+        copies = [W] + [W.clone() for _ in range(ncopy - 1)]
+        calls, keep = mv_calls(copies, synth.KSWEEP_ROWS, K, x, y)
+        rec(f"ksweep_4096x{K}", timed(calls, 5), W.numel(), copies=ncopy)
+        del copies, keep
+    torch.cuda.synchronize()
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -436,6 +550,7 @@ def run_ours(args):
     launches_per_step = 1 if args.mode == "persistent" else 4 * case.n_layers
 
     cpu = cpu_baseline(case) if (rank == 0 and ws == 1 and not args.no_cpu_baseline) else None
+    suite = config_suite(mq, device) if (rank == 0 and not args.no_configs and args.layers == 28) else None
 
     if rank == 0:
         line = {
@@ -453,6 +568,7 @@ def run_ours(args):
             "frac_of_measured_hbm": value / ws / peak, "frac_of_nominal_8TBs": value / ws / NOMINAL_HBM_GBS,
             "roofline": roofline,
             "cpu_baseline": cpu,
+            "configs": suite,
             "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
@@ -474,6 +590,7 @@ def main(argv=None):
     ap.add_argument("--mode", choices=["persistent", "graph", "pdl"], default="pdl",
                     help="step launch mode: one persistent kernel, or four kernels per layer (plain or PDL)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-config timings (context only)")
     ap.add_argument("--layers", type=int, default=28,
                     help="layers of the 7B stack (28 = the bench workload; fewer only for small profiling runs)")
     args = ap.parse_args(argv)
