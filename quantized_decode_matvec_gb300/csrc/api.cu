@@ -142,7 +142,7 @@ void plan_ring(MvPlan& q0, int64_t units, int kind, int nc, const DeviceInfo& de
     }
     q.S = (q.C + q.nseg - 1) / q.nseg;
     q.nseg = (q.C + q.S - 1) / q.S;
-    const int wmax = (nc == 1) ? 15 : 8;  // consumer warps (the kernel's launch bound minus the producer)
+    const int wmax = (nc <= 2) ? 15 : 8;  // consumer warps (the kernel's launch bound minus the producer)
     if (q.nseg > wmax) return;
     const int nwc = q.nseg * (wmax / q.nseg);
     const int ipw = 32 / q.L;
@@ -196,7 +196,7 @@ bool plan_step(const mq_step_shape& h, const DeviceInfo& dev, StepPlan* out)
 {
     StepPlan sp = {};
     const int nc = h.ncols;
-    const int wmax = (nc == 1) ? 15 : 8;
+    const int wmax = (nc <= 2) ? 15 : 8;
     const int64_t G = dev.num_sms;
     const int kinds[4] = {KIND_MV, KIND_MV, KIND_GU, KIND_DOWN};
     const int64_t Ks[4] = {h.H, h.o_K, h.H, h.I};

@@ -8,7 +8,7 @@
 
 namespace mq {
 
-// consumer warps + the producer warp: 15 + 1 for one column; 8 + 1 for more
+// consumer warps + the producer warp: 15 + 1 for one or two columns; 8 + 1 for more
 // columns, which need more registers per thread (activation and
 // accumulators).  The register file is split between the SM's four
 // schedulers, so the busiest scheduler's warp count sets the per-thread
@@ -16,9 +16,9 @@ namespace mq {
 template <int NC>
 constexpr int ring_max_warps()
 {
-    return NC == 1 ? 16 : 9;
+    return NC <= 2 ? 16 : 9;
 }
-constexpr int ring_max_consumers(int nc) { return nc == 1 ? 15 : 8; }
+constexpr int ring_max_consumers(int nc) { return nc <= 2 ? 15 : 8; }
 
 // Sum of v over the L lanes of each lane group, into every lane of the group.
 template <int L>
