@@ -56,6 +56,10 @@ def _load():
         lib.mqo_silu.restype = ctypes.c_double
         lib.mqo_silu_mul.argtypes = [f64p, f64p, i64, f64p]
         lib.mqo_ffn.argtypes = [u8p, u8p, f32p, i64, i64, i64, u8p, f64p, f64p, f32p, u8p, f64p]
+        lib.mqo_dequant_w_row.argtypes = [ctypes.c_int, u8p, i64, f64p]
+        lib.mqo_matvec_w.argtypes = [ctypes.c_int, u8p, u8p, i64, i64, i64, i64p, i64, f64p, f64p]
+        lib.mqo_dequant_w_row.restype = None
+        lib.mqo_matvec_w.restype = None
         for name in ("mqo_quantize_q8_0", "mqo_unpack_q4K", "mqo_dequant_q4K_row", "mqo_dequant_q8_0",
                      "mqo_block_sums", "mqo_matvec", "mqo_matvec_rows", "mqo_silu_mul", "mqo_ffn"):
             getattr(lib, name).restype = None
@@ -219,3 +223,40 @@ def ffn(W_gu: np.ndarray, W_down: np.ndarray, x: np.ndarray, H: int, I: int) -> 
 def within_tolerance(y: np.ndarray, y_ref: np.ndarray, T: np.ndarray) -> np.ndarray:
     """|y - y_ref| <= 1e-3 * T + 1e-5, elementwise."""
     return np.abs(np.asarray(y, np.float64) - y_ref) <= 1e-3 * T + 1e-5
+
+
+# ---- 32-weight block types: q4_0 (18 bytes) and q8_0 (34 bytes) weights ------------------------------------
+
+W_BLOCK_BYTES = {"q4_0": 18, "q8_0": 34}
+
+
+def w_row_bytes(wtype: str, K: int) -> int:
+    return K // QK8 * W_BLOCK_BYTES[wtype]
+
+
+def dequant_w_row(wtype: str, row: np.ndarray, K: int) -> np.ndarray:
+    """One row of K weights of a 32-weight block type -> binary64."""
+    row = _u8(row).reshape(-1)
+    if row.size != w_row_bytes(wtype, K):
+        raise ValueError("row size does not match K")
+    out = np.empty(K, np.float64)
+    _load().mqo_dequant_w_row(W_BLOCK_BYTES[wtype], _p(row, ctypes.c_uint8), K, _p(out, ctypes.c_double))
+    return out
+
+
+def matvec_w(wtype: str, W: np.ndarray, xq: np.ndarray, rows: int, K: int,
+             row_ids: Optional[np.ndarray] = None) -> Tuple[np.ndarray, np.ndarray]:
+    """y, T [ncols, rows or len(row_ids)] for q4_0 / q8_0 weights and q8_0 activations, fp64."""
+    W = _u8(W).reshape(-1)
+    xq2 = _u8(xq).reshape(-1, q8_0_bytes(K))
+    ncols = xq2.shape[0]
+    if W.size != rows * w_row_bytes(wtype, K):
+        raise ValueError("W size does not match rows x K")
+    ids = None if row_ids is None else np.ascontiguousarray(row_ids, dtype=np.int64)
+    n = rows if ids is None else ids.size
+    y = np.empty((ncols, n), np.float64)
+    T = np.empty((ncols, n), np.float64)
+    _load().mqo_matvec_w(W_BLOCK_BYTES[wtype], _p(W, ctypes.c_uint8), _p(np.ascontiguousarray(xq2), ctypes.c_uint8),
+                         rows, K, ncols, None if ids is None else _p(ids, ctypes.c_int64), n,
+                         _p(y, ctypes.c_double), _p(T, ctypes.c_double))
+    return y, T

@@ -224,6 +224,75 @@ void mqo_block_sums(const uint8_t* W, const uint8_t* xq, int64_t rows, int64_t K
 }
 
 /* ---------------------------------------------------------------------------
+ * Other weight types of the pages' models (GGUF-compatible readings), for the
+ * same MMVQ dot product against q8_0 activations:
+ *   q4_0, 32 weights in 18 bytes: [0:2] f16 d, [2:18] sixteen bytes; byte i
+ *         holds weight i in its low nibble and weight i+16 in its high
+ *         nibble; w = d * (q - 8) with q in 0..15.
+ *   q8_0, 32 weights in 34 bytes, the activation's own block format:
+ *         w = d * q with q an int8.
+ * The type is named by its block size in bytes (18 or 34).
+ * ------------------------------------------------------------------------- */
+#define MQO_Q4_0_BYTES 18
+
+/* one weight block -> (f64 scale, 32 signed integer weights w/d) */
+static void mqo_unpack_wblock(int block_bytes, const uint8_t* blk, double* d, int q[32])
+{
+    *d = (double)mqo_f16_to_f32(mqo_le16(blk));
+    if (block_bytes == MQO_Q4_0_BYTES) {
+        for (int i = 0; i < 16; ++i) {
+            q[i] = (blk[2 + i] & 15) - 8;
+            q[i + 16] = (blk[2 + i] >> 4) - 8;
+        }
+    } else {
+        for (int i = 0; i < MQO_QK8; ++i) q[i] = (int)(int8_t)blk[2 + i];
+    }
+}
+
+/* dequantize one row of K weights of a 32-weight block type to binary64 */
+void mqo_dequant_w_row(int block_bytes, const uint8_t* row, int64_t K, double* w)
+{
+    double d;
+    int q[32];
+    for (int64_t b = 0; b < K / MQO_QK8; ++b) {
+        mqo_unpack_wblock(block_bytes, row + b * block_bytes, &d, q);
+        for (int i = 0; i < MQO_QK8; ++i) w[b * MQO_QK8 + i] = d * q[i];
+    }
+}
+
+/* y = sum_b dq8_b * (d_b * sumi_b) with sumi_b = sum_i q_bi * q8_bi (int), and
+ * T = sum_b |that product|, for one row of a 32-weight block type */
+static void mqo_row_dot_w(int block_bytes, const uint8_t* row, const uint8_t* xq, int64_t K, double* y, double* T)
+{
+    double acc = 0.0, tsum = 0.0, d, dq;
+    int q[32], q8[32];
+    for (int64_t b = 0; b < K / MQO_QK8; ++b) {
+        mqo_unpack_wblock(block_bytes, row + b * block_bytes, &d, q);
+        mqo_unpack_q8_0(xq + b * MQO_Q8_BYTES, &dq, q8);
+        int64_t sumi = 0;
+        for (int i = 0; i < MQO_QK8; ++i) sumi += (int64_t)q[i] * q8[i];
+        const double t = dq * (d * (double)sumi);
+        acc += t;
+        tsum += fabs(t);
+    }
+    *y = acc;
+    if (T) *T = tsum;
+}
+
+/* y[c][t], T[c][t] for the listed rows (all rows when row_ids is NULL) */
+void mqo_matvec_w(int block_bytes, const uint8_t* W, const uint8_t* xq, int64_t rows, int64_t K, int64_t ncols,
+                  const int64_t* row_ids, int64_t n_ids, double* y, double* T)
+{
+    const int64_t rb = K / MQO_QK8 * block_bytes, cb = K / MQO_QK8 * MQO_Q8_BYTES;
+    const int64_t n = row_ids ? n_ids : rows;
+    for (int64_t c = 0; c < ncols; ++c)
+        for (int64_t t = 0; t < n; ++t) {
+            const int64_t r = row_ids ? row_ids[t] : t;
+            mqo_row_dot_w(block_bytes, W + r * rb, xq + c * cb, K, &y[c * n + t], T ? &T[c * n + t] : 0);
+        }
+}
+
+/* ---------------------------------------------------------------------------
  * One output row of the matvec, via the per-block integer sums:
  *   y = sum_b sum_j dq8_J * (d_b * sc_bj * sumi_J - dmin_b * m_bj * sumq_J)
  * plus T = sum of |each of the two products| (the tolerance scale).

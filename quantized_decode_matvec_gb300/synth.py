@@ -71,6 +71,28 @@ def q4K_matrix(rows: int, K: int, seed: int, tag: int = TAG_W, layer: int = 0,
     return img.reshape(rows, nb * Q4K_BLOCK_BYTES)
 
 
+# 32-weight block types of the pages' other models: block bytes, default scale sigma
+WBLOCK = {"q4_0": (18, 2e-3), "q8_0": (34, 2e-4)}
+TAG_WQ = 13  # q4_0 / q8_0 weight matrices
+
+
+def wq_matrix(wtype: str, rows: int, K: int, seed: int, tag: int = TAG_WQ, layer: int = 0,
+              d_sigma: float | None = None) -> np.ndarray:
+    """Random q4_0 or q8_0 weight matrix as uint8 [rows, K/32*block_bytes]: uniform bytes, then
+    bytes 0-1 of every block overwritten with binary16 |N(0, d_sigma)| (the block scale)."""
+    if K % QK8_0:
+        raise ValueError("K must be a multiple of 32")
+    bb, sigma = WBLOCK[wtype]
+    nb = K // QK8_0
+    rng = stream(seed, tag, layer, bb)
+    nbytes = rows * nb * bb
+    raw = rng.bit_generator.random_raw((nbytes + 7) // 8).astype("<u8", copy=False)
+    img = raw.view(np.uint8)[:nbytes].reshape(rows * nb, bb)
+    d = np.abs(rng.standard_normal(rows * nb)) * (sigma if d_sigma is None else d_sigma)
+    img[:, 0:2] = d.astype(np.float16).view(np.uint8).reshape(-1, 2)
+    return img.reshape(rows, nb * bb)
+
+
 def activation(K: int, ncols: int, seed: int, tag: int = TAG_X, layer: int = 0,
                outlier_p: float = 1e-3, outlier_scale: float = 20.0) -> np.ndarray:
     """fp32 [ncols, K] N(0,1) activation with sparse x20 outliers."""
