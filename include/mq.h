@@ -72,6 +72,7 @@ typedef int mq_status;
 /* quantization types (mq_concat_rows*) */
 #define MQ_TYPE_Q4_K 1
 #define MQ_TYPE_Q8_0 2
+#define MQ_TYPE_Q4_0 3  /* 32 weights in 18 bytes: f16 d, 16 bytes of nibbles (see mq_matvec_q4_0_q8_0) */
 
 /* limits: K * ncols <= MQ_MAX_K_TIMES_NCOLS (the q8_0 activation is staged in
  * shared memory), K <= MQ_MAX_K, ncols <= MQ_MAX_NCOLS */
@@ -153,6 +154,21 @@ mq_status mq_check_mv_desc(const mq_mv_desc* h_desc);
  * launches nothing; K must be a positive multiple of 256. */
 mq_status mq_matvec_q4K_q8_0(const mq_mv_desc* d_desc, int32_t rows, int32_t K, int32_t ncols,
                              void* stream);
+
+/* ---- the matvec for the other weight types -------------------------------------
+ * The pages' 0.5B model is quantized q4_0 ("07 . R3 -- Small-model per-token
+ * overhead", sections 4 and 5); the same MMVQ dot product against q8_0
+ * activations serves q4_0 and q8_0 weights (GGUF-compatible layouts):
+ *   q4_0: 32 weights in 18 bytes: [0:2] f16 d, [2:18] byte i holds weight i
+ *         in its low nibble and weight i+16 in its high nibble; w = d*(q-8).
+ *   q8_0: 32 weights in 34 bytes, the activation's block format; w = d*q.
+ * Same descriptor, shapes, limits and rules as mq_matvec_q4K_q8_0, with W of
+ * rows x K/32 blocks of that type (row bytes K/32*18 or K/32*34); K % 256 ==
+ * 0 so rows stay 16-byte multiples.  These run only on the bulk-copy ring
+ * kernels: a shape whose ring plan does not fit the device returns
+ * MQ_ERR_UNSUPPORTED. */
+mq_status mq_matvec_q4_0_q8_0(const mq_mv_desc* d_desc, int32_t rows, int32_t K, int32_t ncols, void* stream);
+mq_status mq_matvec_q8_0_q8_0(const mq_mv_desc* d_desc, int32_t rows, int32_t K, int32_t ncols, void* stream);
 
 /* ---- fused FFN -----------------------------------------------------------------
  *   W_gu   q4_K [2I][H]: gate rows 0..I-1, then up rows I..2I-1 (ffn_gu)

@@ -14,7 +14,8 @@ cudaError_t set_mv_attributes(int max_smem);
 cudaError_t set_gu_attributes(int max_smem);
 cudaError_t set_ring_attributes(int max_smem);
 cudaError_t set_step_attributes(int max_smem);
-void plan_ring(MvPlan& q, int64_t units, int kind, int nc, const DeviceInfo& dev);
+cudaError_t set_wring_attributes(int max_smem);
+void plan_ring(MvPlan& q, int64_t units, int kind, int nc, const DeviceInfo& dev, int64_t unit_bytes);
 }  // namespace mq
 
 namespace {
@@ -73,7 +74,8 @@ mq_status record_cuda_error(cudaError_t e) { return cuda_fail(e); }
 int variant_policy() { return g_variant_policy; }
 int fault_policy() { return g_fault_policy; }
 
-bool plan_mv(int64_t rows, int K, int nc, int kind, int I, const DeviceInfo& dev, MvPlan* p)
+bool plan_mv(int64_t rows, int K, int nc, int kind, int I, const DeviceInfo& dev, MvPlan* p, int unit_bytes,
+             bool ring_only)
 {
     MvPlan q = {};
     q.C = K / 64;
@@ -112,7 +114,7 @@ bool plan_mv(int64_t rows, int K, int nc, int kind, int I, const DeviceInfo& dev
     q.block = int(32 * nw);
     q.smem = int(smem);
     q.variant = 0;
-    if (variant_policy() != VARIANT_FORCE_REGISTER) plan_ring(q, units, kind, nc, dev);
+    if (ring_only || variant_policy() != VARIANT_FORCE_REGISTER) plan_ring(q, units, kind, nc, dev, unit_bytes);
     *p = q;
     return true;
 }
@@ -125,7 +127,7 @@ bool plan_mv(int64_t rows, int K, int nc, int kind, int I, const DeviceInfo& dev
 //  * tiles of T = 2*rg*m rows (about 24 KB), at most the CTA's rows rounded up;
 //  * 2..8 stages, within ~110 KB of shared memory when possible so that the
 //    next kernel's CTA fits beside this one under programmatic dependent launch.
-void plan_ring(MvPlan& q0, int64_t units, int kind, int nc, const DeviceInfo& dev)
+void plan_ring(MvPlan& q0, int64_t units, int kind, int nc, const DeviceInfo& dev, int64_t unit_bytes)
 {
     // work unit: half a super-block (128 weights); C counts units per row here
     MvPlan q = q0;
@@ -147,17 +149,18 @@ void plan_ring(MvPlan& q0, int64_t units, int kind, int nc, const DeviceInfo& de
     const int nwc = q.nseg * (wmax / q.nseg);
     const int ipw = 32 / q.L;
     const int rg = (nwc / q.nseg) * ipw;
-    const int64_t row_bytes = int64_t(q.C / 2) * 144;
+    const int64_t row_bytes = int64_t(q.C) * unit_bytes;  // q.C units of 128 weights
     // tiles of whole row pairs per row-lane (consumers take two rows per step)
     const int64_t unit = 2 * rg * row_bytes;
     int64_t m = (24576 + unit / 2) / unit;
     if (m < 1) m = 1;
     int64_t T = 2 * rg * m;
-    const int64_t rpc_round = (q.rows_per_cta + 2 * rg - 1) / (2 * rg) * (2 * rg);
-    if (T > rpc_round) T = rpc_round;
-    // a CTA's few rows beyond one tile (q|k|v: 31 rows, tiles of 30) ride in
-    // that tile rather than in a tile of their own
-    if (q.rows_per_cta > T && q.rows_per_cta * row_bytes <= 65536) T = q.rows_per_cta;
+    // tiles of at most ~64 KB (wide rows, e.g. q8_0 weights: fewer rows than a
+    // full step of the row-lanes; the consumers handle any tile height)
+    if (T * row_bytes > 65536) T = 65536 / row_bytes > 1 ? 65536 / row_bytes : 1;
+    // no tile beyond the CTA's rows; a CTA's few rows beyond one tile (q|k|v:
+    // 31 rows, tiles of 30) ride in that tile rather than in a tile of their own
+    if (T > q.rows_per_cta || (q.rows_per_cta * row_bytes <= 65536)) T = q.rows_per_cta;
     const int64_t stage = (T * row_bytes + 127) / 128 * 128;
     const int64_t act = int64_t(nc) * q.C * 160;
     const int64_t part = int64_t(q.rows_per_cta) * q.nseg * nc * 4;
@@ -281,6 +284,7 @@ cudaError_t set_kernel_attributes(int max_smem)
     if (e == cudaSuccess) e = set_gu_attributes(max_smem);
     if (e == cudaSuccess) e = set_ring_attributes(max_smem);
     if (e == cudaSuccess) e = set_step_attributes(max_smem);
+    if (e == cudaSuccess) e = set_wring_attributes(max_smem);
     return e;
 }
 
@@ -372,12 +376,12 @@ size_t mq_q8_0_bytes(int64_t K) { return (K < 0 || K % 32) ? 0 : size_t(K / 32) 
 
 int mq_quant_block_elems(int32_t ttype)
 {
-    return ttype == MQ_TYPE_Q4_K ? 256 : ttype == MQ_TYPE_Q8_0 ? 32 : 0;
+    return ttype == MQ_TYPE_Q4_K ? 256 : (ttype == MQ_TYPE_Q8_0 || ttype == MQ_TYPE_Q4_0) ? 32 : 0;
 }
 
 int mq_quant_block_bytes(int32_t ttype)
 {
-    return ttype == MQ_TYPE_Q4_K ? 144 : ttype == MQ_TYPE_Q8_0 ? 34 : 0;
+    return ttype == MQ_TYPE_Q4_K ? 144 : ttype == MQ_TYPE_Q8_0 ? 34 : ttype == MQ_TYPE_Q4_0 ? 18 : 0;
 }
 
 // Mirrors mq_concat_rows' preconditions clause by clause ("04 . 8o",
@@ -472,6 +476,36 @@ mq_status mq_matvec_q4K_q8_0(const mq_mv_desc* d_desc, int32_t rows, int32_t K, 
     const mq::DeviceInfo* dev = nullptr;
     if ((st = current_dev(&dev)) != MQ_OK) return st;
     return launch_matvec(d_desc, mq::KIND_MV, rows, K, ncols, dev, as_stream(stream), false);
+}
+
+// q4_0 / q8_0 weights: the same checks and descriptor, the ring kernel with
+// that type's unit format (there is no register-streaming fallback for them)
+static mq_status matvec_wtype(int wtype, const mq_mv_desc* d_desc, int32_t rows, int32_t K, int32_t ncols,
+                              void* stream)
+{
+    mq_status st = check_mv_shape(rows, K, ncols);
+    if (st != MQ_OK) return st;
+    if (rows == 0 || ncols == 0) return MQ_OK;
+    if (!d_desc) return MQ_ERR_INVALID_ARG;
+    if (!aligned(d_desc, 8)) return MQ_ERR_ALIGN;
+    const mq::DeviceInfo* dev = nullptr;
+    if ((st = current_dev(&dev)) != MQ_OK) return st;
+    mq::MvPlan p;
+    const int unit_bytes = wtype == MQ_TYPE_Q4_0 ? 72 : 136;  // four 32-weight blocks
+    if (!mq::plan_mv(rows, K, ncols, mq::KIND_MV, 0, *dev, &p, unit_bytes, true) || p.variant != 1)
+        return MQ_ERR_UNSUPPORTED;
+    cudaError_t e = mq::launch_wring(d_desc, wtype, rows, K, ncols, p, dev->status, as_stream(stream), false);
+    return e == cudaSuccess ? MQ_OK : cuda_fail(e);
+}
+
+mq_status mq_matvec_q4_0_q8_0(const mq_mv_desc* d_desc, int32_t rows, int32_t K, int32_t ncols, void* stream)
+{
+    return matvec_wtype(MQ_TYPE_Q4_0, d_desc, rows, K, ncols, stream);
+}
+
+mq_status mq_matvec_q8_0_q8_0(const mq_mv_desc* d_desc, int32_t rows, int32_t K, int32_t ncols, void* stream)
+{
+    return matvec_wtype(MQ_TYPE_Q8_0, d_desc, rows, K, ncols, stream);
 }
 
 static mq_status check_ffn_shape(int64_t H, int64_t I, int64_t ncols)

@@ -71,7 +71,10 @@ const DeviceInfo* current_device_info();
 mq_status record_cuda_error(cudaError_t e);
 
 // returns false if the shapes cannot be planned within the device limits
-bool plan_mv(int64_t rows, int K, int ncols, int kind, int I, const DeviceInfo& dev, MvPlan* p);
+// unit_bytes: row bytes per 128 weights (72 for q4_K and q4_0, 136 for q8_0 weights)
+// ring_only: plan the bulk-copy ring kernels whatever the variant policy
+bool plan_mv(int64_t rows, int K, int ncols, int kind, int I, const DeviceInfo& dev, MvPlan* p, int unit_bytes = 72,
+             bool ring_only = false);
 
 cudaError_t launch_quantize(const float* x, void* xq, int64_t nblocks, cudaStream_t s);
 // launch_mv / launch_gu dispatch on p.variant
@@ -81,6 +84,9 @@ cudaError_t launch_gu(const mq_ffn_desc* d, int H, int I, int ncols, const MvPla
                       cudaStream_t s, bool pdl);
 cudaError_t launch_ring(const void* desc, int kind, int a, int b, int ncols, const MvPlan& p, unsigned* status,
                         cudaStream_t s, bool pdl);
+// the matvec for q4_0 / q8_0 weights (wtype MQ_TYPE_Q4_0 or MQ_TYPE_Q8_0), ring plans only
+cudaError_t launch_wring(const void* desc, int wtype, int rows, int K, int ncols, const MvPlan& p, unsigned* status,
+                         cudaStream_t s, bool pdl);
 bool plan_step(const mq_step_shape& h, const DeviceInfo& dev, StepPlan* sp);
 cudaError_t launch_step(const mq_layer_desc* layers, const StepPlan& sp, int ncols, unsigned* status, unsigned* ws,
                         cudaStream_t s);

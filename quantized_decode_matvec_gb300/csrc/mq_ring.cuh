@@ -65,7 +65,7 @@ __device__ __forceinline__ ConsumeArgs consume_args(const MvPlan& p, int nrows, 
 
 // (not inlined: called once per matrix, it keeps its own register allocation
 // instead of adding to the caller's)
-template <int NC, int L>
+template <int NC, int L, class Fmt = FmtQ4K>
 __device__ __noinline__ bool ring_consume_L(const ConsumeArgs p, const uint8_t* ring, uint64_t* full,
                                             uint64_t* empty, const UnitAct act, float* __restrict__ part,
                                             uint64_t limit_ns)
@@ -83,10 +83,8 @@ __device__ __noinline__ bool ring_consume_L(const ConsumeArgs p, const uint8_t* 
     // every tile's full/empty handshake, so the stage counts stay exact
     const bool warp_active = warp < nwc_used;
     const bool on = warp_active && (l < p.S) && (u < p.C);
-    const bool upper = (u & 1) != 0;
-    const uint32_t row_bytes = uint32_t(p.C / 2) * kQ4KBytes;
-    const uint32_t off_h = uint32_t(u >> 1) * kQ4KBytes;
-    const uint32_t off_q = off_h + 16 + 64 * (u & 1);
+    const uint32_t row_bytes = Fmt::row_bytes(p.C);
+    const typename Fmt::Off off = Fmt::offsets(u);
 
     constexpr bool kRegAct = NC <= 2;
     uint4 A[NC][8];
@@ -101,13 +99,8 @@ __device__ __noinline__ bool ring_consume_L(const ConsumeArgs p, const uint8_t* 
 #pragma unroll
         for (int c = 0; c < NC; ++c) load_act(c, c);
     }
-    auto load_w = [&](const uint8_t* stage, int rr, UnitW& w) {
-        const uint8_t* rb = stage + uint32_t(rr) * row_bytes;
-        w.h = lds16(rb + off_h);
-        w.qa0 = lds16(rb + off_q);
-        w.qb0 = lds16(rb + off_q + 16);
-        w.qa1 = lds16(rb + off_q + 32);
-        w.qb1 = lds16(rb + off_q + 48);
+    auto load_w = [&](const uint8_t* stage, int rr, typename Fmt::W& w) {
+        Fmt::load(stage + uint32_t(rr) * row_bytes, off, w);
     };
 
     const int ntiles = (nrows + p.T - 1) / p.T;
@@ -125,16 +118,16 @@ __device__ __noinline__ bool ring_consume_L(const ConsumeArgs p, const uint8_t* 
 #pragma unroll
             for (int c = 0; c < NC; ++c) acc_a[c] = acc_b[c] = 0.0f;
             if (va || vb) {
-                UnitW wa, wb;
+                typename Fmt::W wa, wb;
                 load_w(stage, va ? ra : rb, wa);
                 load_w(stage, vb ? rb : ra, wb);
-                const UnitScales ka = unit_scales(wa.h, upper), kb = unit_scales(wb.h, upper);
+                const typename Fmt::S ka = Fmt::prep(wa, off), kb = Fmt::prep(wb, off);
 #pragma unroll
                 for (int c = 0; c < NC; ++c) {
                     if (!kRegAct) load_act(c, 0);
                     const int cc = kRegAct ? c : 0;
-                    if (va) acc_a[c] = unit_column(wa, ka, A[cc], DQ[cc], DQSQ[cc], 0.0f);
-                    if (vb) acc_b[c] = unit_column(wb, kb, A[cc], DQ[cc], DQSQ[cc], 0.0f);
+                    if (va) acc_a[c] = Fmt::column(wa, ka, A[cc], DQ[cc], DQSQ[cc]);
+                    if (vb) acc_b[c] = Fmt::column(wb, kb, A[cc], DQ[cc], DQSQ[cc]);
                 }
             }
 #pragma unroll
@@ -150,15 +143,15 @@ __device__ __noinline__ bool ring_consume_L(const ConsumeArgs p, const uint8_t* 
     return true;
 }
 
-template <int NC>
+template <int NC, class Fmt = FmtQ4K>
 __device__ __forceinline__ bool ring_consume(const MvPlan& p, int nrows, int tile_base, int nwc_used,
                                              const uint8_t* ring, uint64_t* full, uint64_t* empty,
                                              const UnitAct& act, float* __restrict__ part, uint64_t limit_ns)
 {
     const ConsumeArgs a = consume_args(p, nrows, tile_base, nwc_used);
-    if (p.L == 32) return ring_consume_L<NC, 32>(a, ring, full, empty, act, part, limit_ns);
-    if (p.L == 16) return ring_consume_L<NC, 16>(a, ring, full, empty, act, part, limit_ns);
-    return ring_consume_L<NC, 8>(a, ring, full, empty, act, part, limit_ns);
+    if (p.L == 32) return ring_consume_L<NC, 32, Fmt>(a, ring, full, empty, act, part, limit_ns);
+    if (p.L == 16) return ring_consume_L<NC, 16, Fmt>(a, ring, full, empty, act, part, limit_ns);
+    return ring_consume_L<NC, 8, Fmt>(a, ring, full, empty, act, part, limit_ns);
 }
 
 }  // namespace mq

@@ -340,4 +340,175 @@ __device__ __forceinline__ float unit_column(const UnitW& w, const UnitScales& k
     return fmaf(-k.dmin, u, acc);
 }
 
+// ---------------------------------------------------------------------------
+// Weight formats of the ring consumer.  A format gives, for the 128-weight
+// unit u of a row: the row's bytes per unit, where the unit's bytes sit, how a
+// lane loads them from a ring stage, what it derives once per unit (scales),
+// and the unit's contribution for one activation column (unit layout above).
+// ---------------------------------------------------------------------------
+
+// q4_K: half a super-block, 72 bytes of row per unit
+struct FmtQ4K {
+    using W = UnitW;
+    using S = UnitScales;
+    struct Off {
+        uint32_t h, q;
+        bool upper;
+    };
+    __device__ __forceinline__ static uint32_t row_bytes(int U) { return uint32_t(U / 2) * kQ4KBytes; }
+    __device__ __forceinline__ static Off offsets(int u)
+    {
+        const uint32_t h = uint32_t(u >> 1) * kQ4KBytes;
+        return Off{h, h + 16 + 64 * uint32_t(u & 1), (u & 1) != 0};
+    }
+    __device__ __forceinline__ static void load(const uint8_t* row, const Off& o, W& w)
+    {
+        w.h = *reinterpret_cast<const uint4*>(row + o.h);
+        w.qa0 = *reinterpret_cast<const uint4*>(row + o.q);
+        w.qb0 = *reinterpret_cast<const uint4*>(row + o.q + 16);
+        w.qa1 = *reinterpret_cast<const uint4*>(row + o.q + 32);
+        w.qb1 = *reinterpret_cast<const uint4*>(row + o.q + 48);
+    }
+    __device__ __forceinline__ static S prep(const W& w, const Off& o) { return unit_scales(w.h, o.upper); }
+    __device__ __forceinline__ static float column(const W& w, const S& k, const uint4 (&A)[8], const float4& dq,
+                                                   const float4& dqsq)
+    {
+        return unit_column(w, k, A, dq, dqsq, 0.0f);
+    }
+};
+
+__device__ __forceinline__ float f16_bits_to_float(uint32_t bits)
+{
+    return __half2float(__ushort_as_half(uint16_t(bits)));
+}
+
+// q4_0 weights ("32 weights in 18 bytes: f16 d, then 16 bytes; byte i holds
+// weight i in its low nibble and weight i+16 in its high nibble; w = d(q-8)"):
+// a unit is 4 blocks, 72 bytes at byte 72u of the row (8-byte aligned: rows
+// are 16-byte aligned when K % 256 == 0).  Block j's scale and quants sit at
+// bytes 18j and 18j+2: words 0, 4(hi), 9, 13(hi) and quants from word
+// offsets 0.5, 5, 9.5, 14 (a half-word offset is undone by a funnel shift).
+// Low nibbles meet codes 0..15 of the block (plane 2j), high nibbles codes
+// 16..31 (plane 2j+1); the -8 comes off through the block's code sum:
+// d*(dq*sum(q*a) - 8*dq*sum(a)).
+struct FmtQ4_0 {
+    struct W {
+        uint32_t w[18];
+    };
+    struct S {
+        float d[4];
+    };
+    struct Off {
+        uint32_t o;
+    };
+    __device__ __forceinline__ static uint32_t row_bytes(int U) { return uint32_t(U) * 72; }
+    __device__ __forceinline__ static Off offsets(int u) { return Off{uint32_t(u) * 72}; }
+    __device__ __forceinline__ static void load(const uint8_t* row, const Off& o, W& w)
+    {
+        const uint2* p = reinterpret_cast<const uint2*>(row + o.o);
+#pragma unroll
+        for (int k = 0; k < 9; ++k) {
+            const uint2 v = p[k];
+            w.w[2 * k] = v.x;
+            w.w[2 * k + 1] = v.y;
+        }
+    }
+    __device__ __forceinline__ static S prep(const W& w, const Off&)
+    {
+        return S{{f16_bits_to_float(w.w[0]), f16_bits_to_float(w.w[4] >> 16), f16_bits_to_float(w.w[9]),
+                  f16_bits_to_float(w.w[13] >> 16)}};
+    }
+    // sum over the block's 32 weights of q * code, q in 0..15
+    __device__ __forceinline__ static int block_dot(uint32_t q0, uint32_t q1, uint32_t q2, uint32_t q3, const uint4& lo,
+                                                    const uint4& hi)
+    {
+        const uint32_t m = 0x0f0f0f0fu;
+        int s = dp4a_us(q0 & m, lo.x, 0);
+        s = dp4a_us(q1 & m, lo.y, s);
+        s = dp4a_us(q2 & m, lo.z, s);
+        s = dp4a_us(q3 & m, lo.w, s);
+        s = dp4a_us((q0 >> 4) & m, hi.x, s);
+        s = dp4a_us((q1 >> 4) & m, hi.y, s);
+        s = dp4a_us((q2 >> 4) & m, hi.z, s);
+        return dp4a_us((q3 >> 4) & m, hi.w, s);
+    }
+    __device__ __forceinline__ static float column(const W& w, const S& k, const uint4 (&A)[8], const float4& dq,
+                                                   const float4& dqsq)
+    {
+        const uint32_t* v = w.w;
+        const int s0 = block_dot(__funnelshift_r(v[0], v[1], 16), __funnelshift_r(v[1], v[2], 16),
+                                 __funnelshift_r(v[2], v[3], 16), __funnelshift_r(v[3], v[4], 16), A[0], A[1]);
+        const int s1 = block_dot(v[5], v[6], v[7], v[8], A[2], A[3]);
+        const int s2 = block_dot(__funnelshift_r(v[9], v[10], 16), __funnelshift_r(v[10], v[11], 16),
+                                 __funnelshift_r(v[11], v[12], 16), __funnelshift_r(v[12], v[13], 16), A[4], A[5]);
+        const int s3 = block_dot(v[14], v[15], v[16], v[17], A[6], A[7]);
+        float t = k.d[0] * fmaf(dq.x, float(s0), -8.0f * dqsq.x);
+        t = fmaf(k.d[1], fmaf(dq.y, float(s1), -8.0f * dqsq.y), t);
+        t = fmaf(k.d[2], fmaf(dq.z, float(s2), -8.0f * dqsq.z), t);
+        return fmaf(k.d[3], fmaf(dq.w, float(s3), -8.0f * dqsq.w), t);
+    }
+};
+
+// q8_0 weights (the activation's own block format, w = d*q): a unit is 4
+// blocks, 136 bytes at byte 136u of the row (8-byte aligned).  Block j's scale
+// and quants sit at bytes 34j and 34j+2: scale words 0, 8(hi), 17, 25(hi) and
+// quants from word offsets 0.5, 9, 17.5, 26.
+struct FmtQ8_0 {
+    struct W {
+        uint32_t w[34];
+    };
+    struct S {
+        float d[4];
+    };
+    struct Off {
+        uint32_t o;
+    };
+    __device__ __forceinline__ static uint32_t row_bytes(int U) { return uint32_t(U) * 136; }
+    __device__ __forceinline__ static Off offsets(int u) { return Off{uint32_t(u) * 136}; }
+    __device__ __forceinline__ static void load(const uint8_t* row, const Off& o, W& w)
+    {
+        const uint2* p = reinterpret_cast<const uint2*>(row + o.o);
+#pragma unroll
+        for (int k = 0; k < 17; ++k) {
+            const uint2 v = p[k];
+            w.w[2 * k] = v.x;
+            w.w[2 * k + 1] = v.y;
+        }
+    }
+    __device__ __forceinline__ static S prep(const W& w, const Off&)
+    {
+        return S{{f16_bits_to_float(w.w[0]), f16_bits_to_float(w.w[8] >> 16), f16_bits_to_float(w.w[17]),
+                  f16_bits_to_float(w.w[25] >> 16)}};
+    }
+    // sum over the block's 32 weights of q * code, q signed; words at v[0..8]
+    // with half-word offset `shift` (0 or 16)
+    template <int kShift>
+    __device__ __forceinline__ static int block_dot(const uint32_t* v, const uint4& lo, const uint4& hi)
+    {
+        auto word = [&](int i) -> int {
+            return kShift ? int(__funnelshift_r(v[i], v[i + 1], kShift)) : int(v[i]);
+        };
+        int s = __dp4a(word(0), int(lo.x), 0);
+        s = __dp4a(word(1), int(lo.y), s);
+        s = __dp4a(word(2), int(lo.z), s);
+        s = __dp4a(word(3), int(lo.w), s);
+        s = __dp4a(word(4), int(hi.x), s);
+        s = __dp4a(word(5), int(hi.y), s);
+        s = __dp4a(word(6), int(hi.z), s);
+        return __dp4a(word(7), int(hi.w), s);
+    }
+    __device__ __forceinline__ static float column(const W& w, const S& k, const uint4 (&A)[8], const float4& dq,
+                                                   const float4&)
+    {
+        const int s0 = block_dot<16>(w.w + 0, A[0], A[1]);
+        const int s1 = block_dot<0>(w.w + 9, A[2], A[3]);
+        const int s2 = block_dot<16>(w.w + 17, A[4], A[5]);
+        const int s3 = block_dot<0>(w.w + 26, A[6], A[7]);
+        float t = k.d[0] * (dq.x * float(s0));
+        t = fmaf(k.d[1], dq.y * float(s1), t);
+        t = fmaf(k.d[2], dq.z * float(s2), t);
+        return fmaf(k.d[3], dq.w * float(s3), t);
+    }
+};
+
 }  // namespace mq

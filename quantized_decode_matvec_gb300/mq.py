@@ -46,6 +46,7 @@ MQ_FAULT_NONE = 0
 MQ_FAULT_WITHHOLD_TILE = 1
 MQ_TYPE_Q4_K = 1
 MQ_TYPE_Q8_0 = 2
+MQ_TYPE_Q4_0 = 3
 MQ_MAX_NCOLS = 8
 MQ_MAX_K = 131072
 MQ_MAX_K_TIMES_NCOLS = 163840
@@ -97,6 +98,8 @@ _sig("mq_concat_rows", c_i32, c_vp, ctypes.POINTER(c_vp), ctypes.POINTER(c_i64),
 _sig("mq_quantize_q8_0", c_i32, c_vp, c_vp, c_i64, c_i32, c_vp)
 _sig("mq_check_mv_desc", c_i32, ctypes.POINTER(MvDesc))
 _sig("mq_matvec_q4K_q8_0", c_i32, c_vp, c_i32, c_i32, c_i32, c_vp)
+_sig("mq_matvec_q4_0_q8_0", c_i32, c_vp, c_i32, c_i32, c_i32, c_vp)
+_sig("mq_matvec_q8_0_q8_0", c_i32, c_vp, c_i32, c_i32, c_i32, c_vp)
 _sig("mq_check_ffn_desc", c_i32, ctypes.POINTER(FfnDesc))
 _sig("mq_ffn_gu_silu_down", c_i32, c_vp, c_i32, c_i32, c_i32, c_vp)
 _sig("mq_ffn_gate_up", c_i32, c_vp, c_i32, c_i32, c_i32, c_vp)
@@ -110,7 +113,7 @@ _sig("mq_debug_set_fault", c_i32, c_i32)
 EXPORTS = ["mq_status_string", "mq_abi_version", "mq_last_cuda_error", "mq_init", "mq_read_device_status",
            "mq_q4K_row_bytes", "mq_q8_0_bytes", "mq_quant_block_elems", "mq_quant_block_bytes",
            "mq_concat_rows_feasible", "mq_concat_rows", "mq_quantize_q8_0", "mq_check_mv_desc",
-           "mq_matvec_q4K_q8_0", "mq_check_ffn_desc", "mq_ffn_gu_silu_down", "mq_ffn_gate_up", "mq_step",
+           "mq_matvec_q4K_q8_0", "mq_matvec_q4_0_q8_0", "mq_matvec_q8_0_q8_0", "mq_check_ffn_desc", "mq_ffn_gu_silu_down", "mq_ffn_gate_up", "mq_step",
            "mq_ffn_gu_silu_down_noalloc",
            "mq_debug_block_sums_q4K_q8_0", "mq_debug_set_variant", "mq_debug_set_fault"]
 
@@ -194,6 +197,14 @@ def mq_check_mv_desc(d: MvDesc) -> int:
 
 def mq_matvec_q4K_q8_0(d_desc: int, rows: int, K: int, ncols: int, stream: int = 0) -> int:
     return _lib.mq_matvec_q4K_q8_0(c_vp(d_desc), rows, K, ncols, c_vp(stream))
+
+
+def mq_matvec_q4_0_q8_0(d_desc: int, rows: int, K: int, ncols: int, stream: int = 0) -> int:
+    return _lib.mq_matvec_q4_0_q8_0(c_vp(d_desc), rows, K, ncols, c_vp(stream))
+
+
+def mq_matvec_q8_0_q8_0(d_desc: int, rows: int, K: int, ncols: int, stream: int = 0) -> int:
+    return _lib.mq_matvec_q8_0_q8_0(c_vp(d_desc), rows, K, ncols, c_vp(stream))
 
 
 def mq_check_ffn_desc(d: FfnDesc) -> int:
@@ -308,6 +319,23 @@ def matvec_q4K_q8_0(W, rows: int, K: int, x=None, xq=None, y=None, xq_out=None, 
     _check(mq_check_mv_desc(d), "mq_check_mv_desc")
     dd = upload_struct(d, W.device)
     _check(mq_matvec_q4K_q8_0(_ptr(dd), rows, K, ncols, _stream(stream)), "mq_matvec_q4K_q8_0")
+    return y, dd
+
+
+def matvec_w(wtype: str, W, rows: int, K: int, x=None, xq=None, y=None, ncols: Optional[int] = None, stream=None):
+    """y [ncols, rows] fp32 = W . q8_0(x) (or W . xq) for q4_0 (``wtype="q4_0"``) or q8_0
+    (``"q8_0"``) weights.  Returns (y, desc_buffer)."""
+    torch = _torch()
+    act = x if x is not None else xq
+    if ncols is None:
+        ncols = act.shape[0] if act.dim() == 2 else 1
+    if y is None:
+        y = torch.empty((ncols, rows), dtype=torch.float32, device=W.device)
+    d = mv_desc(W, rows, K, y, x=x, xq=xq, ncols=ncols, y_ld=y.shape[-1])
+    _check(mq_check_mv_desc(d), "mq_check_mv_desc")
+    dd = upload_struct(d, W.device)
+    fn = {"q4_0": mq_matvec_q4_0_q8_0, "q8_0": mq_matvec_q8_0_q8_0}[wtype]
+    _check(fn(_ptr(dd), rows, K, ncols, _stream(stream)), f"mq_matvec_{wtype}_q8_0")
     return y, dd
 
 

@@ -44,6 +44,8 @@ def test_sizes(mq_lib):
     assert mq_lib.mq_quant_block_elems(mq_lib.MQ_TYPE_Q8_0) == 32
     assert mq_lib.mq_quant_block_bytes(mq_lib.MQ_TYPE_Q8_0) == 34
     assert mq_lib.mq_quant_block_bytes(99) == 0
+    assert mq_lib.mq_quant_block_elems(mq_lib.MQ_TYPE_Q4_0) == 32
+    assert mq_lib.mq_quant_block_bytes(mq_lib.MQ_TYPE_Q4_0) == 18
     assert mq_lib.mq_abi_version() == 2
     assert mq_lib.mq_status_string(0) == "ok"
     assert "shape" in mq_lib.mq_status_string(2)
@@ -86,6 +88,12 @@ def test_host_validation_rejects_before_launch(mq_lib):
     assert m.mq_quantize_q8_0(0x1002, 0x1000, 64, 1) == m.MQ_ERR_ALIGN
     assert m.mq_quantize_q8_0(0x1000, 0x1001, 64, 1) == m.MQ_ERR_ALIGN
     assert m.mq_quantize_q8_0(0x1000, 0x1000, 48, 1) == m.MQ_ERR_SHAPE
+    for fn in (m.mq_matvec_q4_0_q8_0, m.mq_matvec_q8_0_q8_0):  # other weight types: same checks
+        assert fn(0, 10, 100, 1) == m.MQ_ERR_SHAPE
+        assert fn(0, 10, 256, 9) == m.MQ_ERR_SHAPE
+        assert fn(0, 0, 256, 1) == m.MQ_OK
+        assert fn(0, 10, 256, 1) == m.MQ_ERR_INVALID_ARG
+        assert fn(0x1004, 10, 256, 1) == m.MQ_ERR_ALIGN
     assert m.mq_ffn_gu_silu_down(0, 3584, 100, 1) == m.MQ_ERR_SHAPE
     assert m.mq_ffn_gu_silu_down(0, 3584, 18944, 1) == m.MQ_ERR_INVALID_ARG
     assert m.mq_step(0, m.StepShape(0, 3584, 18944, 4608, 3584, 3584, 1, 0)) == m.MQ_OK   # no layers
