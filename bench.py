@@ -413,6 +413,22 @@ def config_suite(mq, device):
         calls, keep = mv_calls(copies, synth.KSWEEP_ROWS, K, x, y)
         rec(f"ksweep_4096x{K}", timed(calls, 5), W.numel(), copies=ncopy)
         del copies, keep
+    # the other weight types (q4_0: the pages' 0.5B model; q8_0), 4096 x 14336, rotated copies
+    K = 14336
+    x = torch.from_numpy(synth.activation(K, 1, seed=synth.KSWEEP_SEED)).to(device)
+    y = torch.empty((1, synth.KSWEEP_ROWS), dtype=torch.float32, device=device)
+    for wt in ("q4_0", "q8_0"):
+        W = torch.from_numpy(synth.wq_matrix(wt, synth.KSWEEP_ROWS, K, seed=synth.KSWEEP_SEED)).to(device)
+        ncopy = l2 // W.numel() + 1
+        copies = [W] + [W.clone() for _ in range(ncopy - 1)]
+        fn = mq.mq_matvec_q4_0_q8_0 if wt == "q4_0" else mq.mq_matvec_q8_0_q8_0
+        descs = [mq.upload_struct(mq.mv_desc(c_, synth.KSWEEP_ROWS, K, y, x=x), device) for c_ in copies]
+
+        def mk(d, fn=fn):
+            return lambda: mq._check(fn(d.data_ptr(), synth.KSWEEP_ROWS, K, 1,
+                                        torch.cuda.current_stream().cuda_stream), "matvec")
+        rec(f"{wt}_weights_4096x{K}", timed([mk(d) for d in descs], 5), W.numel(), copies=ncopy)
+        del copies, descs
     torch.cuda.synchronize()
     return out
 
