@@ -15,7 +15,9 @@ cudaError_t set_gu_attributes(int max_smem);
 cudaError_t set_ring_attributes(int max_smem);
 cudaError_t set_step_attributes(int max_smem);
 cudaError_t set_wring_attributes(int max_smem);
-void plan_ring(MvPlan& q, int64_t units, int kind, int nc, const DeviceInfo& dev, int64_t unit_bytes);
+cudaError_t set_ring_cols_attributes(int max_smem);
+void plan_ring(MvPlan& q, int64_t units, int kind, int nc, const DeviceInfo& dev, int64_t unit_bytes,
+               bool allow_cols);
 }  // namespace mq
 
 namespace {
@@ -114,8 +116,58 @@ bool plan_mv(int64_t rows, int K, int nc, int kind, int I, const DeviceInfo& dev
     q.block = int(32 * nw);
     q.smem = int(smem);
     q.variant = 0;
-    if (ring_only || variant_policy() != VARIANT_FORCE_REGISTER) plan_ring(q, units, kind, nc, dev, unit_bytes);
+    if (ring_only || variant_policy() != VARIANT_FORCE_REGISTER)
+        plan_ring(q, units, kind, nc, dev, unit_bytes, !ring_only);  // column lanes: q4_K only
     *p = q;
+    return true;
+}
+
+// How the consumer warps split a row of C units (128 weights each) for nc
+// columns, shared by the per-matrix and the persistent plans so that both
+// reduce in the same order (bit-identical results):
+//  * unit lanes (1..4 columns, or 5..8 when column lanes do not fit): L lanes
+//    per (row, segment) item, lane l on unit seg*S + l, nseg segments of S <= L
+//    units, wmax = 15 consumer warps for 1..2 columns, 8 for more;
+//  * column lanes (5..8 columns, q4_K, when the segments fit in 15 warps):
+//    one item per warp, lane = (unit-lane, column), 4 unit-lanes per item, 15
+//    consumer warps.  (Measured on GB300: faster than unit lanes from 5
+//    columns up, slower at 3 and 4, where the unit lanes' once-per-unit scale
+//    unpacking wins.)
+// Returns false when the segments do not fit in the warps.
+static bool unit_split(int C, int nc, bool allow_cols, MvPlan& q)
+{
+    q.cmap = 0;
+    if (nc >= 5 && allow_cols) {
+        const int lu = 32 / (nc <= 4 ? 4 : 8);
+        int nseg = (C + lu - 1) / lu;
+        const int S = (C + nseg - 1) / nseg;
+        nseg = (C + S - 1) / S;
+        if (nseg <= 15) {
+            q.cmap = 1;
+            q.L = 32;  // one item per warp
+            q.nseg = nseg;
+            q.S = S;
+            q.nwc = nseg * (15 / nseg);
+            q.rg = q.nwc / nseg;
+            return true;
+        }
+    }
+    if (C <= 8) {
+        q.L = 8;
+        q.nseg = 1;
+    } else if (C <= 16) {
+        q.L = 16;
+        q.nseg = 1;
+    } else {
+        q.L = 32;
+        q.nseg = (C + 31) / 32;
+    }
+    q.S = (C + q.nseg - 1) / q.nseg;
+    q.nseg = (C + q.S - 1) / q.S;
+    const int wmax = (nc <= 2) ? 15 : 8;
+    if (q.nseg > wmax) return false;
+    q.nwc = q.nseg * (wmax / q.nseg);
+    q.rg = (q.nwc / q.nseg) * (32 / q.L);
     return true;
 }
 
@@ -127,28 +179,15 @@ bool plan_mv(int64_t rows, int K, int nc, int kind, int I, const DeviceInfo& dev
 //  * tiles of T = 2*rg*m rows (about 24 KB), at most the CTA's rows rounded up;
 //  * 2..8 stages, within ~110 KB of shared memory when possible so that the
 //    next kernel's CTA fits beside this one under programmatic dependent launch.
-void plan_ring(MvPlan& q0, int64_t units, int kind, int nc, const DeviceInfo& dev, int64_t unit_bytes)
+void plan_ring(MvPlan& q0, int64_t units, int kind, int nc, const DeviceInfo& dev, int64_t unit_bytes,
+               bool allow_cols)
 {
     // work unit: half a super-block (128 weights); C counts units per row here
     MvPlan q = q0;
     q.C = q0.C / 2;
-    if (q.C <= 8) {
-        q.L = 8;
-        q.nseg = 1;
-    } else if (q.C <= 16) {
-        q.L = 16;
-        q.nseg = 1;
-    } else {
-        q.L = 32;
-        q.nseg = (q.C + 31) / 32;
-    }
-    q.S = (q.C + q.nseg - 1) / q.nseg;
-    q.nseg = (q.C + q.S - 1) / q.S;
-    const int wmax = (nc <= 2) ? 15 : 8;  // consumer warps (the kernel's launch bound minus the producer)
-    if (q.nseg > wmax) return;
-    const int nwc = q.nseg * (wmax / q.nseg);
-    const int ipw = 32 / q.L;
-    const int rg = (nwc / q.nseg) * ipw;
+    if (!unit_split(q.C, nc, allow_cols, q)) return;
+    const int nwc = q.nwc;
+    const int rg = q.rg;
     const int64_t row_bytes = int64_t(q.C) * unit_bytes;  // q.C units of 128 weights
     // tiles of whole row pairs per row-lane (consumers take two rows per step)
     const int64_t unit = 2 * rg * row_bytes;
@@ -199,7 +238,7 @@ bool plan_step(const mq_step_shape& h, const DeviceInfo& dev, StepPlan* out)
 {
     StepPlan sp = {};
     const int nc = h.ncols;
-    const int wmax = (nc <= 2) ? 15 : 8;
+    int nwc_max = 1;  // consumer warps of the kernel: the most any phase uses
     const int64_t G = dev.num_sms;
     const int kinds[4] = {KIND_MV, KIND_MV, KIND_GU, KIND_DOWN};
     const int64_t Ks[4] = {h.H, h.o_K, h.H, h.I};
@@ -208,21 +247,8 @@ bool plan_step(const mq_step_shape& h, const DeviceInfo& dev, StepPlan* out)
     for (int ph = 0; ph < 4; ++ph) {
         MvPlan q = {};
         q.C = int(Ks[ph] / 128);
-        if (q.C <= 8) {
-            q.L = 8;
-            q.nseg = 1;
-        } else if (q.C <= 16) {
-            q.L = 16;
-            q.nseg = 1;
-        } else {
-            q.L = 32;
-            q.nseg = (q.C + 31) / 32;
-        }
-        q.S = (q.C + q.nseg - 1) / q.nseg;
-        q.nseg = (q.C + q.S - 1) / q.S;
-        if (q.nseg > wmax) return false;
-        q.nwc = q.nseg * (wmax / q.nseg);
-        q.rg = (q.nwc / q.nseg) * (32 / q.L);
+        if (!unit_split(q.C, nc, true, q)) return false;
+        if (q.nwc > nwc_max) nwc_max = q.nwc;
         const bool gu = kinds[ph] == KIND_GU;
         const int64_t units = gu ? Rs[ph] / 32 : Rs[ph];
         const int64_t upc = (units + G - 1) / G;
@@ -271,7 +297,7 @@ bool plan_step(const mq_step_shape& h, const DeviceInfo& dev, StepPlan* out)
     // prefetched tiles before use and crowd the critical path's loads)
     int64_t pf = int64_t(dev.l2_bytes) / 3 / (G * stage);
     sp.pf_tiles = int(pf < 0 ? 0 : (pf > 16 ? 16 : pf));
-    sp.nwc = wmax;
+    sp.nwc = nwc_max;
     sp.grid = int(G);
     sp.smem = int(off_vals + vals);
     *out = sp;
@@ -285,6 +311,7 @@ cudaError_t set_kernel_attributes(int max_smem)
     if (e == cudaSuccess) e = set_ring_attributes(max_smem);
     if (e == cudaSuccess) e = set_step_attributes(max_smem);
     if (e == cudaSuccess) e = set_wring_attributes(max_smem);
+    if (e == cudaSuccess) e = set_ring_cols_attributes(max_smem);
     return e;
 }
 

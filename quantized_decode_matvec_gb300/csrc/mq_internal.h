@@ -32,6 +32,7 @@ struct MvPlan {
     int off_ring, off_act, off_part, off_vals;  // shared-memory offsets
     int fault;         // test-only: FAULT_* injected by the ring kernels (0 = none)
     int wait_ms;       // limit of every mbarrier wait of the ring kernels
+    int cmap;          // 1: column lanes (3..8 columns, ring_consume_cols), 0: unit lanes
 };
 
 // Plan of the persistent step kernel: one ring plan per phase (qkv, o, gate/up,

@@ -13,12 +13,21 @@ namespace mq {
 // accumulators).  The register file is split between the SM's four
 // schedulers, so the busiest scheduler's warp count sets the per-thread
 // budget: 16 warps (4 per scheduler) allow 128 registers, 17 only 96.
-template <int NC>
-constexpr int ring_max_warps()
+template <int NC, bool kCols = false>
+__host__ __device__ constexpr int ring_max_warps()
 {
-    return NC <= 2 ? 16 : 9;
+    return (NC <= 2 || kCols) ? 16 : 9;
 }
 constexpr int ring_max_consumers(int nc) { return nc <= 2 ? 15 : 8; }
+
+// Column lanes (3..8 columns): lane = (unit-lane ul, column c) with c the low
+// bits; cols_group columns per group (4 or 8), 32/cols_group unit-lanes per
+// item.
+template <int NC>
+__host__ __device__ constexpr int cols_group()
+{
+    return NC <= 4 ? 4 : 8;
+}
 
 // Sum of v over the L lanes of each lane group, into every lane of the group.
 template <int L>
@@ -143,12 +152,82 @@ __device__ __noinline__ bool ring_consume_L(const ConsumeArgs p, const uint8_t* 
     return true;
 }
 
+// Consumer side for 3..8 columns with column lanes: lane (ul, c) keeps the
+// codes and scales of unit seg*S + ul of column c in registers (so every
+// column's activation stays in registers, whatever the column count), loads
+// that unit's weights of each row (the lanes of one unit read the same bytes:
+// shared-memory broadcast) and reduces over its unit-lanes per column.  The
+// warp <-> (segment, row-lane) split, tiles, partials and combine order are
+// those of ring_consume_L with one item per warp.
 template <int NC, class Fmt = FmtQ4K>
+__device__ __noinline__ bool ring_consume_cols(const ConsumeArgs p, const uint8_t* ring, uint64_t* full,
+                                               uint64_t* empty, const UnitAct act, float* __restrict__ part,
+                                               uint64_t limit_ns)
+{
+    constexpr int CP = cols_group<NC>();
+    const int nrows = p.nrows, tile_base = p.tile_base, nwc_used = p.nwc_used;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nseg = p.nseg;
+    const int seg = warp % nseg, jj = warp / nseg;
+    const int c = lane % CP, ul = lane / CP;
+    const int rg = p.rg;
+    const int u = seg * p.S + ul;
+    const bool warp_active = warp < nwc_used;
+    const bool on = warp_active && (ul < p.S) && (u < p.C) && (c < NC);
+    const uint32_t row_bytes = Fmt::row_bytes(p.C);
+    const typename Fmt::Off off = Fmt::offsets(on ? u : 0);
+    uint4 A[8];
+    float4 DQ = make_float4(0.f, 0.f, 0.f, 0.f), DQSQ = DQ;
+    if (on) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) A[k] = act.planes[size_t(c * 8 + k) * act.U + u];
+        DQ = act.scales[(size_t(c) * act.U + u) * 2];
+        DQSQ = act.scales[(size_t(c) * act.U + u) * 2 + 1];
+    }
+    const int ntiles = (nrows + p.T - 1) / p.T;
+    for (int i = 0; i < ntiles; ++i) {
+        const int gi = tile_base + i;
+        const int s = gi % p.ns;
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], uint32_t(gi / p.ns) & 1u, limit_ns));
+        if (!ok) return false;
+        const uint8_t* stage = ring + uint32_t(s) * uint32_t(p.stage_bytes);
+        const int tr0 = i * p.T, tn = min(p.T, nrows - tr0);
+        for (int r = warp_active ? jj : tn; r < tn; r += 2 * rg) {
+            const int ra = r, rb = r + rg;
+            const bool va = on && ra < tn, vb = on && rb < tn;
+            float acc_a = 0.0f, acc_b = 0.0f;
+            if (va || vb) {
+                typename Fmt::W wa, wb;
+                Fmt::load(stage + uint32_t(va ? ra : rb) * row_bytes, off, wa);
+                Fmt::load(stage + uint32_t(vb ? rb : ra) * row_bytes, off, wb);
+                const typename Fmt::S ka = Fmt::prep(wa, off), kb = Fmt::prep(wb, off);
+                if (va) acc_a = Fmt::column(wa, ka, A, DQ, DQSQ);
+                if (vb) acc_b = Fmt::column(wb, kb, A, DQ, DQSQ);
+            }
+#pragma unroll
+            for (int o = CP; o < 32; o <<= 1) {
+                acc_a += __shfl_xor_sync(0xffffffffu, acc_a, o);
+                acc_b += __shfl_xor_sync(0xffffffffu, acc_b, o);
+            }
+            if (ul == 0 && c < NC) {
+                if (ra < tn) part[((tr0 + ra) * nseg + seg) * NC + c] = acc_a;
+                if (rb < tn) part[((tr0 + rb) * nseg + seg) * NC + c] = acc_b;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    return true;
+}
+
+// kCols: the kernel was built for column lanes (its plans all have cmap = 1)
+template <int NC, class Fmt = FmtQ4K, bool kCols = false>
 __device__ __forceinline__ bool ring_consume(const MvPlan& p, int nrows, int tile_base, int nwc_used,
                                              const uint8_t* ring, uint64_t* full, uint64_t* empty,
                                              const UnitAct& act, float* __restrict__ part, uint64_t limit_ns)
 {
     const ConsumeArgs a = consume_args(p, nrows, tile_base, nwc_used);
+    if constexpr (kCols) return ring_consume_cols<NC, Fmt>(a, ring, full, empty, act, part, limit_ns);
     if (p.L == 32) return ring_consume_L<NC, 32, Fmt>(a, ring, full, empty, act, part, limit_ns);
     if (p.L == 16) return ring_consume_L<NC, 16, Fmt>(a, ring, full, empty, act, part, limit_ns);
     return ring_consume_L<NC, 8, Fmt>(a, ring, full, empty, act, part, limit_ns);
