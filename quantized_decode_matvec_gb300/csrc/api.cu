@@ -127,7 +127,7 @@ bool plan_mv(int64_t rows, int K, int nc, int kind, int I, const DeviceInfo& dev
 // reduce in the same order (bit-identical results):
 //  * unit lanes (1..4 columns, or 5..8 when column lanes do not fit): L lanes
 //    per (row, segment) item, lane l on unit seg*S + l, nseg segments of S <= L
-//    units, wmax = 15 consumer warps for 1..2 columns, 8 for more;
+//    units, up to 15 consumer warps (3..8 columns: 8 when they divide evenly);
 //  * column lanes (5..8 columns, q4_K, when the segments fit in 15 warps):
 //    one item per warp, lane = (unit-lane, column), 4 unit-lanes per item, 15
 //    consumer warps.  (Measured on GB300: faster than unit lanes from 5
@@ -164,17 +164,19 @@ static bool unit_split(int C, int nc, bool allow_cols, MvPlan& q)
     }
     q.S = (C + q.nseg - 1) / q.nseg;
     q.nseg = (C + q.S - 1) / q.S;
-    const int wmax = (nc <= 2) ? 15 : 8;
-    if (q.nseg > wmax) return false;
-    q.nwc = q.nseg * (wmax / q.nseg);
+    if (q.nseg > 15) return false;
+    // 3..8 columns: 8 warps (9-warp kernel, more registers per thread) when the
+    // segments fill them, else up to 15 (16-warp kernel): long rows split into
+    // 3, 5, 6, 7 ... segments would leave most of the 8 warps idle
+    const int w8 = (q.nseg <= 8) ? q.nseg * (8 / q.nseg) : 0;
+    q.nwc = (nc >= 3 && w8 == 8) ? 8 : q.nseg * (15 / q.nseg);
     q.rg = (q.nwc / q.nseg) * (32 / q.L);
     return true;
 }
 
 // Bulk-copy ring plan on top of a register-streaming plan q (same rows per CTA,
 // same segments).  Leaves q unchanged when the ring does not apply.
-//  * consumers: nwc = nseg * floor(wmax/nseg) warps (wmax 15 for one column,
-//    8 for more), segment-stationary,
+//  * consumers: nwc warps from unit_split, segment-stationary,
 //    rg = warps per segment * items per warp row-lanes;
 //  * tiles of T = 2*rg*m rows (about 24 KB), at most the CTA's rows rounded up;
 //  * 2..8 stages, within ~110 KB of shared memory when possible so that the

@@ -13,12 +13,14 @@ namespace mq {
 // accumulators).  The register file is split between the SM's four
 // schedulers, so the busiest scheduler's warp count sets the per-thread
 // budget: 16 warps (4 per scheduler) allow 128 registers, 17 only 96.
-template <int NC, bool kCols = false>
+// kMode: 0 = unit lanes, the kernel built for 1..2 columns (16 warps) or the
+// 9-warp form; 1 = column lanes (16 warps); 2 = unit lanes for 3..8 columns
+// with 16 warps (activation columns read from shared memory per row pair)
+template <int NC, int kMode = 0>
 __host__ __device__ constexpr int ring_max_warps()
 {
-    return (NC <= 2 || kCols) ? 16 : 9;
+    return (NC <= 2 || kMode != 0) ? 16 : 9;
 }
-constexpr int ring_max_consumers(int nc) { return nc <= 2 ? 15 : 8; }
 
 // Column lanes (3..8 columns): lane = (unit-lane ul, column c) with c the low
 // bits; cols_group columns per group (4 or 8), 32/cols_group unit-lanes per
@@ -220,14 +222,14 @@ __device__ __noinline__ bool ring_consume_cols(const ConsumeArgs p, const uint8_
     return true;
 }
 
-// kCols: the kernel was built for column lanes (its plans all have cmap = 1)
-template <int NC, class Fmt = FmtQ4K, bool kCols = false>
+// kMode 1: the kernel was built for column lanes (its plans all have cmap = 1)
+template <int NC, class Fmt = FmtQ4K, int kMode = 0>
 __device__ __forceinline__ bool ring_consume(const MvPlan& p, int nrows, int tile_base, int nwc_used,
                                              const uint8_t* ring, uint64_t* full, uint64_t* empty,
                                              const UnitAct& act, float* __restrict__ part, uint64_t limit_ns)
 {
     const ConsumeArgs a = consume_args(p, nrows, tile_base, nwc_used);
-    if constexpr (kCols) return ring_consume_cols<NC, Fmt>(a, ring, full, empty, act, part, limit_ns);
+    if constexpr (kMode == 1) return ring_consume_cols<NC, Fmt>(a, ring, full, empty, act, part, limit_ns);
     if (p.L == 32) return ring_consume_L<NC, 32, Fmt>(a, ring, full, empty, act, part, limit_ns);
     if (p.L == 16) return ring_consume_L<NC, 16, Fmt>(a, ring, full, empty, act, part, limit_ns);
     return ring_consume_L<NC, 8, Fmt>(a, ring, full, empty, act, part, limit_ns);

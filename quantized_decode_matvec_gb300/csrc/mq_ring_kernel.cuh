@@ -38,8 +38,8 @@ namespace mq {
 // ring tiles a CTA issues before its dependency wait (the rest follow the activation)
 constexpr int kEarlyTiles = 2;
 
-template <int NC, int KIND, class Fmt = FmtQ4K, bool kCols = false>
-__global__ void __launch_bounds__(32 * ring_max_warps<NC, kCols>(), 1)
+template <int NC, int KIND, class Fmt = FmtQ4K, int kMode = 0>
+__global__ void __launch_bounds__(32 * ring_max_warps<NC, kMode>(), 1)
     ring_kernel(const void* __restrict__ desc, int a_h, int b_h, MvPlan p, unsigned* status)
 {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(32 * ring_max_warps<NC, kCols>(), 1)
             stage_units_q8<NC>(xq, K, act, nullptr, ctid, cthr);
         named_barrier_sync(1, cthr);
         named_barrier_arrive(2, cthr + 32);  // release the producer's remaining ring tiles
-        if (!ring_consume<NC, Fmt, kCols>(p, nrows, 0, p.nwc, ring, full, empty, act, part, limit_ns) && lane == 0)
+        if (!ring_consume<NC, Fmt, kMode>(p, nrows, 0, p.nwc, ring, full, empty, act, part, limit_ns) && lane == 0)
             abort_flag = 1;
     }
     __syncthreads();

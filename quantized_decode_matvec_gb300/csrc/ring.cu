@@ -7,7 +7,7 @@ namespace mq {
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-// column-lane instances (3..8 columns), in ring_cols.cu
+// 3..8 columns with 16 warps (column lanes, or unit lanes beyond 8 warps), in ring_cols.cu
 cudaError_t launch_ring_cols(const void* desc, int kind, int a, int b, int ncols, const MvPlan& p, unsigned* status,
                              cudaStream_t s, bool pdl);
 
@@ -37,7 +37,9 @@ static cudaError_t launch_ring_kind(const void* desc, int a, int b, int ncols, c
 cudaError_t launch_ring(const void* desc, int kind, int a, int b, int ncols, const MvPlan& p, unsigned* status,
                         cudaStream_t s, bool pdl)
 {
-    if (p.cmap) return launch_ring_cols(desc, kind, a, b, ncols, p, status, s, pdl);
+    // 3..8 columns beyond 8 consumer warps: the 16-warp instances
+    if (ncols >= 3 && (p.cmap || p.block > 32 * ring_max_warps<3>()))
+        return launch_ring_cols(desc, kind, a, b, ncols, p, status, s, pdl);
     if (p.block > 32 * (ncols <= 2 ? ring_max_warps<1>() : ring_max_warps<3>())) return cudaErrorInvalidConfiguration;
     switch (kind) {
         case KIND_MV: return launch_ring_kind<KIND_MV>(desc, a, b, ncols, p, status, s, pdl);

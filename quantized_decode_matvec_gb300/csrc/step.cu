@@ -222,7 +222,7 @@ __device__ __forceinline__ unsigned check_layers(const mq_layer_desc* layers, co
 }
 
 template <int NC>
-__global__ void __launch_bounds__(32 * ring_max_warps<NC, true>(), 1)
+__global__ void __launch_bounds__(32 * ring_max_warps<NC, 1>(), 1)
     step_kernel(const mq_layer_desc* __restrict__ layers, StepPlan sp, unsigned* status, unsigned* ws)
 {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -336,7 +336,7 @@ __global__ void __launch_bounds__(32 * ring_max_warps<NC, true>(), 1)
             named_barrier_sync(1, cthr);
             bool ok;
             if (NC >= 3 && P.cmap)  // the same split as the per-matrix kernel of this shape
-                ok = ring_consume<NC, FmtQ4K, true>(P, pr.nrows, gi, P.nwc, ring, full, empty, act, part, limit_ns);
+                ok = ring_consume<NC, FmtQ4K, 1>(P, pr.nrows, gi, P.nwc, ring, full, empty, act, part, limit_ns);
             else
                 ok = ring_consume<NC>(P, pr.nrows, gi, P.nwc, ring, full, empty, act, part, limit_ns);
             gi += (pr.nrows + P.T - 1) / P.T;
