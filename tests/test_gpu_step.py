@@ -246,7 +246,7 @@ def test_step_7b_full_size_sampled(cuda_ready):
     wdev, host = _weights(case)
     bufs = _bufs(mq, case, wdev)
     multi = _bufs(mq, case, wdev)
-    g = StepGraph(bufs, flags=mq.MQ_STEP_PERSISTENT)   # the configuration the benchmark times
+    g = StepGraph(bufs, flags=mq.MQ_STEP_PDL)   # the configuration the benchmark times by default
     assert g.captured, g.capture_error
     rng = np.random.default_rng(0)
     rows = rng.choice(1 << 20, 48, replace=False)
@@ -258,9 +258,9 @@ def test_step_7b_full_size_sampled(cuda_ready):
         layers = range(case.n_layers) if r == 0 else (0, case.n_layers - 1)
         for l in layers:
             _check_layer_oracle(case, host, outs, a, b, c, l, rows=rows)
-        if r == 2:  # the multi-kernel path gives the same bytes at full size
+        if r == 2:  # the persistent kernel gives the same bytes at full size
             _set_inputs(multi, a, b, c)
-            multi.step()
+            multi.step(flags=mq.MQ_STEP_PERSISTENT)
             m = _outputs(multi)
             for k in outs:
                 assert np.array_equal(outs[k].view(np.uint8), m[k].view(np.uint8)), k
