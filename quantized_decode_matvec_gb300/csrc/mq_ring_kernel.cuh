@@ -38,6 +38,8 @@ namespace mq {
 // ring tiles a CTA issues before its dependency wait (the rest follow the
 // activation); 1 or 3 measured slower for the down projection, equal elsewhere
 constexpr int kEarlyTiles = 2;
+// each CTA prefetches its share of the activation's lines into L2 before the wait
+constexpr bool kPrefetchAct = true;
 
 template <int NC, int KIND, class Fmt = FmtQ4K, int kMode = 0>
 __global__ void __launch_bounds__(32 * ring_max_warps<NC, kMode>(), 1)
@@ -149,6 +151,12 @@ __global__ void __launch_bounds__(32 * ring_max_warps<NC, kMode>(), 1)
         // queued behind a ring's worth of weight bytes on their way into this SM.
         if (lane == 0)
             for (; issued < ntiles && issued < kEarlyTiles && issued < p.ns; ++issued) issue(issued);
+        if (kPrefetchAct && lane == 1) {  // the activation into L2 (a hint), each line by one CTA
+            const char* a = x ? reinterpret_cast<const char*>(x) : reinterpret_cast<const char*>(xq);
+            const size_t abytes = x ? size_t(NC) * K * 4 : size_t(NC) * (K / kQK8) * kQ8Bytes;
+            for (size_t o = size_t(blockIdx.x) * 128; o < abytes; o += size_t(gridDim.x) * 128)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(a + o));
+        }
         __syncwarp();
         griddep_wait();
         named_barrier_sync(2, (p.nwc + 1) * 32);  // the consumers' staging is done
