@@ -81,7 +81,7 @@ __device__ __noinline__ bool ring_consume_L(const ConsumeArgs p, const uint8_t* 
                                             uint64_t* empty, const UnitAct act, float* __restrict__ part,
                                             uint64_t limit_ns)
 {
-    const int nrows = p.nrows, tile_base = p.tile_base, nwc_used = p.nwc_used;
+    const int nrows = p.nrows, nwc_used = p.nwc_used;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nseg = p.nseg;
     const int seg = warp % nseg, jj = warp / nseg;
@@ -95,61 +95,57 @@ __device__ __noinline__ bool ring_consume_L(const ConsumeArgs p, const uint8_t* 
     const bool warp_active = warp < nwc_used;
     const bool on = warp_active && (l < p.S) && (u < p.C);
     const uint32_t row_bytes = Fmt::row_bytes(p.C);
-    const typename Fmt::Off off = Fmt::offsets(u);
+    // A lane without a unit computes on unit 0 and drops the result, and rows
+    // past the tile's end are clamped to its last row: the row loop has no
+    // divergent branch, only selects and predicated stores.
+    const int uu = on ? u : 0;
+    const typename Fmt::Off off = Fmt::offsets(uu);
 
     constexpr bool kRegAct = NC <= 2;
     uint4 A[NC][8];
     float4 DQ[NC], DQSQ[NC];
     auto load_act = [&](int c, int slot) {  // column c's codes and scales into A[slot], DQ[slot], DQSQ[slot]
 #pragma unroll
-        for (int k = 0; k < 8; ++k) A[slot][k] = act.planes[size_t(c * 8 + k) * act.U + u];
-        DQ[slot] = act.scales[(size_t(c) * act.U + u) * 2];
-        DQSQ[slot] = act.scales[(size_t(c) * act.U + u) * 2 + 1];
+        for (int k = 0; k < 8; ++k) A[slot][k] = act.planes[size_t(c * 8 + k) * act.U + uu];
+        DQ[slot] = act.scales[(size_t(c) * act.U + uu) * 2];
+        DQSQ[slot] = act.scales[(size_t(c) * act.U + uu) * 2 + 1];
     };
-    if (kRegAct && on) {
+    if (kRegAct) {
 #pragma unroll
         for (int c = 0; c < NC; ++c) load_act(c, c);
     }
-    auto load_w = [&](const uint8_t* stage, int rr, typename Fmt::W& w) {
-        Fmt::load(stage + uint32_t(rr) * row_bytes, off, w);
-    };
 
-    const int ntiles = (nrows + p.T - 1) / p.T;
-    for (int i = 0; i < ntiles; ++i) {
-        const int gi = tile_base + i;  // position in the ring's tile sequence
-        const int s = gi % p.ns;
-        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], uint32_t(gi / p.ns) & 1u, limit_ns));
+    int s = p.tile_base % p.ns;  // ring stage and its parity, advanced per tile
+    uint32_t par = uint32_t(p.tile_base / p.ns) & 1u;
+    for (int tr0 = 0; tr0 < nrows; tr0 += p.T) {
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], par, limit_ns));
         if (!ok) return false;
         const uint8_t* stage = ring + uint32_t(s) * uint32_t(p.stage_bytes);
-        const int tr0 = i * p.T, tn = min(p.T, nrows - tr0);
-        for (int r = warp_active ? rho0 : tn; r < tn; r += 2 * rg) {
+        const int tn = min(p.T, nrows - tr0);
+        for (int r = warp_active ? rho0 : tn; r < tn; r += 2 * rg) {  // r is warp-uniform
             const int ra = r + sub, rb = r + rg + sub;
             const bool va = on && ra < tn, vb = on && rb < tn;
-            float acc_a[NC], acc_b[NC];
-#pragma unroll
-            for (int c = 0; c < NC; ++c) acc_a[c] = acc_b[c] = 0.0f;
-            if (va || vb) {
-                typename Fmt::W wa, wb;
-                load_w(stage, va ? ra : rb, wa);
-                load_w(stage, vb ? rb : ra, wb);
-                const typename Fmt::S ka = Fmt::prep(wa, off), kb = Fmt::prep(wb, off);
-#pragma unroll
-                for (int c = 0; c < NC; ++c) {
-                    if (!kRegAct) load_act(c, 0);
-                    const int cc = kRegAct ? c : 0;
-                    if (va) acc_a[c] = Fmt::column(wa, ka, A[cc], DQ[cc], DQSQ[cc]);
-                    if (vb) acc_b[c] = Fmt::column(wb, kb, A[cc], DQ[cc], DQSQ[cc]);
-                }
-            }
+            typename Fmt::W wa, wb;
+            Fmt::load(stage + uint32_t(min(ra, tn - 1)) * row_bytes, off, wa);
+            Fmt::load(stage + uint32_t(min(rb, tn - 1)) * row_bytes, off, wb);
+            const typename Fmt::S ka = Fmt::prep(wa, off), kb = Fmt::prep(wb, off);
 #pragma unroll
             for (int c = 0; c < NC; ++c) {
-                const float t = group_sum2<L>(acc_a[c], acc_b[c], l);
+                if (!kRegAct) load_act(c, 0);
+                const int cc = kRegAct ? c : 0;
+                const float xa = Fmt::column(wa, ka, A[cc], DQ[cc], DQSQ[cc]);
+                const float xb = Fmt::column(wb, kb, A[cc], DQ[cc], DQSQ[cc]);
+                const float t = group_sum2<L>(va ? xa : 0.0f, vb ? xb : 0.0f, l);
                 if (l == 0 && ra < tn) part[((tr0 + ra) * nseg + seg) * NC + c] = t;
                 if (l == (L >> 1) && rb < tn) part[((tr0 + rb) * nseg + seg) * NC + c] = t;
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
+        if (++s == p.ns) {
+            s = 0;
+            par ^= 1u;
+        }
     }
     return true;
 }
