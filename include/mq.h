@@ -53,7 +53,7 @@
 extern "C" {
 #endif
 
-#define MQ_ABI_VERSION 2
+#define MQ_ABI_VERSION 3
 
 typedef int mq_status;
 #define MQ_OK 0
@@ -218,8 +218,9 @@ typedef struct mq_layer_desc {
 #define MQ_STEP_PDL 1u         /* multi-kernel path: launch with programmatic dependent launch */
 #define MQ_STEP_PERSISTENT 2u  /* one persistent kernel for the whole stack (needs `workspace`) */
 
-/* bytes of device workspace the persistent step needs (grid-barrier words) */
-#define MQ_STEP_WORKSPACE_BYTES 256
+/* bytes of the persistent step's fixed workspace words (abort word, per-CTA
+ * phase flags); the whole workspace a shape needs is mq_step_workspace_bytes */
+#define MQ_STEP_WORKSPACE_BYTES 4352
 
 typedef struct mq_step_shape {
     int32_t n_layers;
@@ -231,20 +232,29 @@ typedef struct mq_step_shape {
     int32_t ncols;
     uint32_t flags;   /* MQ_STEP_* */
     void* workspace;  /* MQ_STEP_PERSISTENT: caller-owned device memory of
-                         MQ_STEP_WORKSPACE_BYTES, 4-byte aligned; zeroed by
-                         the call on its stream (so a captured graph re-zeroes
-                         it every replay); two steps that overlap on the GPU
-                         must not share it */
+                         mq_step_workspace_bytes(shape) bytes, 16-byte
+                         aligned; zeroed by the call on its stream (so a
+                         captured graph re-zeroes it every replay); two steps
+                         that overlap on the GPU must not share it */
 } mq_step_shape;
 
 /* Without MQ_STEP_PERSISTENT: four launches per layer (qkv, o, gate/up, down).
  * With it: a single cooperative launch of one CTA per SM that runs every
- * layer, the weight stream running ahead across the dependency points, which
- * are grid-wide barriers on `workspace` (bounded waits; a timeout records
- * MQ_DEV_TIMEOUT).  Both give bit-identical outputs.  The persistent kernel
- * needs every SM: it fails with MQ_ERR_CUDA if the device cannot host its
- * whole grid at once. */
+ * layer, the weight stream running ahead across the dependency points.  At
+ * each point a CTA waits, bounded in time (a timeout records MQ_DEV_TIMEOUT),
+ * until every CTA has finished the previous phase: each CTA publishes a phase
+ * flag in `workspace` after it has written that phase's outputs, and the
+ * gate/up phase also writes h there as tagged records (a data word and its
+ * phase in one 8-byte store), which the down phase reads and checks.  Both
+ * paths give bit-identical outputs.  The persistent kernel needs every SM: it
+ * fails with MQ_ERR_CUDA if the device cannot host its whole grid at once. */
 mq_status mq_step(const mq_layer_desc* d_layers, const mq_step_shape* h_shape, void* stream);
+
+/* Bytes of workspace mq_step needs for h_shape with MQ_STEP_PERSISTENT:
+ * MQ_STEP_WORKSPACE_BYTES plus ncols * (I/128) * 320 bytes of h records.
+ * Host only; checks the shape as mq_step does (MQ_ERR_SHAPE, and
+ * MQ_ERR_INVALID_ARG for a null pointer). */
+mq_status mq_step_workspace_bytes(const mq_step_shape* h_shape, size_t* bytes);
 
 /* ---- the FFN without caller scratch --------------------------------------------------
  * No counterpart in the pages: they describe the FFN kernels, not how a

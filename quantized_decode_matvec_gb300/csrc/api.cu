@@ -301,7 +301,9 @@ bool plan_step(const mq_step_shape& h, const DeviceInfo& dev, StepPlan* out)
     sp.pf_tiles = int(pf < 0 ? 0 : (pf > 16 ? 16 : pf));
     sp.nwc = nwc_max;
     sp.grid = int(G);
+    if (sp.grid > kWsMaxCtas) return false;  // one phase flag per CTA in the workspace
     sp.smem = int(off_vals + vals);
+    sp.ws_bytes = step_workspace_bytes(nc, h.I);
     *out = sp;
     return true;
 }
@@ -600,6 +602,16 @@ mq_status mq_ffn_gate_up(const mq_ffn_desc* d_desc, int32_t H, int32_t I, int32_
     return e == cudaSuccess ? MQ_OK : cuda_fail(e);
 }
 
+mq_status mq_step_workspace_bytes(const mq_step_shape* h, size_t* bytes)
+{
+    if (!h || !bytes) return MQ_ERR_INVALID_ARG;
+    if (h->n_layers < 0 || h->ncols < 0) return MQ_ERR_SHAPE;
+    mq_status st = check_ffn_shape(h->H, h->I, h->ncols);
+    if (st != MQ_OK) return st;
+    *bytes = mq::step_workspace_bytes(h->ncols, h->I);
+    return MQ_OK;
+}
+
 mq_status mq_step(const mq_layer_desc* d_layers, const mq_step_shape* h, void* stream)
 {
     if (!h) return MQ_ERR_INVALID_ARG;
@@ -614,7 +626,7 @@ mq_status mq_step(const mq_layer_desc* d_layers, const mq_step_shape* h, void* s
     if (h->qkv_rows == 0 || h->o_rows == 0) return MQ_ERR_SHAPE;
     if (h->flags & MQ_STEP_PERSISTENT) {
         if (!h->workspace) return MQ_ERR_INVALID_ARG;
-        if (!aligned(h->workspace, 4)) return MQ_ERR_ALIGN;
+        if (!aligned(h->workspace, 16)) return MQ_ERR_ALIGN;
     }
     const mq::DeviceInfo* dev = nullptr;
     if ((st = current_dev(&dev)) != MQ_OK) return st;

@@ -341,4 +341,33 @@ __device__ __forceinline__ void chunk_accumulate_regs(const Chunk& k, int c4, co
         acc[c] = chunk_column(k, fd0, fd1, fm0, fm1, P[c][0], P[c][1], P[c][2], P[c][3], SC[c], acc[c]);
 }
 
+// Tagged records: a 32-bit word and a 32-bit tag written by one 8-byte
+// relaxed store at GPU scope.  An aligned 8-byte access is single-copy atomic,
+// so a relaxed load at GPU scope of the same record returns the word together
+// with the tag it was stored with: a reader that sees the tag it expects has
+// the word, with no fence on either side.
+__device__ __forceinline__ void st_tagged(uint64_t* p, uint32_t word, uint32_t tag)
+{
+    const uint64_t v = uint64_t(word) | (uint64_t(tag) << 32);
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// two consecutive records (16-byte aligned); each 8-byte element is atomic
+__device__ __forceinline__ void ld_tagged2(const uint64_t* p, uint64_t& a, uint64_t& b)
+{
+    asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+
+__device__ __forceinline__ void st_relaxed_u32(unsigned* p, unsigned v)
+{
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p)
+{
+    unsigned v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 }  // namespace mq

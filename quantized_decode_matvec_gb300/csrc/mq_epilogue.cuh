@@ -26,11 +26,18 @@ __device__ __forceinline__ void mv_epilogue(const float* __restrict__ part, int 
 // b0 .. b0 + n/32 - 1 of each column).  Called by all threads of the CTA.
 // Runs on threads tid = 0..nthr-1 (whole warps); `sync` is a barrier over
 // exactly those threads.
+//
+// rec (nullable): h also as tagged records in the activation's unit layout,
+// for a reader in the same launch: per column 40 * (I/128) records, record r
+// carrying word r of the unit layout (code planes, then dq and dq*sumq per
+// block) with `tag` in its upper half; one 8-byte store per record, so a
+// reader that sees the tag sees the word with it.
 template <int NC, typename SyncFn>
 __device__ __forceinline__ void gu_epilogue_on(const float* __restrict__ part, float* __restrict__ vals, int nseg,
                                                int n, int i0, int I, uint8_t* __restrict__ hq,
                                                float* __restrict__ gu_dbg, float* __restrict__ h_dbg, int tid,
-                                               int nthr, SyncFn sync)
+                                               int nthr, SyncFn sync, uint64_t* __restrict__ rec = nullptr,
+                                               uint32_t tag = 0)
 {
     const int nrows = 2 * n;
     const int nblk = I / kQK8, b0 = i0 / kQK8;
@@ -58,6 +65,24 @@ __device__ __forceinline__ void gu_epilogue_on(const float* __restrict__ part, f
         if (lane == 0) *reinterpret_cast<uint16_t*>(ob) = __half_as_ushort(dh);
         ob[2 + lane] = uint8_t(int8_t(q));
         if (h_dbg) h_dbg[size_t(c) * I + i0 + i] = h;
+        if (rec) {
+            // block j = unit j/4, slot j%4: codes 16k..16k+15 of the unit are plane k
+            // (four words), so this block's 32 codes are planes 2*slot and 2*slot+1
+            const int j = b0 + k, uh = j >> 2, slot = j & 3, Uh = I / 128;
+            const uint32_t byte = uint32_t(q) & 0xffu;
+            const uint32_t w = byte | (__shfl_down_sync(0xffffffffu, byte, 1) << 8) |
+                               (__shfl_down_sync(0xffffffffu, byte, 2) << 16) |
+                               (__shfl_down_sync(0xffffffffu, byte, 3) << 24);
+            const int sq = __reduce_add_sync(0xffffffffu, q);
+            if ((lane & 3) == 0)
+                st_tagged(rec + ((size_t(c) * 8 + 2 * slot + (lane >> 4)) * Uh + uh) * 4 + ((lane & 15) >> 2), w, tag);
+            if (lane == 0) {
+                const float dq = __half2float(dh);
+                uint64_t* sr = rec + size_t(NC) * 32 * Uh + (size_t(c) * Uh + uh) * 8;
+                st_tagged(sr + slot, __float_as_uint(dq), tag);
+                st_tagged(sr + 4 + slot, __float_as_uint(dq * float(sq)), tag);
+            }
+        }
     }
 }
 

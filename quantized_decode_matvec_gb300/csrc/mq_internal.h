@@ -37,7 +37,18 @@ struct MvPlan {
 
 // Plan of the persistent step kernel: one ring plan per phase (qkv, o, gate/up,
 // down) sharing the ring geometry and shared-memory layout of ph[0].
+// Persistent-step workspace (bytes): [0, 256) control words (word 1: abort),
+// [256, 4352) one phase flag (u32) per CTA, then the h records: per column
+// 40 * (I/128) records of 8 bytes (a 32-bit word of the activation's unit
+// layout and the phase that wrote it).
+constexpr int kWsFlagsOff = 256;
+constexpr int kWsMaxCtas = 1024;
+constexpr int kWsRecOff = kWsFlagsOff + 4 * kWsMaxCtas;
+static_assert(kWsRecOff == MQ_STEP_WORKSPACE_BYTES, "workspace layout and header disagree");
+inline size_t step_workspace_bytes(int ncols, int I) { return size_t(kWsRecOff) + size_t(ncols) * (I / 128) * 40 * 8; }
+
 struct StepPlan {
+    size_t ws_bytes;  // workspace the launch zeroes and uses
     MvPlan ph[4];
     int K[4];      // reduction length per phase
     int R[4];      // rows per phase (gate/up: I)

@@ -12,13 +12,19 @@
 //   shared memory while phase p finishes: weights are never written by any
 //   kernel, so fetching them early is always correct;
 // * consumers follow the dependency chain a real decode has: before a
-//   phase stages its activation they wait at a grid-wide barrier until every
-//   CTA has written the previous phase's outputs (the down projection really
-//   reads the h_q8 written by the gate/up phase; the other inputs stand for
-//   results of the previous phase and are treated the same way);
-// * every wait (ring mbarriers, grid barrier) is bounded in time; on a
-//   timeout a CTA records MQ_DEV_TIMEOUT, raises the step's abort word so the
-//   other CTAs stop too, drains its own copies in flight and returns.
+//   phase stages its activation they wait until every CTA has written the
+//   previous phase's outputs.  The down projection really reads the h written
+//   by the gate/up phase: that phase also writes h as tagged records (a word
+//   of the activation's unit layout and the phase, in one 8-byte store), and
+//   the down phase copies them into shared memory once every tag is there.
+//   The other inputs stand for results of the previous phase: after a phase's
+//   outputs are written each CTA publishes a phase flag, and the next phase
+//   waits for every CTA's flag.  No fence sits on this path: the records
+//   carry their own readiness, and the flags only order phases whose inputs
+//   no CTA of this launch writes;
+// * every wait (ring mbarriers, phase flags, h records) is bounded in time;
+//   on a timeout a CTA records MQ_DEV_TIMEOUT, raises the step's abort word so
+//   the other CTAs stop too, drains its own copies in flight and returns.
 //
 // Arithmetic, segment split and combine order per matrix are those of the
 // per-matrix ring kernels, so the outputs are bit-identical to mq_step's
@@ -32,33 +38,73 @@
 
 namespace mq {
 
-// Grid barrier on the step workspace: word 0 counts CTA arrivals (monotonic
-// within a launch, zeroed by the host before it), word 1 is the abort word.
-__device__ __forceinline__ void grid_arrive(unsigned* ws)
-{
-    // release at GPU scope: orders this CTA's earlier writes (gathered by the
-    // preceding CTA barrier) before the arrival
-    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ws) : "memory");
-}
+// record pairs a staging thread loads per round
+constexpr int kRecBatch = 4;
 
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p)
-{
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
+// Dependency points on the step workspace (zeroed by the host before each
+// launch): word 1 is the abort word, then one phase flag per CTA, then the h
+// records.  Tags and flags are "phase number + 1", so zero means "not yet".
 
-// true when the count reaches target; false on timeout or when another CTA aborted
-__device__ __forceinline__ bool grid_wait(unsigned* ws, unsigned target, uint64_t limit_ns)
+// Wait until every CTA's phase flag is at least `target`; the consumer threads
+// share the CTAs' flags out between them.  False on a timeout or when another
+// CTA aborted.
+__device__ __forceinline__ bool wait_flags(const unsigned* flags, int G, unsigned target, const unsigned* abort_word,
+                                           uint64_t limit_ns, int tid, int nthr)
 {
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 0;; ++it) {
-        if (ld_acquire_gpu(ws) >= target) return true;
+        bool ready = true;
+        for (int i = tid; i < G; i += nthr) ready &= ld_relaxed_u32(flags + i) >= target;
+        if (__all_sync(0xffffffffu, ready)) return true;
         if ((it & 15u) == 15u) {
-            if (ld_acquire_gpu(ws + 1) != 0) return false;
-            if (global_timer_ns() - t0 > limit_ns) return false;
+            const bool stop = ld_relaxed_u32(abort_word) != 0 || global_timer_ns() - t0 > limit_ns;
+            if (__any_sync(0xffffffffu, stop)) return false;
         }
     }
+}
+
+// The down phase's activation: the h records that this launch's gate/up phase
+// wrote with `tag`, copied word for word into the unit layout (record r is
+// word r of the planes-then-scales area).  Each thread loads its share of
+// record pairs and reads again the ones whose tag is not there yet, bounded
+// in time.  False on a timeout or when another CTA aborted.
+template <int NC>
+__device__ __forceinline__ bool stage_units_rec(const uint64_t* rec, int U, UnitAct s, uint32_t tag,
+                                                const unsigned* abort_word, uint64_t limit_ns, int tid, int nthr)
+{
+    uint32_t* dst = reinterpret_cast<uint32_t*>(s.planes);
+    const int npair = NC * 20 * U;  // 40 * U words per column, two per load
+    constexpr int B = kRecBatch;
+    for (int p0 = tid; p0 < npair; p0 += B * nthr) {
+        uint64_t a[B], b[B];
+#pragma unroll
+        for (int k = 0; k < B; ++k) {
+            const int i = p0 + k * nthr;
+            a[k] = b[k] = uint64_t(tag) << 32;  // pairs past the end count as there
+            if (i < npair) ld_tagged2(rec + 2 * size_t(i), a[k], b[k]);
+        }
+        uint64_t t0 = 0;
+        for (uint32_t it = 0;; ++it) {
+            bool all = true;
+#pragma unroll
+            for (int k = 0; k < B; ++k)
+                if (uint32_t(a[k] >> 32) != tag || uint32_t(b[k] >> 32) != tag) {
+                    all = false;
+                    ld_tagged2(rec + 2 * size_t(p0 + k * nthr), a[k], b[k]);
+                }
+            if (all) break;
+            if (it == 0)
+                t0 = global_timer_ns();
+            else if ((it & 15u) == 0 && (ld_relaxed_u32(abort_word) != 0 || global_timer_ns() - t0 > limit_ns))
+                return false;
+        }
+#pragma unroll
+        for (int k = 0; k < B; ++k) {
+            const int i = p0 + k * nthr;
+            if (i < npair) *reinterpret_cast<uint2*>(dst + 2 * i) = make_uint2(uint32_t(a[k]), uint32_t(b[k]));
+        }
+    }
+    return true;
 }
 
 // phase views of a layer descriptor
@@ -232,6 +278,8 @@ __global__ void __launch_bounds__(32 * ring_max_warps<NC, 1>(), 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nwc = sp.nwc;
     const uint64_t limit_ns = uint64_t(P0.wait_ms) * 1000000ull;
+    unsigned* const flags = ws + kWsFlagsOff / 4;
+    uint64_t* const rec = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(ws) + kWsRecOff);
 
     {
         const unsigned bad = check_layers(layers, sp, NC);  // every CTA reaches the same verdict
@@ -319,21 +367,23 @@ __global__ void __launch_bounds__(32 * ring_max_warps<NC, 1>(), 1)
             const PhaseJob j = phase_job(&layers[l], ph);
             const PhaseRows pr = phase_rows(sp, ph, b, G);
             const int K = sp.K[ph];
-            // wait until every CTA has written the previous phase's outputs
-            if (k > 0) {
-                if (ctid == 0 && !grid_wait(ws, unsigned(k) * unsigned(G), limit_ns)) abort_flag = 1;
-                named_barrier_sync(1, cthr);
-                if (abort_flag) return false;
-            }
+            // wait until every CTA has written the previous phase's outputs: the
+            // down phase reads h itself as tagged records; the other phases, whose
+            // inputs are separate buffers standing for the previous phase's
+            // results, wait for every CTA's flag of that phase
+            if (k > 0 && ph != 3 && !wait_flags(flags, G, unsigned(k), ws + 1, limit_ns, ctid, cthr) && lane == 0)
+                abort_flag = 1;
             const UnitAct act{reinterpret_cast<uint4*>(smem + P0.off_act),
                               reinterpret_cast<float4*>(smem + P0.off_act + size_t(NC) * 8 * P.C * 16), P.C};
-            if (ph == 3)
-                stage_units_q8<NC, true>(j.xq, K, act, nullptr, ctid, cthr);  // h_q8: written in this kernel
-            else if (j.x)
+            if (ph == 3) {
+                if (!stage_units_rec<NC>(rec, P.C, act, unsigned(k), ws + 1, limit_ns, ctid, cthr)) abort_flag = 1;
+            } else if (j.x) {
                 stage_units_x<NC>(j.x, K, act, (ph <= 1 && b == 0) ? j.xq_out : nullptr, nullptr, ctid, cthr);
-            else
+            } else {
                 stage_units_q8<NC>(j.xq, K, act, nullptr, ctid, cthr);
+            }
             named_barrier_sync(1, cthr);
+            if (abort_flag) return false;
             bool ok;
             if (NC >= 3 && P.cmap)  // the same split as the per-matrix kernel of this shape
                 ok = ring_consume<NC, FmtQ4K, 1>(P, pr.nrows, gi, P.nwc, ring, full, empty, act, part, limit_ns);
@@ -345,12 +395,13 @@ __global__ void __launch_bounds__(32 * ring_max_warps<NC, 1>(), 1)
             if (abort_flag) return false;
             if (ph == 2) {
                 gu_epilogue_on<NC>(part, vals, P.nseg, pr.n, pr.i0, pr.R, static_cast<uint8_t*>(j.ffn->h_q8),
-                                   j.ffn->gu_dbg, j.ffn->h_dbg, ctid, cthr, [cthr]() { named_barrier_sync(1, cthr); });
+                                   j.ffn->gu_dbg, j.ffn->h_dbg, ctid, cthr, [cthr]() { named_barrier_sync(1, cthr); },
+                                   rec, unsigned(k + 1));
             } else {
                 mv_epilogue<NC>(part, P.nseg, pr.nrows, pr.r0, j.y, j.y_ld, ctid, cthr);
             }
             named_barrier_sync(1, cthr);  // this CTA's outputs of phase k are written
-            if (ctid == 0 && k + 1 < nphase) grid_arrive(ws);
+            if (ctid == 0 && k + 1 < nphase) st_relaxed_u32(flags + b, unsigned(k + 1));
             return true;
         };
         for (int l = 0; l < sp.n_layers; ++l)
@@ -369,7 +420,7 @@ __global__ void __launch_bounds__(32 * ring_max_warps<NC, 1>(), 1)
 cudaError_t launch_step(const mq_layer_desc* layers, const StepPlan& sp, int ncols, unsigned* status, unsigned* ws,
                         cudaStream_t s)
 {
-    cudaError_t e = cudaMemsetAsync(ws, 0, 2 * sizeof(unsigned), s);
+    cudaError_t e = cudaMemsetAsync(ws, 0, sp.ws_bytes, s);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(sp.grid);
@@ -377,7 +428,7 @@ cudaError_t launch_step(const mq_layer_desc* layers, const StepPlan& sp, int nco
     cfg.dynamicSmemBytes = sp.smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs resident at once: the grid barrier needs it
+    attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs resident at once: the phase waits need it
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;

@@ -52,7 +52,7 @@ MQ_MAX_K = 131072
 MQ_MAX_K_TIMES_NCOLS = 163840
 MQ_STEP_PDL = 1
 MQ_STEP_PERSISTENT = 2
-MQ_STEP_WORKSPACE_BYTES = 256
+MQ_STEP_WORKSPACE_BYTES = 4352
 MQ_NOALLOC_HQ8_MAX_BYTES = 131072
 
 
@@ -104,6 +104,7 @@ _sig("mq_check_ffn_desc", c_i32, ctypes.POINTER(FfnDesc))
 _sig("mq_ffn_gu_silu_down", c_i32, c_vp, c_i32, c_i32, c_i32, c_vp)
 _sig("mq_ffn_gate_up", c_i32, c_vp, c_i32, c_i32, c_i32, c_vp)
 _sig("mq_step", c_i32, c_vp, ctypes.POINTER(StepShape), c_vp)
+_sig("mq_step_workspace_bytes", c_i32, ctypes.POINTER(StepShape), ctypes.POINTER(ctypes.c_size_t))
 _sig("mq_ffn_gu_silu_down_noalloc", c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_vp)
 _sig("mq_debug_block_sums_q4K_q8_0", c_i32, c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp)
 _sig("mq_debug_set_variant", c_i32, c_i32)
@@ -113,7 +114,7 @@ _sig("mq_debug_set_fault", c_i32, c_i32)
 EXPORTS = ["mq_status_string", "mq_abi_version", "mq_last_cuda_error", "mq_init", "mq_read_device_status",
            "mq_q4K_row_bytes", "mq_q8_0_bytes", "mq_quant_block_elems", "mq_quant_block_bytes",
            "mq_concat_rows_feasible", "mq_concat_rows", "mq_quantize_q8_0", "mq_check_mv_desc",
-           "mq_matvec_q4K_q8_0", "mq_matvec_q4_0_q8_0", "mq_matvec_q8_0_q8_0", "mq_check_ffn_desc", "mq_ffn_gu_silu_down", "mq_ffn_gate_up", "mq_step",
+           "mq_matvec_q4K_q8_0", "mq_matvec_q4_0_q8_0", "mq_matvec_q8_0_q8_0", "mq_check_ffn_desc", "mq_ffn_gu_silu_down", "mq_ffn_gate_up", "mq_step", "mq_step_workspace_bytes",
            "mq_ffn_gu_silu_down_noalloc",
            "mq_debug_block_sums_q4K_q8_0", "mq_debug_set_variant", "mq_debug_set_fault"]
 
@@ -221,6 +222,12 @@ def mq_ffn_gate_up(d_desc: int, H: int, I: int, ncols: int, stream: int = 0) -> 
 
 def mq_step(d_layers: int, shape: StepShape, stream: int = 0) -> int:
     return _lib.mq_step(c_vp(d_layers), ctypes.byref(shape), c_vp(stream))
+
+
+def mq_step_workspace_bytes(shape: StepShape) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_lib.mq_step_workspace_bytes(ctypes.byref(shape), ctypes.byref(n)), "mq_step_workspace_bytes")
+    return int(n.value)
 
 
 def mq_ffn_gu_silu_down_noalloc(W_gu: int, W_down: int, x: int, xq: int, y: int, H: int, I: int, ncols: int,
@@ -441,8 +448,9 @@ class StepBuffers:
             _check(mq_check_ffn_desc(table[l].ffn), "mq_check_ffn_desc")
         self.table_host = table
         self.table = upload_struct(bytes(table), dev)
-        # grid-barrier words of the persistent step (zeroed by mq_step itself)
-        self.workspace = torch.zeros(MQ_STEP_WORKSPACE_BYTES, dtype=torch.uint8, device=dev)
+        # dependency words and h records of the persistent step (zeroed by mq_step itself)
+        nbytes = mq_step_workspace_bytes(StepShape(n, H, I, qkv_rows, o_rows, o_K, ncols, 0, None))
+        self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
 
     def shape(self, flags: int = 0) -> StepShape:
         return StepShape(self.n_layers, self.H, self.I, self.qkv_rows, self.o_rows, self.o_K, self.ncols, flags,

@@ -46,7 +46,7 @@ def test_sizes(mq_lib):
     assert mq_lib.mq_quant_block_bytes(99) == 0
     assert mq_lib.mq_quant_block_elems(mq_lib.MQ_TYPE_Q4_0) == 32
     assert mq_lib.mq_quant_block_bytes(mq_lib.MQ_TYPE_Q4_0) == 18
-    assert mq_lib.mq_abi_version() == 2
+    assert mq_lib.mq_abi_version() == 3
     assert mq_lib.mq_status_string(0) == "ok"
     assert "shape" in mq_lib.mq_status_string(2)
 
@@ -138,3 +138,21 @@ def test_persistent_step_needs_workspace(mq_lib):
     assert m.mq_step(0x1000, shape) == m.MQ_ERR_INVALID_ARG
     shape.workspace = 0x2002
     assert m.mq_step(0x1000, shape) == m.MQ_ERR_ALIGN
+    shape.workspace = 0x2008  # the h records are read 16 bytes at a time
+    assert m.mq_step(0x1000, shape) == m.MQ_ERR_ALIGN
+
+
+def test_step_workspace_bytes(mq_lib):
+    m = mq_lib
+    # fixed words (abort word, one phase flag per CTA), then per column
+    # 40 records of 8 bytes per 128 elements of h
+    shape = m.StepShape(28, 3584, 18944, 4608, 3584, 3584, 1, m.MQ_STEP_PERSISTENT, None)
+    assert m.mq_step_workspace_bytes(shape) == 4352 + 18944 // 128 * 320
+    shape.ncols = 8
+    assert m.mq_step_workspace_bytes(shape) == 4352 + 8 * (18944 // 128) * 320
+    n = ctypes.c_size_t(0)
+    lib = m._lib
+    assert lib.mq_step_workspace_bytes(None, ctypes.byref(n)) == m.MQ_ERR_INVALID_ARG
+    assert lib.mq_step_workspace_bytes(ctypes.byref(shape), None) == m.MQ_ERR_INVALID_ARG
+    shape.I = 1000  # not a multiple of 256
+    assert lib.mq_step_workspace_bytes(ctypes.byref(shape), ctypes.byref(n)) == m.MQ_ERR_SHAPE
