@@ -39,7 +39,7 @@
 namespace mq {
 
 // record pairs a staging thread loads per round
-constexpr int kRecBatch = 4;
+constexpr int kRecBatch = 8;
 
 // Dependency points on the step workspace (zeroed by the host before each
 // launch): word 1 is the abort word, then one phase flag per CTA, then the h
