@@ -127,7 +127,9 @@ bool plan_mv(int64_t rows, int K, int nc, int kind, int I, const DeviceInfo& dev
 // reduce in the same order (bit-identical results):
 //  * unit lanes (1..4 columns, or 5..8 when column lanes do not fit): L lanes
 //    per (row, segment) item, lane l on unit seg*S + l, nseg segments of S <= L
-//    units, up to 15 consumer warps (3..8 columns: 8 when they divide evenly);
+//    units, up to 15 consumer warps (1..2 columns: the L of 32, 16, 8, 4 with
+//    the fewest idle lanes and warps; 3..8 columns: 8 warps when they divide
+//    evenly);
 //  * column lanes (5..8 columns, q4_K, when the segments fit in 15 warps):
 //    one item per warp, lane = (unit-lane, column), 4 unit-lanes per item, 15
 //    consumer warps.  (Measured on GB300: faster than unit lanes from 5
@@ -151,6 +153,32 @@ static bool unit_split(int C, int nc, bool allow_cols, MvPlan& q)
             q.rg = q.nwc / nseg;
             return true;
         }
+    }
+    if (nc <= 2) {
+        // Unit lanes, 1..2 columns: the consumers are issue-bound, so pick the
+        // items of L lanes (32, 16, 8 or 4) that leave the fewest lanes and
+        // warps idle; ties go to the longer items (fewer partials per row).
+        // K = 3584, 28 units: 7 segments of 4 units on 4-lane items in 14 warps
+        // (every lane busy) instead of one segment of 28 on 32 lanes.
+        double best = 0.0;
+        for (const int L : {32, 16, 8, 4}) {
+            int nseg = (C + L - 1) / L;
+            const int S = (C + nseg - 1) / nseg;
+            nseg = (C + S - 1) / S;
+            if (nseg > 15) continue;
+            const int nwc = nseg * (15 / nseg);
+            const double score = double(C) / double(nseg * L) * double(nwc) / 15.0;
+            if (score > best + 1e-9) {
+                best = score;
+                q.L = L;
+                q.nseg = nseg;
+                q.S = S;
+                q.nwc = nwc;
+            }
+        }
+        if (best <= 0.0) return false;
+        q.rg = (q.nwc / q.nseg) * (32 / q.L);
+        return true;
     }
     if (C <= 8) {
         q.L = 8;

@@ -95,9 +95,9 @@ __device__ __noinline__ bool ring_consume_L(const ConsumeArgs p, const uint8_t* 
     const bool warp_active = warp < nwc_used;
     const bool on = warp_active && (l < p.S) && (u < p.C);
     const uint32_t row_bytes = Fmt::row_bytes(p.C);
-    // A lane without a unit computes on unit 0 and drops the result, and rows
-    // past the tile's end are clamped to its last row: the row loop has no
-    // divergent branch, only selects and predicated stores.
+    // 1..2 columns: a lane without a unit computes on unit 0 and drops the
+    // result, and rows past the tile's end are clamped to its last row, so the
+    // row loop has no divergent branch, only selects and predicated stores.
     const int uu = on ? u : 0;
     const typename Fmt::Off off = Fmt::offsets(uu);
 
@@ -125,17 +125,43 @@ __device__ __noinline__ bool ring_consume_L(const ConsumeArgs p, const uint8_t* 
         for (int r = warp_active ? rho0 : tn; r < tn; r += 2 * rg) {  // r is warp-uniform
             const int ra = r + sub, rb = r + rg + sub;
             const bool va = on && ra < tn, vb = on && rb < tn;
-            typename Fmt::W wa, wb;
-            Fmt::load(stage + uint32_t(min(ra, tn - 1)) * row_bytes, off, wa);
-            Fmt::load(stage + uint32_t(min(rb, tn - 1)) * row_bytes, off, wb);
-            const typename Fmt::S ka = Fmt::prep(wa, off), kb = Fmt::prep(wb, off);
+            float xa[NC], xb[NC];
+            if constexpr (kRegAct) {
+                typename Fmt::W wa, wb;
+                Fmt::load(stage + uint32_t(min(ra, tn - 1)) * row_bytes, off, wa);
+                Fmt::load(stage + uint32_t(min(rb, tn - 1)) * row_bytes, off, wb);
+                const typename Fmt::S ka = Fmt::prep(wa, off), kb = Fmt::prep(wb, off);
+#pragma unroll
+                for (int c = 0; c < NC; ++c) {
+                    xa[c] = Fmt::column(wa, ka, A[c], DQ[c], DQSQ[c]);
+                    xb[c] = Fmt::column(wb, kb, A[c], DQ[c], DQSQ[c]);
+                }
+#pragma unroll
+                for (int c = 0; c < NC; ++c) {
+                    xa[c] = va ? xa[c] : 0.0f;
+                    xb[c] = vb ? xb[c] : 0.0f;
+                }
+            } else {
+                // 3..8 columns (activation read from shared memory per row pair):
+                // branches keep fewer values live than computing every lane
+#pragma unroll
+                for (int c = 0; c < NC; ++c) xa[c] = xb[c] = 0.0f;
+                if (va || vb) {
+                    typename Fmt::W wa, wb;
+                    Fmt::load(stage + uint32_t(va ? ra : rb) * row_bytes, off, wa);
+                    Fmt::load(stage + uint32_t(vb ? rb : ra) * row_bytes, off, wb);
+                    const typename Fmt::S ka = Fmt::prep(wa, off), kb = Fmt::prep(wb, off);
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) {
+                        load_act(c, 0);
+                        if (va) xa[c] = Fmt::column(wa, ka, A[0], DQ[0], DQSQ[0]);
+                        if (vb) xb[c] = Fmt::column(wb, kb, A[0], DQ[0], DQSQ[0]);
+                    }
+                }
+            }
 #pragma unroll
             for (int c = 0; c < NC; ++c) {
-                if (!kRegAct) load_act(c, 0);
-                const int cc = kRegAct ? c : 0;
-                const float xa = Fmt::column(wa, ka, A[cc], DQ[cc], DQSQ[cc]);
-                const float xb = Fmt::column(wb, kb, A[cc], DQ[cc], DQSQ[cc]);
-                const float t = group_sum2<L>(va ? xa : 0.0f, vb ? xb : 0.0f, l);
+                const float t = group_sum2<L>(xa[c], xb[c], l);
                 if (l == 0 && ra < tn) part[((tr0 + ra) * nseg + seg) * NC + c] = t;
                 if (l == (L >> 1) && rb < tn) part[((tr0 + rb) * nseg + seg) * NC + c] = t;
             }
@@ -228,6 +254,7 @@ __device__ __forceinline__ bool ring_consume(const MvPlan& p, int nrows, int til
     if constexpr (kMode == 1) return ring_consume_cols<NC, Fmt>(a, ring, full, empty, act, part, limit_ns);
     if (p.L == 32) return ring_consume_L<NC, 32, Fmt>(a, ring, full, empty, act, part, limit_ns);
     if (p.L == 16) return ring_consume_L<NC, 16, Fmt>(a, ring, full, empty, act, part, limit_ns);
+    if (NC <= 2 && p.L == 4) return ring_consume_L<NC, 4, Fmt>(a, ring, full, empty, act, part, limit_ns);
     return ring_consume_L<NC, 8, Fmt>(a, ring, full, empty, act, part, limit_ns);
 }
 
