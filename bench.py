@@ -603,7 +603,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--mode", choices=["persistent", "graph", "pdl"], default="pdl",
+    ap.add_argument("--mode", choices=["persistent", "graph", "pdl"], default="persistent",
                     help="step launch mode: one persistent kernel, or four kernels per layer (plain or PDL)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-config timings (context only)")
