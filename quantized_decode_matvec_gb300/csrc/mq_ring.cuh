@@ -115,6 +115,12 @@ __device__ __noinline__ bool ring_consume_L(const ConsumeArgs p, const uint8_t* 
         for (int c = 0; c < NC; ++c) load_act(c, c);
     }
 
+    // the partial this lane stores: lane 0 of an item holds row r + sub's sum,
+    // lane L/2 row r + rg + sub's (group_sum2); one pointer, advanced per step
+    const bool storer = l == 0 || l == (L >> 1);
+    const int srow = sub + (l == 0 ? 0 : rg);
+    const int pstep = 2 * rg * nseg * NC;
+
     int s = p.tile_base % p.ns;  // ring stage and its parity, advanced per tile
     uint32_t par = uint32_t(p.tile_base / p.ns) & 1u;
     for (int tr0 = 0; tr0 < nrows; tr0 += p.T) {
@@ -122,8 +128,10 @@ __device__ __noinline__ bool ring_consume_L(const ConsumeArgs p, const uint8_t* 
         if (!ok) return false;
         const uint8_t* stage = ring + uint32_t(s) * uint32_t(p.stage_bytes);
         const int tn = min(p.T, nrows - tr0);
-        for (int r = warp_active ? rho0 : tn; r < tn; r += 2 * rg) {  // r is warp-uniform
+        float* pq = part + (size_t(tr0 + rho0 + srow) * nseg + seg) * NC;
+        for (int r = warp_active ? rho0 : tn; r < tn; r += 2 * rg, pq += pstep) {  // r is warp-uniform
             const int ra = r + sub, rb = r + rg + sub;
+            const bool st = storer && r + srow < tn;
             const bool va = on && ra < tn, vb = on && rb < tn;
             float xa[NC], xb[NC];
             if constexpr (kRegAct) {
@@ -162,8 +170,7 @@ __device__ __noinline__ bool ring_consume_L(const ConsumeArgs p, const uint8_t* 
 #pragma unroll
             for (int c = 0; c < NC; ++c) {
                 const float t = group_sum2<L>(xa[c], xb[c], l);
-                if (l == 0 && ra < tn) part[((tr0 + ra) * nseg + seg) * NC + c] = t;
-                if (l == (L >> 1) && rb < tn) part[((tr0 + rb) * nseg + seg) * NC + c] = t;
+                if (st) pq[c] = t;
             }
         }
         __syncwarp();

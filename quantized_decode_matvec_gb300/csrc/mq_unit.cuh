@@ -258,14 +258,14 @@ __device__ __forceinline__ float byte_as_float(uint32_t w, int b)
     return __int_as_float(__byte_perm(w, 0x4B000000u, 0x7540u | uint32_t(b))) - 8388608.0f;
 }
 
-// Scales of the unit's four sub-blocks j = 4h..4h+3 as floats: sc[j], m[j]
-// (sc[1], sc[3] pre-divided by 16, exact, to match the in-place high nibbles
-// of unit_dot), and the block's d and dmin.
+// Scales of the unit's four sub-blocks j = 4h..4h+3: sc[j] as integers, m[j]
+// as floats, and the block's d and dmin.
 //   h = 0: sc_j = s[j] & 63, m_j = s[j+4] & 63                     (j = 0..3)
 //   h = 1: sc_j = (s[j+4] & 15) | (s[j-4] >> 6) << 4,
 //          m_j  = (s[j+4] >> 4) | (s[j] >> 6) << 4                  (j = 4..7)
 struct UnitScales {
-    float sc[4], m[4];
+    int sc[4];  // 0..63
+    float m[4];
     float d, dmin;
 };
 
@@ -278,10 +278,8 @@ __device__ __forceinline__ UnitScales unit_scales(const uint4& hd, bool upper)
     const uint32_t mhi = upper ? 0x30303030u : 0u;
     const uint32_t sc = ((upper ? S2 : S0) & mlo) | ((S0 >> 2) & mhi);
     const uint32_t m = ((upper ? (S2 >> 4) : S1) & mlo) | ((S1 >> 2) & mhi);
-    r.sc[0] = byte_as_float(sc, 0);
-    r.sc[1] = 0.0625f * byte_as_float(sc, 1);
-    r.sc[2] = byte_as_float(sc, 2);
-    r.sc[3] = 0.0625f * byte_as_float(sc, 3);
+#pragma unroll
+    for (int b = 0; b < 4; ++b) r.sc[b] = int(__byte_perm(sc, 0u, 0x4440u | uint32_t(b)));
 #pragma unroll
     for (int b = 0; b < 4; ++b) r.m[b] = byte_as_float(m, b);
     r.d = dd.x;
@@ -322,16 +320,18 @@ __device__ __forceinline__ void unit_dot(const UnitW& w, const uint4 (&A)[8], in
 
 // acc + the unit's contribution for one column:
 // sum_j dq_j*(d*sc_j*s_j - dmin*m_j*sumq_j)
-//   = d * sum_j sc_j*(dq_j*s_j) - dmin * sum_j m_j*(dq_j*sumq_j)
+//   = d * sum_j dq_j*(sc_j*s_j) - dmin * sum_j m_j*(dq_j*sumq_j)
 __device__ __forceinline__ float unit_column(const UnitW& w, const UnitScales& k, const uint4 (&A)[8],
                                              const float4& dq, const float4& dqsq, float acc)
 {
     int s[4];
     unit_dot(w, A, s);
-    float t = k.sc[0] * (dq.x * float(s[0]));
-    t = fmaf(k.sc[1], dq.y * float(s[1]), t);
-    t = fmaf(k.sc[2], dq.z * float(s[2]), t);
-    t = fmaf(k.sc[3], dq.w * float(s[3]), t);
+    // sc_j * s_j in int32 (|s_j| < 2^20 with the high nibbles in place, sc_j < 64);
+    // the high nibbles' factor 16 comes off dq_j (exact: a power of two)
+    float t = dq.x * float(k.sc[0] * s[0]);
+    t = fmaf(dq.y * 0.0625f, float(k.sc[1] * s[1]), t);
+    t = fmaf(dq.z, float(k.sc[2] * s[2]), t);
+    t = fmaf(dq.w * 0.0625f, float(k.sc[3] * s[3]), t);
     float u = k.m[0] * dqsq.x;
     u = fmaf(k.m[1], dqsq.y, u);
     u = fmaf(k.m[2], dqsq.z, u);
