@@ -312,9 +312,14 @@ mq_status mq_debug_set_variant(int32_t policy);
  * delivers each CTA's last tile and every wait is limited to 50 ms, so the
  * consumers' bounded waits run out: the kernels record MQ_DEV_TIMEOUT in the
  * device status word, write no output and return; the GPU context stays
- * usable.  MQ_FAULT_NONE restores normal operation. */
+ * usable.  MQ_FAULT_WITHHOLD_RECORDS: in the persistent step kernel the last
+ * CTA (which always owns h blocks) never writes its h records and every wait is limited to 50 ms, so every
+ * CTA's down phase runs out of time waiting for them: the kernel records
+ * MQ_DEV_TIMEOUT, the abort word stops every CTA, and the launch returns.
+ * MQ_FAULT_NONE restores normal operation. */
 #define MQ_FAULT_NONE 0
 #define MQ_FAULT_WITHHOLD_TILE 1
+#define MQ_FAULT_WITHHOLD_RECORDS 2
 mq_status mq_debug_set_fault(int32_t fault);
 
 #ifdef __cplusplus

@@ -294,8 +294,8 @@ bool plan_step(const mq_step_shape& h, const DeviceInfo& dev, StepPlan* out)
         q.T = int(T);
         q.rows_per_cta = int(rpc);
         q.variant = 1;
-        q.fault = FAULT_NONE;
-        q.wait_ms = 2000;
+        q.fault = fault_policy();
+        q.wait_ms = q.fault == FAULT_NONE ? 2000 : 50;
         const int64_t st = (T * row_bytes + 127) / 128 * 128;
         if (st > stage) stage = st;
         if (int64_t(nc) * q.C * 160 > act) act = int64_t(nc) * q.C * 160;
@@ -369,7 +369,8 @@ int mq_abi_version(void) { return MQ_ABI_VERSION; }
 
 mq_status mq_debug_set_fault(int32_t fault)
 {
-    if (fault != mq::FAULT_NONE && fault != mq::FAULT_WITHHOLD_TILE) return MQ_ERR_INVALID_ARG;
+    if (fault != mq::FAULT_NONE && fault != mq::FAULT_WITHHOLD_TILE && fault != mq::FAULT_WITHHOLD_RECORDS)
+        return MQ_ERR_INVALID_ARG;
     g_fault_policy = fault;
     return MQ_OK;
 }

@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(32 * ring_max_warps<NC, 1>(), 1)
             if (ph == 2) {
                 gu_epilogue_on<NC>(part, vals, P.nseg, pr.n, pr.i0, pr.R, static_cast<uint8_t*>(j.ffn->h_q8),
                                    j.ffn->gu_dbg, j.ffn->h_dbg, ctid, cthr, [cthr]() { named_barrier_sync(1, cthr); },
-                                   rec, unsigned(k + 1));
+                                   (P.fault == FAULT_WITHHOLD_RECORDS && b == G - 1) ? nullptr : rec, unsigned(k + 1));
             } else {
                 mv_epilogue<NC>(part, P.nseg, pr.nrows, pr.r0, j.y, j.y_ld, ctid, cthr);
             }

@@ -1,6 +1,7 @@
 """Failure detection without a GPU fault.
 
-The bulk-copy ring kernels bound every wait on their copy pipeline.  A
+The bulk-copy ring kernels bound every wait on their copy pipeline, and the
+persistent step kernel every wait at its dependency points.  A
 test-only setting makes the producer withhold each CTA's last tile, so the
 consumers' waits run out (a flag that nothing ever sets): the kernel must
 report MQ_DEV_TIMEOUT through the device status word, leave its output
@@ -44,3 +45,41 @@ def test_fault_setter_rejects_unknown(cuda_ready):
     mq = cuda_ready
     assert mq.mq_debug_set_fault(7) == mq.MQ_ERR_INVALID_ARG
     assert mq.mq_debug_set_variant(7) == mq.MQ_ERR_INVALID_ARG
+
+
+def test_persistent_step_record_wait_runs_out_and_reports(cuda_ready):
+    # the persistent step's dependency waits are bounded too: with the last
+    # CTA's h records withheld, every CTA's down phase runs out of time, the abort word
+    # stops the launch, and the next step runs normally
+    import torch
+    mq = cuda_ready
+    case = synth.StepCase("step_fault", 2, 512, 1024, 512, 128, 1, 11)
+    wdev = []
+    for l in range(case.n_layers):
+        w = synth.step_layer_weights(case, l)
+        wdev.append({"qkv": torch.from_numpy(np.concatenate([w["q"], w["k"], w["v"]])).cuda(),
+                     "o": torch.from_numpy(w["o"]).cuda(), "gu": torch.from_numpy(w["gu"]).cuda(),
+                     "down": torch.from_numpy(w["down"]).cuda()})
+    bufs = [mq.StepBuffers(wdev, case.H, case.I, case.qkv_rows, case.H, case.q_rows, 1) for _ in range(2)]
+    for b in bufs:
+        for l in range(case.n_layers):
+            inp = synth.step_layer_inputs(case, l, 3)
+            b.a[l].copy_(torch.from_numpy(inp["a"]))
+            b.b[l].copy_(torch.from_numpy(inp["b"]))
+            b.c[l].copy_(torch.from_numpy(inp["c"]))
+    assert mq.mq_read_device_status(0) == 0
+    assert mq.mq_debug_set_fault(mq.MQ_FAULT_WITHHOLD_RECORDS) == mq.MQ_OK
+    try:
+        bufs[0].step(flags=mq.MQ_STEP_PERSISTENT)
+        torch.cuda.synchronize()                     # returns: every wait is bounded
+    finally:
+        assert mq.mq_debug_set_fault(mq.MQ_FAULT_NONE) == mq.MQ_OK
+    assert mq.mq_read_device_status(0) & mq.MQ_DEV_TIMEOUT
+    # the context is still healthy: the persistent step now matches the multi-kernel step bit for bit
+    bufs[0].step(flags=mq.MQ_STEP_PERSISTENT)
+    bufs[1].step()
+    torch.cuda.synchronize()
+    assert mq.mq_read_device_status(0) == 0
+    for k in ("y_qkv", "y_o", "y_ffn", "h_q8"):
+        x, y = getattr(bufs[0], k).cpu().numpy(), getattr(bufs[1], k).cpu().numpy()
+        assert np.array_equal(x.view(np.uint8), y.view(np.uint8)), k
