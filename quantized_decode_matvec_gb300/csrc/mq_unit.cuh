@@ -246,6 +246,16 @@ __device__ __forceinline__ void stage_units_x(const float* __restrict__ x, int K
     }
 }
 
+// 16 bytes from shared memory (the ring's stages are written by the bulk-copy
+// engine and published by the mbarrier wait that precedes every read)
+__device__ __forceinline__ void lds128(uint4& v, uint32_t addr)
+{
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+}
+
 // The unit's weight bytes: header and 64 quant bytes (four 16-byte words).
 struct UnitW {
     uint4 h;                   // d, dmin, s[0..11]
@@ -363,11 +373,14 @@ struct FmtQ4K {
     }
     __device__ __forceinline__ static void load(const uint8_t* row, const Off& o, W& w)
     {
-        w.h = *reinterpret_cast<const uint4*>(row + o.h);
-        w.qa0 = *reinterpret_cast<const uint4*>(row + o.q);
-        w.qb0 = *reinterpret_cast<const uint4*>(row + o.q + 16);
-        w.qa1 = *reinterpret_cast<const uint4*>(row + o.q + 32);
-        w.qb1 = *reinterpret_cast<const uint4*>(row + o.q + 48);
+        // explicit shared-memory loads on a 32-bit address: the ring is shared
+        // memory, and the generic pointer's conversion stays out of the row loop
+        const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(row));
+        lds128(w.h, a + o.h);
+        lds128(w.qa0, a + o.q);
+        lds128(w.qb0, a + o.q + 16);
+        lds128(w.qa1, a + o.q + 32);
+        lds128(w.qb1, a + o.q + 48);
     }
     __device__ __forceinline__ static S prep(const W& w, const Off& o) { return unit_scales(w.h, o.upper); }
     __device__ __forceinline__ static float column(const W& w, const S& k, const uint4 (&A)[8], const float4& dq,
