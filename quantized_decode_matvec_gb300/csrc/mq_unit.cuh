@@ -63,7 +63,7 @@ __device__ __forceinline__ int group8_sum(int v)
 }
 
 // q8_0 blocks, one thread per block: the form for a 2-byte aligned xq.
-template <int NC, bool kL2Only>
+template <int NC>
 __device__ __forceinline__ void stage_units_q8_by_block(const uint8_t* __restrict__ xq, int K, UnitAct s,
                                                         int32_t* sumq_out, int tid, int nthr)
 {
@@ -73,7 +73,7 @@ __device__ __forceinline__ void stage_units_q8_by_block(const uint8_t* __restric
         const uint16_t* h = reinterpret_cast<const uint16_t*>(xq + (size_t(c) * nq + J) * kQ8Bytes);
         uint16_t v[17];
 #pragma unroll
-        for (int k = 0; k < 17; ++k) v[k] = kL2Only ? __ldcg(h + k) : __ldg(h + k);
+        for (int k = 0; k < 17; ++k) v[k] = __ldg(h + k);
         uint32_t w[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) w[k] = uint32_t(v[1 + 2 * k]) | (uint32_t(v[2 + 2 * k]) << 16);
@@ -91,32 +91,18 @@ __device__ __forceinline__ void stage_units_q8_by_block(const uint8_t* __restric
     }
 }
 
-// 32-bit load; kL2Only: a plain coherent load (not the read-only path), for
-// blocks written earlier in the same kernel by other CTAs and published by
-// the grid barrier's acquire.
-template <bool kL2Only>
-__device__ __forceinline__ uint32_t ld_word(const uint32_t* p)
-{
-    if (kL2Only) {
-        uint32_t v;
-        asm volatile("ld.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-        return v;
-    }
-    return __ldg(p);
-}
-
 // From q8_0 blocks in global memory (34-byte blocks; column c starts at byte
 // c*K/32*34).  sumq_out (nullable, test export): int32 [NC][K/32].
 // A unit's four blocks are 136 contiguous bytes at byte 136u of its column,
 // 34 words when xq is 4-byte aligned (K % 256 == 0 keeps every column and
 // unit on a word boundary): lanes load words 0..31 and lanes 0, 1 words 32,
 // 33, and each lane gathers its four codes and its block's scale by shuffles.
-template <int NC, bool kL2Only = false>
+template <int NC>
 __device__ __forceinline__ void stage_units_q8(const uint8_t* __restrict__ xq, int K, UnitAct s, int32_t* sumq_out,
                                                int tid, int nthr)
 {
     if (reinterpret_cast<uintptr_t>(xq) & 3) {
-        stage_units_q8_by_block<NC, kL2Only>(xq, K, s, sumq_out, tid, nthr);
+        stage_units_q8_by_block<NC>(xq, K, s, sumq_out, tid, nthr);
         return;
     }
     const int lane = tid & 31, warp = tid >> 5, nw = nthr >> 5;
@@ -141,9 +127,9 @@ __device__ __forceinline__ void stage_units_q8(const uint8_t* __restrict__ xq, i
             const int u2 = u + nw < U ? u + nw : u;
             const uint32_t* p = col + size_t(u) * 34;
             const uint32_t* p2 = col + size_t(u2) * 34;
-            const uint32_t w0 = ld_word<kL2Only>(p + lane), v0 = ld_word<kL2Only>(p2 + lane);
-            const uint32_t w1 = lane < 2 ? ld_word<kL2Only>(p + 32 + lane) : 0u;
-            const uint32_t v1 = lane < 2 ? ld_word<kL2Only>(p2 + 32 + lane) : 0u;
+            const uint32_t w0 = __ldg(p + lane), v0 = __ldg(p2 + lane);
+            const uint32_t w1 = lane < 2 ? __ldg(p + 32 + lane) : 0u;
+            const uint32_t v1 = lane < 2 ? __ldg(p2 + 32 + lane) : 0u;
             uint32_t ca, cb2;
             float da, db;
             unit(w0, w1, ca, da);
