@@ -25,15 +25,20 @@ log = logging.getLogger("quantized_decode_matvec_gb300.graph")
 class StepGraph:
     """Captured mq_step over a StepBuffers, with eager fallback.
 
-    ``capture_hook`` (test-only) runs inside the capture window, so a test can
-    plant a capture-illegal host operation and check the fallback.
+    ``io`` (optional): a pair of pinned host tensors shaped like
+    ``bufs.inputs`` and ``bufs.outputs``; the step then copies the inputs in
+    and the outputs out as part of the same graph (one launch per step from
+    host buffers to host buffers).  ``capture_hook`` (test-only) runs inside
+    the capture window, so a test can plant a capture-illegal host operation
+    and check the fallback.
     """
 
     def __init__(self, bufs: "mq.StepBuffers", flags: int = 0, use_graph: bool = True,
                  capture_hook: Optional[Callable[[], None]] = None, warmup: int = 1,
-                 stream: Optional[torch.cuda.Stream] = None):
+                 stream: Optional[torch.cuda.Stream] = None, io: Optional[tuple] = None):
         self.bufs = bufs
         self.flags = flags
+        self.io = io
         self.stream = stream if stream is not None else torch.cuda.Stream(device=bufs.device)
         self.graph: Optional[torch.cuda.CUDAGraph] = None
         self.captured = False
@@ -53,7 +58,7 @@ class StepGraph:
             with torch.cuda.graph(g, stream=self.stream):
                 if hook is not None:
                     hook()
-                self.bufs.step(self.stream, self.flags)
+                self._step()
         except Exception as e:  # capture failure: fall back to eager, keep running
             self.capture_error = f"{type(e).__name__}: {e}"
             log.warning("mq_step capture failed, running eagerly: %s", self.capture_error)
@@ -76,7 +81,15 @@ class StepGraph:
             if self.captured:
                 self.graph.replay()
             else:
-                self.bufs.step(self.stream, self.flags)
+                self._step()
+
+    def _step(self) -> None:
+        # on self.stream (current): inputs in, the step, outputs out
+        if self.io is not None:
+            self.bufs.inputs.copy_(self.io[0], non_blocking=True)
+        self.bufs.step(self.stream, self.flags)
+        if self.io is not None:
+            self.io[1].copy_(self.bufs.outputs, non_blocking=True)
 
     def node_count(self) -> Optional[int]:
         """Kernel nodes in the captured graph (None if not captured or not queryable)."""
@@ -103,13 +116,16 @@ class PinnedFeeder:
 
     def __init__(self, bufs: "mq.StepBuffers"):
         self.bufs = bufs
-        self.a = torch.empty(bufs.a.shape, dtype=torch.float32, pin_memory=True)
-        self.b = torch.empty(bufs.b.shape, dtype=torch.float32, pin_memory=True)
-        self.c = torch.empty(bufs.c.shape, dtype=torch.float32, pin_memory=True)
+        # one pinned buffer laid out like the device inputs (a, b, c views)
+        self.inputs = torch.empty(bufs.inputs.shape, dtype=torch.float32, pin_memory=True)
+        na, nb = bufs.a.numel(), bufs.b.numel()
+        self.a = self.inputs[:na].view(bufs.a.shape)
+        self.b = self.inputs[na:na + nb].view(bufs.b.shape)
+        self.c = self.inputs[na + nb:].view(bufs.c.shape)
 
     @property
     def h2d_bytes(self) -> int:
-        return (self.a.numel() + self.b.numel() + self.c.numel()) * 4
+        return self.inputs.numel() * 4
 
     def load(self, a, b, c) -> None:
         self.a.copy_(torch.as_tensor(a).reshape(self.a.shape))
@@ -118,6 +134,4 @@ class PinnedFeeder:
 
     def push(self, stream) -> None:
         with torch.cuda.stream(stream):
-            self.bufs.a.copy_(self.a, non_blocking=True)
-            self.bufs.b.copy_(self.b, non_blocking=True)
-            self.bufs.c.copy_(self.c, non_blocking=True)
+            self.bufs.inputs.copy_(self.inputs, non_blocking=True)  # one host-to-device copy

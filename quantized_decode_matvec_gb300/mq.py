@@ -423,14 +423,20 @@ class StepBuffers:
         self.device = dev
         n = self.n_layers
         self.weights = weights
-        # inputs [layer, ncols, K]
-        self.a = torch.zeros((n, ncols, H), dtype=torch.float32, device=dev)
-        self.b = torch.zeros((n, ncols, o_K), dtype=torch.float32, device=dev)
-        self.c = torch.zeros((n, ncols, H), dtype=torch.float32, device=dev)
-        # outputs
-        self.y_qkv = torch.zeros((n, ncols, qkv_rows), dtype=torch.float32, device=dev)
-        self.y_o = torch.zeros((n, ncols, o_rows), dtype=torch.float32, device=dev)
-        self.y_ffn = torch.zeros((n, ncols, H), dtype=torch.float32, device=dev)
+        # inputs [layer, ncols, K]: views of one buffer, so that a step's inputs
+        # arrive in one host-to-device copy (each view starts on a 16-byte
+        # boundary: H and o_K are multiples of 256)
+        na, nb = n * ncols * H, n * ncols * o_K
+        self.inputs = torch.zeros(na + nb + na, dtype=torch.float32, device=dev)
+        self.a = self.inputs[:na].view(n, ncols, H)
+        self.b = self.inputs[na:na + nb].view(n, ncols, o_K)
+        self.c = self.inputs[na + nb:].view(n, ncols, H)
+        # outputs: views of one buffer too (one device-to-host copy)
+        nq, no = n * ncols * qkv_rows, n * ncols * o_rows
+        self.outputs = torch.zeros(nq + no + n * ncols * H, dtype=torch.float32, device=dev)
+        self.y_qkv = self.outputs[:nq].view(n, ncols, qkv_rows)
+        self.y_o = self.outputs[nq:nq + no].view(n, ncols, o_rows)
+        self.y_ffn = self.outputs[nq + no:].view(n, ncols, H)
         self.h_q8 = torch.zeros((n, ncols, I // 32 * 34), dtype=torch.uint8, device=dev)
         self.debug = debug
         if debug:

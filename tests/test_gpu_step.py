@@ -267,3 +267,29 @@ def test_step_7b_full_size_sampled(cuda_ready):
     assert mq.mq_read_device_status(0) == 0
     del wdev, bufs, g
     torch.cuda.empty_cache()
+
+
+def test_step_graph_with_host_io(cuda_ready):
+    # the input copy, the persistent step and the output copy captured as one
+    # graph: each replay reads the pinned inputs as they are at replay time and
+    # leaves the outputs in pinned host memory, byte-identical to an eager step
+    import torch
+    from quantized_decode_matvec_gb300.graph import PinnedFeeder, StepGraph
+    mq = cuda_ready
+    wdev, host = _weights(SMALL)
+    eager = _bufs(mq, SMALL, wdev)
+    graphed = _bufs(mq, SMALL, wdev)
+    feeder = PinnedFeeder(graphed)
+    host_out = torch.empty(graphed.outputs.shape, dtype=torch.float32, pin_memory=True)
+    g = StepGraph(graphed, flags=mq.MQ_STEP_PERSISTENT, io=(feeder.inputs, host_out))
+    assert g.captured, g.capture_error
+    for r in range(3):
+        a, b, c = _inputs(SMALL, 40 + r)
+        feeder.load(a, b, c)
+        g.run()
+        g.stream.synchronize()
+        _set_inputs(eager, a, b, c)
+        eager.step(flags=mq.MQ_STEP_PERSISTENT)
+        torch.cuda.synchronize()
+        assert np.array_equal(host_out.numpy().view(np.uint8), eager.outputs.cpu().numpy().view(np.uint8)), r
+    assert mq.mq_read_device_status(0) == 0
