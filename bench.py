@@ -179,14 +179,17 @@ def recorded_traffic(profile_name: str):
     return None
 
 
-def build_step(case, device, mq):
-    """Upload the step's weights (q|k|v concatenated on the device with mq_concat_rows)."""
+def build_step(case, device, mq, host=None):
+    """Upload the step's weights (q|k|v concatenated on the device with mq_concat_rows).
+    With a list `host`, also keep each layer's host bytes there (for the oracle's baseline)."""
     import torch
     from quantized_decode_matvec_gb300 import synth
     stream = torch.cuda.current_stream().cuda_stream
     layers = []
     for l in range(case.n_layers):
         w = synth.step_layer_weights(case, l)
+        if host is not None:
+            host.append({"q": w["q"], "k": w["k"], "v": w["v"], "o": w["o"], "gu": w["gu"], "down": w["down"]})
         q, k, v = (torch.from_numpy(w[n]).to(device) for n in ("q", "k", "v"))
         qkv = torch.empty((case.qkv_rows, q.shape[1]), dtype=torch.uint8, device=device)
         st = mq.mq_concat_rows(qkv.data_ptr(), [q.data_ptr(), k.data_ptr(), v.data_ptr()],
@@ -229,70 +232,154 @@ def sem(v):
 # CPU oracle baseline (test infrastructure, timed as it stands)
 # ---------------------------------------------------------------------------------------------------------
 
-def oracle_step_layers(case, layers, replay=0, budget_s=None, layer_ids=None):
-    """Run the oracle over layers of the step; returns (weight bytes processed, seconds, layers done)."""
-    import oracle
-    from quantized_decode_matvec_gb300 import synth
-    done, nbytes, spent = 0, 0, 0.0
-    ids = layer_ids if layer_ids is not None else range(case.n_layers)
-    for l in ids:
-        w = layers(l)
-        inp = synth.step_layer_inputs(case, l, replay)
+def host_cores() -> int:
+    """Host threads this process may run on (its CPU affinity)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+class OracleArm:
+    """The CPU oracle as it stands, on `threads` host threads.
+
+    One thread calls the oracle's own functions (``oracle.ffn`` is its whole
+    FFN chain in C).  More threads split every matvec into a static partition
+    of its rows, one contiguous slice per thread (ctypes releases the GIL for
+    the duration of each C call), and keep the FFN chain's stage order: all of
+    g|u, then SiLU*mul and the q8_0 of h, then down.  Each output row is the
+    oracle's own per-row computation, so both give the same bytes.
+    """
+
+    def __init__(self, threads: int = 1):
+        self.threads = max(1, int(threads))
+        self.pool = None
+        if self.threads > 1:
+            from concurrent.futures import ThreadPoolExecutor
+            self.pool = ThreadPoolExecutor(self.threads)
+
+    def close(self):
+        if self.pool is not None:
+            self.pool.shutdown()
+            self.pool = None
+
+    def _rows(self, fn, rows):
+        bounds = np.linspace(0, rows, self.threads + 1).astype(np.int64)
+        parts = [np.arange(bounds[i], bounds[i + 1], dtype=np.int64) for i in range(self.threads)
+                 if bounds[i + 1] > bounds[i]]
+        return np.concatenate(list(self.pool.map(fn, parts)), axis=1)
+
+    def matvec(self, W, xq, rows, K):
+        import oracle
+        if self.pool is None:
+            return oracle.matvec(W, xq, rows, K)[0]
+        return self._rows(lambda ids: oracle.matvec(W, xq, rows, K, row_ids=ids)[0], rows)
+
+    def matvec_w(self, wtype, W, xq, rows, K):
+        import oracle
+        if self.pool is None:
+            return oracle.matvec_w(wtype, W, xq, rows, K)[0]
+        return self._rows(lambda ids: oracle.matvec_w(wtype, W, xq, rows, K, row_ids=ids)[0], rows)
+
+    def ffn(self, W_gu, W_down, x, H, I):
+        import oracle
+        if self.pool is None:
+            return oracle.ffn(W_gu, W_down, x, H, I)[0]
+        xq = oracle.quantize_q8_0(np.asarray(x, np.float32).reshape(-1, H))
+        gu = self.matvec(W_gu, xq, 2 * I, H)
+        h = oracle.silu_mul(gu[:, :I], gu[:, I:])
+        hq = oracle.quantize_q8_0(h.astype(np.float32))
+        return self.matvec(W_down, hq, H, I)
+
+    def step_layer(self, case, w, inp):
+        """One layer of the decode step: q|k|v, o, then the FFN, in order."""
+        import oracle
+        qkv = w["qkv"] if "qkv" in w else np.concatenate([w["q"], w["k"], w["v"]])
+        self.matvec(qkv, oracle.quantize_q8_0(inp["a"]), case.qkv_rows, case.H)
+        self.matvec(w["o"], oracle.quantize_q8_0(inp["b"]), case.H, case.q_rows)
+        self.ffn(w["gu"], w["down"], inp["c"], case.H, case.I)
+
+    def step(self, case, weights, inputs):
+        """One whole step (every layer); returns seconds."""
         t0 = time.perf_counter()
-        qkv = np.concatenate([w["q"], w["k"], w["v"]])
-        oracle.matvec(qkv, oracle.quantize_q8_0(inp["a"]), case.qkv_rows, case.H)
-        oracle.matvec(w["o"], oracle.quantize_q8_0(inp["b"]), case.H, case.q_rows)
-        oracle.ffn(w["gu"], w["down"], inp["c"], case.H, case.I)
-        spent += time.perf_counter() - t0
-        nbytes += sum(w[n].nbytes for n in ("q", "k", "v", "o", "gu", "down"))
-        done += 1
-        if budget_s is not None and spent >= budget_s:
-            break
-    return nbytes, spent, done
+        for l in range(case.n_layers):
+            self.step_layer(case, weights[l], inputs[l])
+        return time.perf_counter() - t0
 
 
-def cpu_baseline(case, budget_s=12.0):
+def oracle_time(fn, reps=3):
+    """Median seconds of `reps` calls of fn()."""
+    t = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        fn()
+        t.append(time.perf_counter() - t0)
+    return statistics.median(t)
+
+
+def host_step_weights(case):
+    """Host copies of every layer's weights (q|k|v concatenated), as the GPU arm uploads them."""
     from quantized_decode_matvec_gb300 import synth
-    cache = {}
+    out = []
+    for l in range(case.n_layers):
+        w = synth.step_layer_weights(case, l)
+        out.append({"qkv": np.concatenate([w["q"], w["k"], w["v"]]), "o": w["o"], "gu": w["gu"],
+                    "down": w["down"]})
+    return out
 
-    def layers(l):
-        if l not in cache:
-            cache.clear()
-            cache[l] = synth.step_layer_weights(case, l)
-        return cache[l]
 
-    nbytes, spent, done = oracle_step_layers(case, layers, budget_s=budget_s)
-    return {"value": nbytes / spent / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{done} of {case.n_layers} layers of one step (q|k|v, o, ffn_gu+SiLU*mul+q8_0, down), "
-                      f"single-threaded C oracle, fp64 accumulation, {spent:.1f} s"}
+def cpu_baseline(case, weights):
+    """The oracle on the host cores over one whole step of the workload: one thread, and all the
+    threads of this process's CPU affinity (static row partition).  The all-threads arm is the
+    headline (value, cores); the one-thread arm rides along."""
+    from quantized_decode_matvec_gb300 import synth
+    inputs = [synth.step_layer_inputs(case, l, 0) for l in range(case.n_layers)]
+    wbytes = synth.weight_bytes_step(case)
+    n = host_cores()
+    arm1 = OracleArm(1)
+    s1 = arm1.step(case, weights, inputs)
+    armn = OracleArm(n)
+    sn = armn.step(case, weights, inputs)
+    armn.close()
+    return {"value": wbytes / sn / 1e9, "unit": UNIT, "cores": n, "kind": "oracle",
+            "seconds": sn,
+            "sample": f"one whole step ({case.n_layers} of {case.n_layers} layers: q|k|v, o, ffn_gu+SiLU*mul+q8_0, "
+                      f"down), C oracle with fp64 accumulation, rows split statically over {n} threads "
+                      f"(the process's CPU affinity), {sn:.2f} s",
+            "single_thread": {"value": wbytes / s1 / 1e9, "unit": UNIT, "cores": 1, "seconds": s1,
+                              "sample": "the same whole step on one thread"}}
 
 
 def run_reference(args):
-    """The reference arm: the CPU oracle as it stands, each step a bounded sample of the workload."""
+    """The reference arm: the CPU oracle as it stands on the host cores (all threads of the
+    process's affinity, static row partition), each step one whole step of the workload."""
     from quantized_decode_matvec_gb300 import synth
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
     case = synth.STEP_7B
-    n_cached = 2
-    cache = {l: synth.step_layer_weights(case, l) for l in range(n_cached)}
-    layers = lambda l: cache[l % n_cached]
+    weights = host_step_weights(case)
+    n = host_cores()
+    arm = OracleArm(n)
     for i in range(args.warmup):
-        oracle_step_layers(case, layers, layer_ids=[i % n_cached])
-    times, nbytes = [], 0
+        arm.step(case, weights, [synth.step_layer_inputs(case, l, i) for l in range(case.n_layers)])
+    times = []
     for i in range(args.steps):
-        b, s, _ = oracle_step_layers(case, layers, layer_ids=[i % n_cached])
-        times.append(s)
-        nbytes += b
+        inputs = [synth.step_layer_inputs(case, l, args.warmup + i) for l in range(case.n_layers)]
+        times.append(arm.step(case, weights, inputs))
+    arm.close()
+    wbytes = synth.weight_bytes_step(case)
     total = sum(times)
-    value = nbytes / total / 1e9
+    value = wbytes * args.steps / total / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": case.name, "sample_per_step": "one layer of the 28 (q|k|v, o, FFN chain)"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle", "cores": 1,
-                         "sample": "one of 28 layers per step, single-threaded C oracle"},
+        "config": {"workload": f"{case.name}: {case.n_layers} layers x (q|k|v 4608x3584, o 3584x3584, ffn_gu "
+                               f"37888x3584 + SiLU*mul + q8_0(h), down 3584x18944), batch 1",
+                   "sample_per_step": "one whole step (every layer)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle", "cores": n,
+                         "sample": f"one whole step per timed step, C oracle, rows split over {n} threads"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -303,19 +390,35 @@ def run_reference(args):
 # the GPU arm
 # ---------------------------------------------------------------------------------------------------------
 
-def config_suite(mq, device):
+def config_suite(mq, device, oracle_arms=True):
     """The other workloads of the matvec, each timed on its own (context for the step's number).
 
     Every call is captured in a CUDA graph and replayed; times are CUDA events around whole
     replays (per-call = replay / calls).  Workloads smaller than twice the L2 are timed on
     rotated device copies of the same weights, so each call streams its weights from HBM;
     the single matvec is also reported warm (its 295 KB stay in L2).
+
+    With oracle_arms, each entry also carries the CPU oracle's time for the same call on the
+    same host bytes (median of up to 3 runs): on one thread and on all the threads of the
+    process's affinity (static row partition); the 0.5B FFN as all 24 layers in order.
     """
     import torch
+    import oracle
     from quantized_decode_matvec_gb300 import synth
     l2 = 2 * 129 * 1024 * 1024
     out = {}
     stream = torch.cuda.Stream(device)
+    arms = [OracleArm(1), OracleArm(host_cores())] if oracle_arms else []
+
+    def ora(name, fn, reps=3, per=1):
+        """oracle seconds of fn(arm) on each arm, as µs per call (`per` calls per fn)"""
+        if not arms:
+            return
+        t1 = oracle_time(lambda: fn(arms[0]), reps)
+        tn = oracle_time(lambda: fn(arms[1]), reps)
+        out[name].update(oracle_us_1_thread=round(t1 * 1e6 / per, 1),
+                         oracle_us_all_threads=round(tn * 1e6 / per, 1), oracle_threads=arms[1].threads,
+                         gpu_over_oracle_all_threads=round(tn * 1e6 / per / out[name]["us_per_call"], 1))
 
     def timed(calls, reps=10):
         """median per-call ms of a graph holding `calls` (a list of zero-arg launches)."""
@@ -380,27 +483,36 @@ def config_suite(mq, device):
     calls, keep = mv_calls(copies, c.rows, c.K, x, y)
     rec("matvec_512x1024_hbm", timed(calls, 5), W.numel(), copies=ncopy)
     del copies, keep
+    ora("matvec_512x1024_hbm", lambda a: a.matvec(W_np, oracle.quantize_q8_0(x_np), c.rows, c.K))
 
     # 0.5B-class FFN, 24 layers (202 MB: larger than L2 as it is)
     f = synth.FFN_05B
-    pairs = [tuple(torch.from_numpy(w).to(device) for w in synth.ffn_layer_weights(f, l)) for l in range(f.n_layers)]
-    x = torch.from_numpy(synth.ffn_layer_input(f, 0)).to(device)
+    host = [synth.ffn_layer_weights(f, l) for l in range(f.n_layers)]
+    pairs = [tuple(torch.from_numpy(w).to(device) for w in hw) for hw in host]
+    x_np = synth.ffn_layer_input(f, 0)
+    x = torch.from_numpy(x_np).to(device)
     calls, keep = ffn_calls(pairs, f.H, f.I, x)
     ms = timed(calls)
     wb = sum(a.numel() + b.numel() for a, b in pairs)
     rec("ffn_0.5B_x24_per_layer", ms, wb // f.n_layers, total_us_24_layers=round(ms * 1e3 * f.n_layers, 2))
     del pairs, keep
+    ora("ffn_0.5B_x24_per_layer", lambda a: [a.ffn(gu, dn, x_np, f.H, f.I) for gu, dn in host], reps=1,
+        per=f.n_layers)
+    del host
 
     # 7B FFN (115 MB: rotated over 5 copies), batch 1 and 2/4/8 columns
     f = synth.FFN_7B
-    gu, dn = (torch.from_numpy(w).to(device) for w in synth.ffn_layer_weights(f, 0))
+    gu_np, dn_np = synth.ffn_layer_weights(f, 0)
+    gu, dn = torch.from_numpy(gu_np).to(device), torch.from_numpy(dn_np).to(device)
     pairs = [(gu, dn)] + [(gu.clone(), dn.clone()) for _ in range(4)]
     wb = gu.numel() + dn.numel()
     for nc in (1,) + tuple(synth.FFN_7B_NCOLS):
-        x = torch.from_numpy(synth.ffn_layer_input(f, 0, nc)).to(device)
+        x_np = synth.ffn_layer_input(f, 0, nc)
+        x = torch.from_numpy(x_np).to(device)
         calls, keep = ffn_calls(pairs, f.H, f.I, x)
         rec(f"ffn_7B_ncols{nc}", timed(calls), wb, copies=len(pairs))
-    del pairs, gu, dn, keep
+        ora(f"ffn_7B_ncols{nc}", lambda a: a.ffn(gu_np, dn_np, x_np, f.H, f.I), reps=1)
+    del pairs, gu, dn, keep, gu_np, dn_np
 
     # K sweep, 4096 rows (rotated copies to exceed twice the L2)
     for K in synth.KSWEEP_KS:
@@ -413,12 +525,15 @@ def config_suite(mq, device):
         calls, keep = mv_calls(copies, synth.KSWEEP_ROWS, K, x, y)
         rec(f"ksweep_4096x{K}", timed(calls, 5), W.numel(), copies=ncopy)
         del copies, keep
+        ora(f"ksweep_4096x{K}", lambda a: a.matvec(W_np, oracle.quantize_q8_0(x_np), synth.KSWEEP_ROWS, K))
     # the other weight types (q4_0: the pages' 0.5B model; q8_0), 4096 x 14336, rotated copies
     K = 14336
-    x = torch.from_numpy(synth.activation(K, 1, seed=synth.KSWEEP_SEED)).to(device)
+    x_np = synth.activation(K, 1, seed=synth.KSWEEP_SEED)
+    x = torch.from_numpy(x_np).to(device)
     y = torch.empty((1, synth.KSWEEP_ROWS), dtype=torch.float32, device=device)
     for wt in ("q4_0", "q8_0"):
-        W = torch.from_numpy(synth.wq_matrix(wt, synth.KSWEEP_ROWS, K, seed=synth.KSWEEP_SEED)).to(device)
+        W_np = synth.wq_matrix(wt, synth.KSWEEP_ROWS, K, seed=synth.KSWEEP_SEED)
+        W = torch.from_numpy(W_np).to(device)
         ncopy = l2 // W.numel() + 1
         copies = [W] + [W.clone() for _ in range(ncopy - 1)]
         fn = mq.mq_matvec_q4_0_q8_0 if wt == "q4_0" else mq.mq_matvec_q8_0_q8_0
@@ -429,7 +544,11 @@ def config_suite(mq, device):
                                         torch.cuda.current_stream().cuda_stream), "matvec")
         rec(f"{wt}_weights_4096x{K}", timed([mk(d) for d in descs], 5), W.numel(), copies=ncopy)
         del copies, descs
+        ora(f"{wt}_weights_4096x{K}",
+            lambda a: a.matvec_w(wt, W_np, oracle.quantize_q8_0(x_np), synth.KSWEEP_ROWS, K))
     torch.cuda.synchronize()
+    for a in arms:
+        a.close()
     return out
 
 
@@ -454,7 +573,9 @@ def run_ours(args):
     wbytes = synth.weight_bytes_step(case)
     per_layer = wbytes // case.n_layers
 
-    layers = build_step(case, device, mq)
+    want_cpu = rank == 0 and ws == 1 and not args.no_cpu_baseline
+    host_weights = [] if want_cpu else None
+    layers = build_step(case, device, mq, host=host_weights)
     bufs = mq.StepBuffers(layers, case.H, case.I, case.qkv_rows, case.H, case.q_rows, case.ncols)
     fill_inputs(bufs, case, 0)
     mode_flags = {"persistent": mq.MQ_STEP_PERSISTENT, "graph": 0, "pdl": mq.MQ_STEP_PDL}
@@ -564,8 +685,10 @@ def run_ours(args):
     assert mq.mq_read_device_status(0) == 0
     launches_per_step = 1 if args.mode == "persistent" else 4 * case.n_layers
 
-    cpu = cpu_baseline(case) if (rank == 0 and ws == 1 and not args.no_cpu_baseline) else None
-    suite = config_suite(mq, device) if (rank == 0 and not args.no_configs and args.layers == 28) else None
+    cpu = cpu_baseline(case, host_weights) if want_cpu else None
+    host_weights = None
+    suite = (config_suite(mq, device, oracle_arms=not args.no_cpu_baseline)
+             if (rank == 0 and not args.no_configs and args.layers == 28) else None)
 
     if rank == 0:
         line = {

@@ -278,9 +278,9 @@ mq_status mq_step_workspace_bytes(const mq_step_shape* h_shape, size_t* bytes);
  * Limit: ncols * (I/32) * 34 bytes of h_q8 must not exceed
  * MQ_NOALLOC_HQ8_MAX_BYTES; larger calls return MQ_ERR_UNSUPPORTED before
  * any device work (use mq_ffn_gu_silu_down with caller scratch for them).
- * Setup: the first call on each device looks up that device's copy of the
- * array (the device must be current); make that first call before any stream
- * capture.  Needs mq_init for the device.
+ * Setup: mq_init looks up that device's copy of the array once and caches
+ * its address; the call itself only reads the cached address.  Needs mq_init
+ * for the device.
  * Races: every call on one device uses the same array, so two calls that
  * overlap on the GPU (two streams, two host threads, or a call in flight
  * while another runs) race on it and give wrong results; order them on one

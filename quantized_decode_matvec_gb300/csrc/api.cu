@@ -404,6 +404,7 @@ mq_status mq_init(int device)
         if ((e = cudaGetSymbolAddress(&p, g_status_word)) != cudaSuccess) break;
         info.status = static_cast<unsigned*>(p);
         if ((e = cudaMemset(info.status, 0, sizeof(unsigned))) != cudaSuccess) break;
+        if ((e = mq::noalloc_setup(device)) != cudaSuccess) break;
         if ((e = cudaDeviceSynchronize()) != cudaSuccess) break;
         info.ready = true;
     } while (0);

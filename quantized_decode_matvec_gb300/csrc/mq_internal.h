@@ -106,6 +106,9 @@ cudaError_t launch_block_sums(const mq_mv_desc* d, int rows, int K, int ncols, i
                               int smem, unsigned* status, cudaStream_t s);
 // raises the dynamic shared memory limit of every kernel on the current device
 cudaError_t set_kernel_attributes(int max_smem);
+// looks up the device address of the no-alloc FFN's fixed scratch on device
+// `dev` (current) and caches it
+cudaError_t noalloc_setup(int dev);
 
 }  // namespace mq
 

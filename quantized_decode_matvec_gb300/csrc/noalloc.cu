@@ -21,26 +21,34 @@ constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
 std::atomic<unsigned char*> g_scratch_addr[kMaxDevices];  // null until that device's first call
 
-// device address of this device's g_noalloc_scratch, looked up on the first
-// call with the device current
+// Looks up the device address of the current device's g_noalloc_scratch once
+// (the device must be current) and caches it; mq_init does this for its device.
+cudaError_t lookup_scratch(int dev, unsigned char** out)
+{
+    unsigned char* ptr = g_scratch_addr[dev].load(std::memory_order_acquire);
+    if (!ptr) {
+        std::lock_guard<std::mutex> lock(g_setup_mutex);
+        ptr = g_scratch_addr[dev].load(std::memory_order_relaxed);
+        if (!ptr) {
+            const cudaError_t e = cudaGetSymbolAddress((void**)&ptr, g_noalloc_scratch);
+            if (e != cudaSuccess) return e;
+            g_scratch_addr[dev].store(ptr, std::memory_order_release);
+        }
+    }
+    *out = ptr;
+    return cudaSuccess;
+}
+
+// device address of this device's g_noalloc_scratch (cached by mq_init; looked
+// up here if mq_init ran before this file's array was registered)
 mq_status scratch_for_current_device(unsigned char** out)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return mq::record_cuda_error(e);
     if (dev < 0 || dev >= kMaxDevices) return MQ_ERR_NOT_INITIALIZED;
-    unsigned char* ptr = g_scratch_addr[dev].load(std::memory_order_acquire);
-    if (!ptr) {
-        std::lock_guard<std::mutex> lock(g_setup_mutex);
-        ptr = g_scratch_addr[dev].load(std::memory_order_relaxed);
-        if (!ptr) {
-            e = cudaGetSymbolAddress((void**)&ptr, g_noalloc_scratch);
-            if (e != cudaSuccess) return mq::record_cuda_error(e);
-            g_scratch_addr[dev].store(ptr, std::memory_order_release);
-        }
-    }
-    *out = ptr;
-    return MQ_OK;
+    e = lookup_scratch(dev, out);
+    return e == cudaSuccess ? MQ_OK : mq::record_cuda_error(e);
 }
 
 __global__ void write_ffn_desc_kernel(mq_ffn_desc* dst, mq_ffn_desc src)
@@ -49,6 +57,16 @@ __global__ void write_ffn_desc_kernel(mq_ffn_desc* dst, mq_ffn_desc src)
 }
 
 }  // namespace
+
+namespace mq {
+// called by mq_init with `dev` current
+cudaError_t noalloc_setup(int dev)
+{
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    unsigned char* p = nullptr;
+    return lookup_scratch(dev, &p);
+}
+}  // namespace mq
 
 extern "C" mq_status mq_ffn_gu_silu_down_noalloc(const void* W_gu, const void* W_down, const float* x,
                                                  const void* xq, float* y, int32_t H, int32_t I, int32_t ncols,

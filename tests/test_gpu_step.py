@@ -17,14 +17,32 @@ pytestmark = pytest.mark.gpu
 SMALL = synth.StepCase("step_small", n_layers=3, H=512, I=1024, q_rows=512, kv_rows=128, ncols=1, seed=5)
 
 
-def _weights(case, device="cuda"):
+def _weights(case, device="cuda", concat_on_device=False):
+    """Per-layer weights on the device and on the host.  With concat_on_device the
+    q|k|v matrix is built on the GPU by mq_concat_rows (as the benchmark builds it)
+    and checked byte for byte against the host concatenation."""
     import torch
+    from quantized_decode_matvec_gb300 import mq
     out, host = [], []
     for l in range(case.n_layers):
         w = synth.step_layer_weights(case, l)
         qkv = np.concatenate([w["q"], w["k"], w["v"]])          # row concatenation q|k|v
         host.append({"qkv": qkv, "o": w["o"], "gu": w["gu"], "down": w["down"]})
-        out.append({k: torch.from_numpy(v).to(device) for k, v in host[-1].items()})
+        dev = {k: torch.from_numpy(v).to(device) for k, v in host[-1].items() if k != "qkv"}
+        if concat_on_device:
+            parts = [torch.from_numpy(w[n]).to(device) for n in ("q", "k", "v")]
+            qkv_d = torch.empty(qkv.shape, dtype=torch.uint8, device=device)
+            st = mq.mq_concat_rows(qkv_d.data_ptr(), [t.data_ptr() for t in parts],
+                                   [case.q_rows, case.kv_rows, case.kv_rows], mq.MQ_TYPE_Q4_K, case.H,
+                                   torch.cuda.current_stream().cuda_stream)
+            assert st == mq.MQ_OK
+            torch.cuda.synchronize()
+            assert np.array_equal(qkv_d.cpu().numpy(), qkv), f"mq_concat_rows q|k|v, layer {l}"
+            dev["qkv"] = qkv_d
+            del parts
+        else:
+            dev["qkv"] = torch.from_numpy(qkv).to(device)
+        out.append(dev)
     return out, host
 
 
@@ -190,9 +208,19 @@ def test_step_pdl_matches_plain(cuda_ready, variant):
         assert np.array_equal(x[k].view(np.uint8), y[k].view(np.uint8)), k
 
 
-@pytest.mark.parametrize("case", [SMALL, synth.StepCase("step_tiny", 2, 256, 256, 256, 256, 1, 6),
-                                  synth.StepCase("step_ncols3", 2, 512, 768, 512, 128, 3, 7)],
-                         ids=["small", "tiny", "ncols3"])
+# every column count's consumer form in the persistent kernel: 1-2 columns keep
+# the activation in registers (2 columns: the two-column register path), 3-4
+# read it from shared memory per row pair, 5-8 run on column lanes
+PERSISTENT_CASES = [SMALL, synth.StepCase("step_tiny", 2, 256, 256, 256, 256, 1, 6),
+                    synth.StepCase("step_ncols2", 2, 1024, 1536, 1024, 256, 2, 10),
+                    synth.StepCase("step_ncols3", 2, 512, 768, 512, 128, 3, 7),
+                    synth.StepCase("step_ncols4", 2, 512, 1024, 512, 128, 4, 11),
+                    synth.StepCase("step_ncols5", 2, 512, 768, 512, 128, 5, 12),
+                    synth.StepCase("step_ncols8", 2, 768, 1024, 768, 128, 8, 13),
+                    synth.StepCase("step_ncols2_long", 1, 3584, 4864, 3584, 512, 2, 14)]
+
+
+@pytest.mark.parametrize("case", PERSISTENT_CASES, ids=[c.name for c in PERSISTENT_CASES])
 def test_persistent_step_bit_identical_to_multikernel(cuda_ready, case):
     mq = cuda_ready
     wdev, host = _weights(case)
@@ -237,17 +265,22 @@ def test_persistent_step_graph_replays(cuda_ready):
 
 @pytest.mark.slow
 def test_step_7b_full_size_sampled(cuda_ready):
-    # the 28-layer 7B-class step at full size, as the benchmark runs it (graph replay),
-    # every layer checked on sampled rows (FFN teacher-forced on the kernel's h_q8)
+    # The 28-layer 7B-class step at full size exactly as the benchmark runs it:
+    # q|k|v built on the device by mq_concat_rows, the persistent kernel captured
+    # as one CUDA graph and replayed.  Every layer of every replay is checked
+    # against the oracle on sampled rows (the FFN teacher-forced on the kernel's
+    # h_q8), and the PDL multi-kernel graph gives the same bytes.
     import torch
     from quantized_decode_matvec_gb300.graph import StepGraph
     mq = cuda_ready
     case = synth.STEP_7B
-    wdev, host = _weights(case)
+    wdev, host = _weights(case, concat_on_device=True)
     bufs = _bufs(mq, case, wdev)
     multi = _bufs(mq, case, wdev)
-    g = StepGraph(bufs, flags=mq.MQ_STEP_PDL)   # the configuration the benchmark times by default
+    g = StepGraph(bufs, flags=mq.MQ_STEP_PERSISTENT)   # the benchmark's default launch mode
     assert g.captured, g.capture_error
+    gp = StepGraph(multi, flags=mq.MQ_STEP_PDL)
+    assert gp.captured, gp.capture_error
     rng = np.random.default_rng(0)
     rows = rng.choice(1 << 20, 48, replace=False)
     for r in (0, 1, 2):
@@ -255,17 +288,15 @@ def test_step_7b_full_size_sampled(cuda_ready):
         _set_inputs(bufs, a, b, c)
         g.run()
         outs = _outputs(bufs)
-        layers = range(case.n_layers) if r == 0 else (0, case.n_layers - 1)
-        for l in layers:
+        for l in range(case.n_layers):
             _check_layer_oracle(case, host, outs, a, b, c, l, rows=rows)
-        if r == 2:  # the persistent kernel gives the same bytes at full size
-            _set_inputs(multi, a, b, c)
-            multi.step(flags=mq.MQ_STEP_PERSISTENT)
-            m = _outputs(multi)
-            for k in outs:
-                assert np.array_equal(outs[k].view(np.uint8), m[k].view(np.uint8)), k
+        _set_inputs(multi, a, b, c)
+        gp.run()
+        m = _outputs(multi)
+        for k in outs:
+            assert np.array_equal(outs[k].view(np.uint8), m[k].view(np.uint8)), (r, k)
     assert mq.mq_read_device_status(0) == 0
-    del wdev, bufs, g
+    del wdev, bufs, multi, g, gp
     torch.cuda.empty_cache()
 
 

@@ -69,6 +69,7 @@ def test_noalloc_strided_output_and_stream(cuda_ready):
     torch.cuda.synchronize()
     y = torch.full((ncols, y_ld), -7.0, dtype=torch.float32, device="cuda")
     s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())  # the fill above runs on the current stream
     with torch.cuda.stream(s):
         mq.ffn_gu_silu_down_noalloc(W_gu, W_down, H, I, x=x, y=y, stream=s)
     s.synchronize()
