@@ -59,6 +59,15 @@ def _load():
         lib.mqo_dequant_w_row.argtypes = [ctypes.c_int, u8p, i64, f64p]
         lib.mqo_matvec_w.argtypes = [ctypes.c_int, u8p, u8p, i64, i64, i64, i64p, i64, f64p, f64p]
         lib.mqo_dequant_w_row.restype = None
+        u16p = ctypes.POINTER(ctypes.c_uint16)
+        lib.mqo_f64_to_f16.argtypes = [ctypes.c_double]
+        lib.mqo_f64_to_f16.restype = ctypes.c_uint16
+        lib.mqo_f64_to_f16_array.argtypes = [f64p, i64, u16p]
+        lib.mqo_f64_to_f16_array.restype = None
+        lib.mqo_dequant_q4K_f16_row.argtypes = [u8p, i64, f64p, u16p]
+        lib.mqo_dequant_q4K_f16_row.restype = None
+        lib.mqo_gemm_f16.argtypes = [u16p, u16p, i64, i64p, i64, i64p, i64, f64p, f64p]
+        lib.mqo_gemm_f16.restype = None
         lib.mqo_matvec_w.restype = None
         for name in ("mqo_quantize_q8_0", "mqo_unpack_q4K", "mqo_dequant_q4K_row", "mqo_dequant_q8_0",
                      "mqo_block_sums", "mqo_matvec", "mqo_matvec_rows", "mqo_silu_mul", "mqo_ffn"):
@@ -259,4 +268,53 @@ def matvec_w(wtype: str, W: np.ndarray, xq: np.ndarray, rows: int, K: int,
     _load().mqo_matvec_w(W_BLOCK_BYTES[wtype], _p(W, ctypes.c_uint8), _p(np.ascontiguousarray(xq2), ctypes.c_uint8),
                          rows, K, ncols, None if ids is None else _p(ids, ctypes.c_int64), n,
                          _p(y, ctypes.c_double), _p(T, ctypes.c_double))
+    return y, T
+
+
+# ---- prefill: the f16 weight cache and the half-precision GEMM ---------------------------------------------
+
+def f64_to_f16(x) -> np.ndarray:
+    """binary64 values -> binary16 bit patterns (uint16), round to nearest, ties to even."""
+    a = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(a.shape, np.uint16)
+    _load().mqo_f64_to_f16_array(_p(a.reshape(-1), ctypes.c_double), a.size,
+                                 _p(out.reshape(-1), ctypes.c_uint16))
+    return out
+
+
+def dequant_q4K_f16(W: np.ndarray, K: int) -> np.ndarray:
+    """uint8 q4_K [rows, K/256*144] -> uint16 binary16 patterns [rows, K] (each weight rounded once)."""
+    W = _u8(W).reshape(-1, q4K_row_bytes(K))
+    out = np.empty((W.shape[0], K), np.uint16)
+    scratch = np.empty(K, np.float64)
+    lib = _load()
+    for r in range(W.shape[0]):
+        row = np.ascontiguousarray(W[r])
+        o = out[r]
+        lib.mqo_dequant_q4K_f16_row(_p(row, ctypes.c_uint8), K, _p(scratch, ctypes.c_double),
+                                    _p(o, ctypes.c_uint16))
+    return out
+
+
+def f32_to_f16_array(x) -> np.ndarray:
+    """fp32 values -> binary16 bit patterns (uint16), round to nearest, ties to even."""
+    return f64_to_f16(np.asarray(x, np.float32).astype(np.float64))
+
+
+def gemm_f16(W16: np.ndarray, X16: np.ndarray, K: int, row_ids=None, tok_ids=None) -> Tuple[np.ndarray, np.ndarray]:
+    """Y [len(tok_ids), len(row_ids)] = X16 . W16^T over the chosen tokens and rows, binary64 sums of the
+    exact binary16 products; and T, the sums of the products' magnitudes.  W16 uint16 [R, K], X16 uint16 [T, K]."""
+    W16 = np.ascontiguousarray(W16, dtype=np.uint16).reshape(-1, K)
+    X16 = np.ascontiguousarray(X16, dtype=np.uint16).reshape(-1, K)
+    rows = np.arange(W16.shape[0], dtype=np.int64) if row_ids is None else np.ascontiguousarray(row_ids, np.int64)
+    toks = np.arange(X16.shape[0], dtype=np.int64) if tok_ids is None else np.ascontiguousarray(tok_ids, np.int64)
+    if rows.size and (rows.min() < 0 or rows.max() >= W16.shape[0]):
+        raise IndexError("row id out of range")
+    if toks.size and (toks.min() < 0 or toks.max() >= X16.shape[0]):
+        raise IndexError("token id out of range")
+    y = np.empty((toks.size, rows.size), np.float64)
+    T = np.empty((toks.size, rows.size), np.float64)
+    _load().mqo_gemm_f16(_p(W16, ctypes.c_uint16), _p(X16, ctypes.c_uint16), K, _p(rows, ctypes.c_int64),
+                         rows.size, _p(toks, ctypes.c_int64), toks.size, _p(y, ctypes.c_double),
+                         _p(T, ctypes.c_double))
     return y, T

@@ -68,10 +68,11 @@ static double mqo_round_half_even(double y)
     return (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;
 }
 
-uint16_t mqo_f32_to_f16(float x)
+/* binary64 -> binary16, round to nearest, ties to even */
+uint16_t mqo_f64_to_f16(double x)
 {
     uint16_t sign = signbit(x) ? 0x8000u : 0u;
-    double a = fabs((double)x);
+    double a = fabs(x);
     if (isnan(x)) return (uint16_t)(sign | 0x7E00u);
     /* 65520 is the midpoint between 65504 (largest finite, odd mantissa) and
      * 2^16; ties go to the even neighbour, which overflows to infinity. */
@@ -87,6 +88,15 @@ uint16_t mqo_f32_to_f16(float x)
     double n = mqo_round_half_even(ldexp(a, 10 - e));   /* in [1024, 2048] */
     uint32_t bits = ((uint32_t)(e + 15) << 10) + (uint32_t)(n - 1024.0);
     return (uint16_t)(sign | bits);  /* a carry to 2048 moves into the exponent */
+}
+
+/* binary32 -> binary16: every binary32 value is exact in binary64, so the
+ * same single rounding applies */
+uint16_t mqo_f32_to_f16(float x) { return mqo_f64_to_f16((double)x); }
+
+void mqo_f64_to_f16_array(const double* x, int64_t n, uint16_t* out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = mqo_f64_to_f16(x[i]);
 }
 
 static uint16_t mqo_le16(const uint8_t* p) { return (uint16_t)(p[0] | (p[1] << 8)); }
@@ -375,5 +385,41 @@ void mqo_ffn(const uint8_t* W_gu, const uint8_t* W_down, const float* x, int64_t
         uint8_t* hq = hq_out + c * hqb;
         mqo_quantize_q8_0(hf, I, hq);
         mqo_matvec(W_down, hq, H, I, 1, y + c * H, 0);
+    }
+}
+
+/* ---------------------------------------------------------------------------
+ * Prefill ("07 . R3 -- Small-model per-token overhead", section 1: the 7B
+ * prefill GEMM runs in half precision over a resident f16 copy of the
+ * weights, dequantized once).
+ * ------------------------------------------------------------------------- */
+
+/* the f16 copy of one q4_K row: each weight d*sc*q - dmin*m in binary64
+ * (the plain definition above), rounded once to binary16; scratch holds K doubles */
+void mqo_dequant_q4K_f16_row(const uint8_t* row, int64_t K, double* scratch, uint16_t* out)
+{
+    mqo_dequant_q4K_row(row, K, scratch);
+    for (int64_t k = 0; k < K; ++k) out[k] = mqo_f64_to_f16(scratch[k]);
+}
+
+/* y[i][j] = sum over k of W16[rows[j]][k] * X16[toks[i]][k], the binary16
+ * values taken exactly and the products summed in binary64; T[i][j] = the sum
+ * of the products' magnitudes (the scale of the float tolerance) */
+void mqo_gemm_f16(const uint16_t* W16, const uint16_t* X16, int64_t K, const int64_t* rows, int64_t nr,
+                  const int64_t* toks, int64_t nt, double* y, double* T)
+{
+    for (int64_t i = 0; i < nt; ++i) {
+        const uint16_t* x = X16 + toks[i] * K;
+        for (int64_t j = 0; j < nr; ++j) {
+            const uint16_t* w = W16 + rows[j] * K;
+            double sum = 0.0, mag = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double prod = (double)mqo_f16_to_f32(w[k]) * (double)mqo_f16_to_f32(x[k]);
+                sum += prod;
+                mag += fabs(prod);
+            }
+            y[i * nr + j] = sum;
+            T[i * nr + j] = mag;
+        }
     }
 }
