@@ -152,6 +152,15 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def measured_bf16_peak():
+    """Dense bf16 tensor TFLOP/s measured on this machine (burst); f16 runs at the same rate."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 1900.0
+
+
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "quantized_decode_matvec_gb300", "csrc")
@@ -494,8 +503,19 @@ def config_suite(mq, device, oracle_arms=True):
     calls, keep = ffn_calls(pairs, f.H, f.I, x)
     ms = timed(calls)
     wb = sum(a.numel() + b.numel() for a, b in pairs)
-    rec("ffn_0.5B_x24_per_layer", ms, wb // f.n_layers, total_us_24_layers=round(ms * 1e3 * f.n_layers, 2))
-    del pairs, keep
+    rec("ffn_0.5B_x24_per_layer", ms, wb // f.n_layers, total_us_24_layers=round(ms * 1e3 * f.n_layers, 2),
+        launch="two kernels per layer (gate/up, down), 48 graph nodes")
+    # the same 24 layers as one persistent launch (mq_step on an FFN-only stack: the down
+    # phase reads h as tagged records, each layer's gate/up waits for every CTA's previous down)
+    sb = mq.StepBuffers([{"gu": gu, "down": dn} for gu, dn in pairs], f.H, f.I, 0, 0, 0, 1)
+    for l in range(f.n_layers):
+        sb.c[l].copy_(torch.from_numpy(synth.ffn_layer_input(f, l)))
+    ms_p = timed([lambda: sb.step(torch.cuda.current_stream(), mq.MQ_STEP_PERSISTENT)]) / f.n_layers
+    rec("ffn_0.5B_x24_persistent_per_layer", ms_p, wb // f.n_layers,
+        total_us_24_layers=round(ms_p * 1e3 * f.n_layers, 2),
+        launch="one persistent kernel for the 24 layers (mq_step, FFN-only stack)")
+    assert mq.mq_read_device_status(0) == 0
+    del pairs, keep, sb
     ora("ffn_0.5B_x24_per_layer", lambda a: [a.ffn(gu, dn, x_np, f.H, f.I) for gu, dn in host], reps=1,
         per=f.n_layers)
     del host
@@ -546,9 +566,78 @@ def config_suite(mq, device, oracle_arms=True):
         del copies, descs
         ora(f"{wt}_weights_4096x{K}",
             lambda a: a.matvec_w(wt, W_np, oracle.quantize_q8_0(x_np), synth.KSWEEP_ROWS, K))
+    # prefill on the tensor cores: one 7B-class layer's GEMMs at 2048 tokens over the resident
+    # f16 weight cache (built by mq_dequant_q4K_f16), activations converted once to f16
+    tflops_peak = measured_bf16_peak()
+    T = 2048
+    st = synth.STEP_7B
+    shapes = {"qkv": (st.qkv_rows, st.H), "o": (st.H, st.q_rows), "ffn_gu": (2 * st.I, st.H), "down": (st.H, st.I)}
+    layer_us = 0.0
+    for name, (R, K) in shapes.items():
+        W16 = mq.dequant_q4K_f16(torch.from_numpy(synth.q4K_matrix(R, K, seed=90, tag=synth.TAG_W)).to(device), R, K)
+        X16 = mq.convert_f32_f16(torch.from_numpy(synth.activation(K, T, seed=91)).to(device))
+        Y = torch.empty((T, R), dtype=torch.float32, device=device)
+        ms = timed([lambda: mq.gemm_f16(W16, X16, out=Y, stream=torch.cuda.current_stream())], reps=5)
+        tf = 2.0 * T * R * K / (ms / 1e3) / 1e12
+        out[f"prefill_gemm_{name}_{R}x{K}_T{T}"] = dict(
+            us_per_call=round(ms * 1e3, 2), tflops=round(tf, 1), bound="tensor",
+            frac_of_measured_f16_peak=round(tf / tflops_peak, 3) if tflops_peak else None,
+            kernel="gemm_f16_kernel (tcgen05.mma kind::f16, 128x256 tiles, TMA 128-byte swizzle)")
+        layer_us += ms * 1e3
+        del W16, X16, Y
+    out["prefill_7B_layer_T2048"] = dict(us_per_layer=round(layer_us, 1),
+                                         tokens_per_s_28_layers=round(T / (28 * layer_us / 1e6), 0),
+                                         note="the four projection GEMMs of one layer; no attention, SiLU*mul or norms")
+    assert mq.mq_read_device_status(0) == 0
     torch.cuda.synchronize()
     for a in arms:
         a.close()
+    return out
+
+
+def scaled_weight_copy(W, shift):
+    """A device copy of a q4_K matrix with every super-block's d and dmin times 2^-shift (benchmark
+    data only: the same quants and scales, smaller block scales)."""
+    import torch
+    Wc = W.clone()
+    blk = Wc.view(-1, 144)
+    dd = blk[:, 0:4].contiguous().view(torch.float16)
+    dd = (dd.float() * 2.0 ** -shift).to(torch.float16)
+    blk[:, 0:4] = dd.contiguous().view(torch.uint8).view(-1, 4)
+    return Wc
+
+
+def chained_arm(mq, case, layers, stream, g_default, shift=11, rounds=3, reps=5):
+    """The step as a real decode chain (MQ_STEP_CHAINED): o reads q|k|v's output, the FFN reads o's,
+    layer l+1 reads layer l's FFN output, passed between CTAs as tagged records.  Timed interleaved
+    with the default persistent step.  A chain with no normalization between layers does not keep its
+    scale (each SwiGLU layer squares it, and the weights' positive mean adds a component common to all
+    rows that grows about K*mean per projection), so its weights are copies with d and dmin times
+    2^-shift: the values stay finite and shrink to zero within a few layers instead of overflowing to
+    inf (the kernels' work is the same for any finite values)."""
+    import torch
+    from quantized_decode_matvec_gb300.graph import StepGraph
+    from quantized_decode_matvec_gb300 import synth
+    wc = [{k: scaled_weight_copy(v, shift) for k, v in w.items()} for w in layers]
+    cb = mq.StepBuffers(wc, case.H, case.I, case.qkv_rows, case.H, case.q_rows, case.ncols, chained=True)
+    cb.a[0].copy_(torch.from_numpy(synth.step_layer_inputs(case, 0, 0)["a"]))
+    gc = StepGraph(cb, flags=mq.MQ_STEP_PERSISTENT, stream=stream)
+    t_chain, t_def = [], []
+    for _ in range(rounds):
+        t_chain += time_replays(gc.run, stream, reps)
+        t_def += time_replays(g_default.run, stream, reps)
+    torch.cuda.synchronize()
+    assert mq.mq_read_device_status(0) == 0
+    mags = cb.y_ffn.abs().amax(dim=(1, 2)).cpu().tolist()
+    nonzero = sum(1 for m in mags if m > 0)
+    out = {"median_ms": statistics.median(t_chain), "mean_ms": statistics.mean(t_chain), "sem_ms": sem(t_chain),
+           "default_persistent_interleaved_median_ms": statistics.median(t_def),
+           "weights": f"the step's weights with d, dmin x 2^-{shift}",
+           "max_abs_ffn_out_first_last_layer": [mags[0], mags[-1]],
+           "layers_with_nonzero_ffn_out": nonzero,
+           "finite": bool(torch.isfinite(cb.outputs).all().item())}
+    del gc, cb, wc
+    torch.cuda.empty_cache()
     return out
 
 
@@ -620,6 +709,9 @@ def run_ours(args):
             arms["eager"] += time_replays(eager_run, stream, 5)
     arm_stats = {k: {"median_ms": statistics.median(v), "mean_ms": statistics.mean(v), "sem_ms": sem(v)}
                  for k, v in arms.items()}
+    if not args.no_chained_arm:
+        arm_stats["persistent_chained"] = chained_arm(mq, case, layers, stream, g)
+
 
     peak, peak_kind = measured_hbm_peak()
     act_bytes = case.n_layers * (3 * case.H * 4 + case.I // 32 * 34 * 2) * case.ncols
@@ -729,6 +821,7 @@ def main(argv=None):
                     help="step launch mode: one persistent kernel, or four kernels per layer (plain or PDL)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-config timings (context only)")
+    ap.add_argument("--no-chained-arm", action="store_true", help="skip the chained-step arm (context only)")
     ap.add_argument("--layers", type=int, default=28,
                     help="layers of the 7B stack (28 = the bench workload; fewer only for small profiling runs)")
     args = ap.parse_args(argv)

@@ -68,6 +68,8 @@ typedef int mq_status;
 #define MQ_DEV_DESC_MISMATCH 1u  /* a kernel's device descriptor disagreed with its launch shape */
 #define MQ_DEV_DESC_ALIGN 2u     /* a device descriptor held a misaligned pointer */
 #define MQ_DEV_TIMEOUT 4u        /* a kernel's bounded wait on its copy pipeline gave up; outputs not written */
+#define MQ_DEV_ALIAS 8u          /* a persistent step's input overlaps an output of the same launch outside
+                                    the MQ_STEP_CHAINED pattern; nothing was written */
 
 /* quantization types (mq_concat_rows*) */
 #define MQ_TYPE_Q4_K 1
@@ -208,7 +210,11 @@ mq_status mq_ffn_gate_up(const mq_ffn_desc* d_desc, int32_t H, int32_t I, int32_
  * Per layer, in order: qkv (the concatenated q|k|v projection, input x = a_l),
  * o (input b_l), then the FFN (input c_l).  d_layers: device array of
  * n_layers layer descriptors.  h_shape: host copy of the shapes (grid sizes;
- * the capture key).  Capturable as one CUDA graph. */
+ * the capture key).  Capturable as one CUDA graph.
+ *
+ * A stack of FFN layers only: qkv_rows == 0 and o_rows == 0 (then o_K and the
+ * qkv and o parts of every descriptor are ignored); either projection may be
+ * left out on its own the same way. */
 typedef struct mq_layer_desc {
     mq_mv_desc qkv;
     mq_mv_desc o;
@@ -217,6 +223,7 @@ typedef struct mq_layer_desc {
 
 #define MQ_STEP_PDL 1u         /* multi-kernel path: launch with programmatic dependent launch */
 #define MQ_STEP_PERSISTENT 2u  /* one persistent kernel for the whole stack (needs `workspace`) */
+#define MQ_STEP_CHAINED 4u     /* every phase reads the previous phase's output (a real decode chain) */
 
 /* bytes of the persistent step's fixed workspace words (abort word, per-CTA
  * phase flags); the whole workspace a shape needs is mq_step_workspace_bytes */
@@ -242,19 +249,62 @@ typedef struct mq_step_shape {
  * With it: a single cooperative launch of one CTA per SM that runs every
  * layer, the weight stream running ahead across the dependency points.  At
  * each point a CTA waits, bounded in time (a timeout records MQ_DEV_TIMEOUT),
- * until every CTA has finished the previous phase: each CTA publishes a phase
- * flag in `workspace` after it has written that phase's outputs, and the
- * gate/up phase also writes h there as tagged records (a data word and its
- * phase in one 8-byte store), which the down phase reads and checks.  Both
- * paths give bit-identical outputs.  The persistent kernel needs every SM: it
- * fails with MQ_ERR_CUDA if the device cannot host its whole grid at once. */
+ * until what it reads has been written.  The gate/up phase writes h into
+ * `workspace` as tagged records (a data word and its phase in one 8-byte
+ * store), which the down phase reads and checks word by word.  Both paths give
+ * bit-identical outputs.  The persistent kernel needs every SM: it fails with
+ * MQ_ERR_CUDA if the device cannot host its whole grid at once.
+ *
+ * Inputs of the persistent step:
+ *  - default: every input (a_l, b_l, c_l or their q8_0 forms) is a buffer that
+ *    no phase of the launch writes.  Each CTA publishes a phase flag once it
+ *    has written a phase's outputs and the next phase waits for every CTA's
+ *    flag, which orders the phases; no input is produced in the launch, so no
+ *    input needs to be made visible.  The kernel checks every input against
+ *    every output of the launch first; an overlap records MQ_DEV_ALIAS and
+ *    nothing is written.
+ *  - MQ_STEP_CHAINED: a decode chain.  The input of every qkv, o and FFN phase
+ *    is the fp32 output of the phase before it: o_l.x == qkv_l.y, ffn_l.x ==
+ *    o_l.y, qkv_{l+1}.x == ffn_l.y (with a phase left out, the one before
+ *    it); layer 0's first phase reads the caller's input.  For ncols > 1 the
+ *    producer's y_ld must equal the consumer's K.  Every such output is also
+ *    written into `workspace` as tagged records, and the consumer stages its
+ *    input from them, so one load both reads a value and proves it written
+ *    (no fence on the path).  The kernel checks the pattern first; a
+ *    descriptor that breaks it records MQ_DEV_DESC_MISMATCH and nothing is
+ *    written.  Without MQ_STEP_PERSISTENT the flag changes nothing: kernel
+ *    boundaries order the launches whatever the inputs are. */
 mq_status mq_step(const mq_layer_desc* d_layers, const mq_step_shape* h_shape, void* stream);
 
-/* Bytes of workspace mq_step needs for h_shape with MQ_STEP_PERSISTENT:
- * MQ_STEP_WORKSPACE_BYTES plus ncols * (I/128) * 320 bytes of h records.
- * Host only; checks the shape as mq_step does (MQ_ERR_SHAPE, and
- * MQ_ERR_INVALID_ARG for a null pointer). */
+/* Bytes of workspace mq_step needs for h_shape with MQ_STEP_PERSISTENT (and
+ * the shape's flags): MQ_STEP_WORKSPACE_BYTES plus ncols * (I/128) * 320
+ * bytes of h records, and with MQ_STEP_CHAINED 8 * ncols * rows bytes of
+ * output records for each of q|k|v, o and down that is present (rows =
+ * qkv_rows, o_rows, H), each rounded up to a multiple of 32.  Host only; checks the shape as mq_step does
+ * (MQ_ERR_SHAPE, and MQ_ERR_INVALID_ARG for a null pointer).  The call cannot
+ * see the workspace's size: a smaller workspace is the caller's error. */
 mq_status mq_step_workspace_bytes(const mq_step_shape* h_shape, size_t* bytes);
+
+/* ---- prefill: the resident f16 weight cache and the tensor-core GEMM -----------------
+ * "07 . R3 -- Small-model per-token overhead", section 1: 7B prefill at 2K
+ * tokens runs a half-precision tensor-core GEMM over a resident f16 copy of
+ * the quantized weights, built once.
+ *
+ * mq_dequant_q4K_f16: W16[r][k] = f16(d*sc*q - dmin*m) of q4_K W [rows][K/256]
+ *   (the weight formed exactly, rounded once to nearest-even); W 16-byte
+ *   aligned, W16 f16 [rows][K] 16-byte aligned, K % 256 == 0.
+ * mq_convert_f32_f16: y[i] = f16(x[i]) (round to nearest-even), n values;
+ *   x 4-byte, y 2-byte aligned.
+ * mq_gemm_f16: Y[t][r] = sum over k of X16[t][k] * W16[r][k], fp32
+ *   accumulation on the tensor cores (tcgen05), fp32 Y [T][R] (row t of Y
+ *   holds token t's R outputs).  W16 [R][K] and X16 [T][K] f16 row-major,
+ *   16-byte aligned; Y 4-byte aligned; K % 64 == 0; R, T >= 1.  Unlike the
+ *   decode calls the operands' addresses are baked into the launch (tensor
+ *   maps built on the host), so a captured graph keeps the buffers it saw.
+ *   Limits: K <= MQ_MAX_K. */
+mq_status mq_dequant_q4K_f16(const void* W, void* W16, int64_t rows, int64_t K, void* stream);
+mq_status mq_convert_f32_f16(const float* x, void* y, int64_t n, void* stream);
+mq_status mq_gemm_f16(const void* W16, const void* X16, float* Y, int32_t R, int32_t K, int32_t T, void* stream);
 
 /* ---- the FFN without caller scratch --------------------------------------------------
  * No counterpart in the pages: they describe the FFN kernels, not how a

@@ -19,8 +19,9 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libmq.so")
 
-SOURCES = ["api.cu", "matvec.cu", "ffn.cu", "quantize.cu", "ring.cu", "step.cu", "noalloc.cu", "wtypes.cu", "ring_cols.cu"]
-HEADERS = ["mq_device.cuh", "mq_stream.cuh", "mq_internal.h", "mq_job.cuh", "mq_epilogue.cuh", "mq_tma.cuh", "mq_unit.cuh", "mq_ring.cuh", "mq_ring_kernel.cuh"]
+SOURCES = ["api.cu", "matvec.cu", "ffn.cu", "quantize.cu", "ring.cu", "step.cu", "noalloc.cu", "wtypes.cu", "ring_cols.cu",
+           "gemm.cu", "dequant.cu", "step_chained.cu"]
+HEADERS = ["mq_device.cuh", "mq_stream.cuh", "mq_internal.h", "mq_job.cuh", "mq_epilogue.cuh", "mq_tma.cuh", "mq_unit.cuh", "mq_ring.cuh", "mq_ring_kernel.cuh", "mq_umma.cuh", "mq_step_kernel.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--extended-lambda", "-Xcompiler", "-fPIC",

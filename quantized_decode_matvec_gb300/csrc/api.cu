@@ -16,6 +16,7 @@ cudaError_t set_ring_attributes(int max_smem);
 cudaError_t set_step_attributes(int max_smem);
 cudaError_t set_wring_attributes(int max_smem);
 cudaError_t set_ring_cols_attributes(int max_smem);
+cudaError_t set_gemm_attributes(int max_smem);
 void plan_ring(MvPlan& q, int64_t units, int kind, int nc, const DeviceInfo& dev, int64_t unit_bytes,
                bool allow_cols);
 }  // namespace mq
@@ -276,6 +277,11 @@ bool plan_step(const mq_step_shape& h, const DeviceInfo& dev, StepPlan* out)
     int64_t stage = 0, act = 0, part = 0, vals = 0;
     for (int ph = 0; ph < 4; ++ph) {
         MvPlan q = {};
+        if (Rs[ph] == 0) {  // a projection left out: no tiles, no staging
+            q.T = 1;
+            sp.ph[ph] = q;
+            continue;
+        }
         q.C = int(Ks[ph] / 128);
         if (!unit_split(q.C, nc, true, q)) return false;
         if (q.nwc > nwc_max) nwc_max = q.nwc;
@@ -294,8 +300,6 @@ bool plan_step(const mq_step_shape& h, const DeviceInfo& dev, StepPlan* out)
         q.T = int(T);
         q.rows_per_cta = int(rpc);
         q.variant = 1;
-        q.fault = fault_policy();
-        q.wait_ms = q.fault == FAULT_NONE ? 2000 : 50;
         const int64_t st = (T * row_bytes + 127) / 128 * 128;
         if (st > stage) stage = st;
         if (int64_t(nc) * q.C * 160 > act) act = int64_t(nc) * q.C * 160;
@@ -309,6 +313,8 @@ bool plan_step(const mq_step_shape& h, const DeviceInfo& dev, StepPlan* out)
     int64_t ns = (dev.max_smem_optin - 256 - fixed) / stage;  // the kernel has a few static bytes too
     if (ns > 8) ns = 8;
     if (ns < 2) return false;
+    // the input/output overlap check keeps 16 byte ranges per layer in the ring's memory
+    if (int64_t(h.n_layers) * 16 * 16 > ns * stage) return false;
     const int off_ring = 256, off_act = int(256 + ns * stage), off_part = int(off_act + act);
     const int off_vals = int(off_part + (part + 15) / 16 * 16);
     for (int ph = 0; ph < 4; ++ph) {
@@ -320,6 +326,8 @@ bool plan_step(const mq_step_shape& h, const DeviceInfo& dev, StepPlan* out)
         q.off_part = off_part;
         q.off_vals = off_vals;
         q.grid = int(G);
+        q.fault = fault_policy();
+        q.wait_ms = q.fault == FAULT_NONE ? 2000 : 50;
     }
     sp.n_layers = h.n_layers;
     // L2 prefetch window: the whole grid's prefetched tiles take at most a
@@ -331,7 +339,10 @@ bool plan_step(const mq_step_shape& h, const DeviceInfo& dev, StepPlan* out)
     sp.grid = int(G);
     if (sp.grid > kWsMaxCtas) return false;  // one phase flag per CTA in the workspace
     sp.smem = int(off_vals + vals);
-    sp.ws_bytes = step_workspace_bytes(nc, h.I);
+    const StepWorkspace w = step_workspace(h);
+    sp.ws_bytes = w.bytes;
+    sp.chained = (h.flags & MQ_STEP_CHAINED) != 0;
+    for (int ph = 0; ph < 4; ++ph) sp.yrec_off[ph] = w.yrec_off[ph];
     *out = sp;
     return true;
 }
@@ -344,6 +355,7 @@ cudaError_t set_kernel_attributes(int max_smem)
     if (e == cudaSuccess) e = set_step_attributes(max_smem);
     if (e == cudaSuccess) e = set_wring_attributes(max_smem);
     if (e == cudaSuccess) e = set_ring_cols_attributes(max_smem);
+    if (e == cudaSuccess) e = set_gemm_attributes(max_smem);
     return e;
 }
 
@@ -632,28 +644,34 @@ mq_status mq_ffn_gate_up(const mq_ffn_desc* d_desc, int32_t H, int32_t I, int32_
     return e == cudaSuccess ? MQ_OK : cuda_fail(e);
 }
 
+// the shapes of a step: q|k|v and o may be left out (zero rows), the FFN may not
+static mq_status check_step_shape(const mq_step_shape* h)
+{
+    if (h->n_layers < 0 || h->ncols < 0 || h->qkv_rows < 0 || h->o_rows < 0) return MQ_ERR_SHAPE;
+    if (h->flags & ~uint32_t(MQ_STEP_PDL | MQ_STEP_PERSISTENT | MQ_STEP_CHAINED)) return MQ_ERR_INVALID_ARG;
+    mq_status st;
+    if (h->qkv_rows > 0 && (st = check_mv_shape(h->qkv_rows, h->H, h->ncols)) != MQ_OK) return st;
+    if (h->o_rows > 0 && (st = check_mv_shape(h->o_rows, h->o_K, h->ncols)) != MQ_OK) return st;
+    return check_ffn_shape(h->H, h->I, h->ncols);
+}
+
 mq_status mq_step_workspace_bytes(const mq_step_shape* h, size_t* bytes)
 {
     if (!h || !bytes) return MQ_ERR_INVALID_ARG;
-    if (h->n_layers < 0 || h->ncols < 0) return MQ_ERR_SHAPE;
-    mq_status st = check_ffn_shape(h->H, h->I, h->ncols);
+    mq_status st = check_step_shape(h);
     if (st != MQ_OK) return st;
-    *bytes = mq::step_workspace_bytes(h->ncols, h->I);
+    *bytes = mq::step_workspace(*h).bytes;
     return MQ_OK;
 }
 
 mq_status mq_step(const mq_layer_desc* d_layers, const mq_step_shape* h, void* stream)
 {
     if (!h) return MQ_ERR_INVALID_ARG;
-    if (h->n_layers < 0) return MQ_ERR_SHAPE;
+    mq_status st = check_step_shape(h);
+    if (st != MQ_OK) return st;
     if (h->n_layers == 0 || h->ncols == 0) return MQ_OK;
     if (!d_layers) return MQ_ERR_INVALID_ARG;
     if (!aligned(d_layers, 8)) return MQ_ERR_ALIGN;
-    mq_status st;
-    if ((st = check_mv_shape(h->qkv_rows, h->H, h->ncols)) != MQ_OK) return st;
-    if ((st = check_mv_shape(h->o_rows, h->o_K, h->ncols)) != MQ_OK) return st;
-    if ((st = check_ffn_shape(h->H, h->I, h->ncols)) != MQ_OK) return st;
-    if (h->qkv_rows == 0 || h->o_rows == 0) return MQ_ERR_SHAPE;
     if (h->flags & MQ_STEP_PERSISTENT) {
         if (!h->workspace) return MQ_ERR_INVALID_ARG;
         if (!aligned(h->workspace, 16)) return MQ_ERR_ALIGN;
@@ -668,23 +686,66 @@ mq_status mq_step(const mq_layer_desc* d_layers, const mq_step_shape* h, void* s
         cudaError_t e = mq::launch_step(d_layers, sp, h->ncols, dev->status, static_cast<unsigned*>(h->workspace), s);
         return e == cudaSuccess ? MQ_OK : cuda_fail(e);
     }
-    // one plan per projection, decided once for the whole stack
+    // one plan per projection, decided once for the whole stack (none for a projection left out)
     mq::MvPlan p_qkv, p_o, p_gu, p_down;
-    if (!mq::plan_mv(h->qkv_rows, h->H, h->ncols, mq::KIND_MV, 0, *dev, &p_qkv) ||
-        !mq::plan_mv(h->o_rows, h->o_K, h->ncols, mq::KIND_MV, 0, *dev, &p_o) ||
+    if ((h->qkv_rows > 0 && !mq::plan_mv(h->qkv_rows, h->H, h->ncols, mq::KIND_MV, 0, *dev, &p_qkv)) ||
+        (h->o_rows > 0 && !mq::plan_mv(h->o_rows, h->o_K, h->ncols, mq::KIND_MV, 0, *dev, &p_o)) ||
         !mq::plan_mv(2 * int64_t(h->I), h->H, h->ncols, mq::KIND_GU, h->I, *dev, &p_gu) ||
         !mq::plan_mv(h->H, h->I, h->ncols, mq::KIND_DOWN, 0, *dev, &p_down))
         return MQ_ERR_UNSUPPORTED;
     for (int32_t l = 0; l < h->n_layers; ++l) {
         const mq_layer_desc* L = d_layers + l;
-        cudaError_t e = mq::launch_mv(&L->qkv, mq::KIND_MV, h->qkv_rows, h->H, h->ncols, p_qkv, dev->status, s, pdl);
-        if (e == cudaSuccess) e = mq::launch_mv(&L->o, mq::KIND_MV, h->o_rows, h->o_K, h->ncols, p_o, dev->status, s, pdl);
+        cudaError_t e = cudaSuccess;
+        if (h->qkv_rows > 0)
+            e = mq::launch_mv(&L->qkv, mq::KIND_MV, h->qkv_rows, h->H, h->ncols, p_qkv, dev->status, s, pdl);
+        if (e == cudaSuccess && h->o_rows > 0)
+            e = mq::launch_mv(&L->o, mq::KIND_MV, h->o_rows, h->o_K, h->ncols, p_o, dev->status, s, pdl);
         if (e == cudaSuccess) e = mq::launch_gu(&L->ffn, h->H, h->I, h->ncols, p_gu, dev->status, s, pdl);
         if (e == cudaSuccess)
             e = mq::launch_mv(&L->ffn, mq::KIND_DOWN, h->H, h->I, h->ncols, p_down, dev->status, s, pdl);
         if (e != cudaSuccess) return cuda_fail(e);
     }
     return MQ_OK;
+}
+
+mq_status mq_dequant_q4K_f16(const void* W, void* W16, int64_t rows, int64_t K, void* stream)
+{
+    if (rows < 0 || K <= 0 || K % 256) return MQ_ERR_SHAPE;
+    if (rows == 0) return MQ_OK;
+    if (!W || !W16) return MQ_ERR_INVALID_ARG;
+    if (!aligned(W, 16) || !aligned(W16, 16)) return MQ_ERR_ALIGN;
+    const mq::DeviceInfo* dev = nullptr;
+    mq_status st = current_dev(&dev);
+    if (st != MQ_OK) return st;
+    cudaError_t e = mq::launch_dequant_q4K_f16(W, W16, rows * (K / 256), dev->num_sms, as_stream(stream));
+    return e == cudaSuccess ? MQ_OK : cuda_fail(e);
+}
+
+mq_status mq_convert_f32_f16(const float* x, void* y, int64_t n, void* stream)
+{
+    if (n < 0) return MQ_ERR_SHAPE;
+    if (n == 0) return MQ_OK;
+    if (!x || !y) return MQ_ERR_INVALID_ARG;
+    if (!aligned(x, 4) || !aligned(y, 2)) return MQ_ERR_ALIGN;
+    const mq::DeviceInfo* dev = nullptr;
+    mq_status st = current_dev(&dev);
+    if (st != MQ_OK) return st;
+    cudaError_t e = mq::launch_f32_to_f16(x, y, n, dev->num_sms, as_stream(stream));
+    return e == cudaSuccess ? MQ_OK : cuda_fail(e);
+}
+
+mq_status mq_gemm_f16(const void* W16, const void* X16, float* Y, int32_t R, int32_t K, int32_t T, void* stream)
+{
+    if (R < 0 || T < 0 || K <= 0 || K % 64) return MQ_ERR_SHAPE;
+    if (K > MQ_MAX_K) return MQ_ERR_UNSUPPORTED;
+    if (R == 0 || T == 0) return MQ_OK;
+    if (!W16 || !X16 || !Y) return MQ_ERR_INVALID_ARG;
+    if (!aligned(W16, 16) || !aligned(X16, 16) || !aligned(Y, 4)) return MQ_ERR_ALIGN;
+    const mq::DeviceInfo* dev = nullptr;
+    mq_status st = current_dev(&dev);
+    if (st != MQ_OK) return st;
+    cudaError_t e = mq::launch_gemm_f16(W16, X16, Y, R, K, T, dev->num_sms, dev->status, as_stream(stream));
+    return e == cudaSuccess ? MQ_OK : cuda_fail(e);
 }
 
 mq_status mq_debug_block_sums_q4K_q8_0(const mq_mv_desc* d_desc, int32_t rows, int32_t K, int32_t ncols,

@@ -1,0 +1,252 @@
+// gemm.cu -- the prefill GEMM on the 5th-generation tensor cores.
+//
+// "07 . R3 -- Small-model per-token overhead", section 1: prefill of the 7B
+// model at 2K tokens runs a half-precision tensor-core GEMM over a resident
+// f16 copy of the weights (the quantized weights dequantized once).  Here:
+//
+//   Y[t][r] = sum_k X[t][k] * W[r][k]      X f16 [T][K], W f16 [R][K], Y fp32 [T][R]
+//
+// with fp32 accumulation in tensor memory.  One CTA per SM walks output tiles
+// of 128 weight rows x 256 tokens (persistent, static round robin; tiles that
+// share a weight block run at the same time, so each block comes from HBM
+// about once and from L2 for the other token tiles).  Per CTA:
+//
+// * warp 0, one lane: TMA loads of 128x64 weight and 256x64 activation tiles
+//   (128-byte swizzle) into a ring of shared-memory stages, tracked by
+//   mbarriers;
+// * warp 1: allocates 512 TMEM columns (two 128x256 fp32 accumulators); one
+//   lane issues four tcgen05.mma (M=128, N=256, K=16) per stage and commits
+//   each stage back to the producer, and each finished tile to the epilogue;
+// * warps 2..5: the epilogue reads its 32 TMEM lanes (32 weight rows) with
+//   tcgen05.ld and stores fp32 Y, coalesced across the rows, while the MMAs
+//   of the next tile fill the other accumulator.
+//
+// Every wait is bounded in time: on a timeout the CTA records MQ_DEV_TIMEOUT,
+// the roles stop, the producer waits (bounded) for its copies in flight and
+// TMEM is freed before the CTA exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "mq_internal.h"
+#include "mq_umma.cuh"
+
+namespace mq {
+
+constexpr int kGemmBM = 128;                          // weight rows per tile (TMEM lanes)
+constexpr int kGemmBN = 256;                          // tokens per tile (accumulator columns)
+constexpr int kGemmBK = 64;                           // f16 per 128-byte swizzled row
+constexpr int kGemmStages = 4;
+constexpr int kGemmATile = kGemmBM * kGemmBK * 2;     // 16 KB
+constexpr int kGemmBTile = kGemmBN * kGemmBK * 2;     // 32 KB
+constexpr int kGemmStage = kGemmATile + kGemmBTile;   // 48 KB
+constexpr int kGemmThreads = 192;
+constexpr uint32_t kGemmTmemCols = 512;
+constexpr int kGemmSmem = kGemmStages * kGemmStage + 1024;  // + alignment slack
+
+struct GemmArgs {
+    int R, K, T;
+    int m_tiles, n_tiles, k_steps;
+    uint64_t limit_ns;
+};
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_f16_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                    float* __restrict__ Y, const GemmArgs a, unsigned* status)
+{
+    extern __shared__ uint8_t gsm_raw[];
+    __shared__ __align__(8) uint64_t full[kGemmStages], empty[kGemmStages], accf[2], acce[2];
+    __shared__ uint32_t tmem_base;
+    __shared__ volatile int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // the swizzled tiles want 1024-byte alignment
+    const uint32_t raw = smem_u32(gsm_raw);
+    uint8_t* const gsm = gsm_raw + ((1024u - (raw & 1023u)) & 1023u);
+    const int ntiles = a.m_tiles * a.n_tiles;
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int s = 0; s < kGemmStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&accf[b], 1);
+            mbar_init(&acce[b], 4 * 32);
+        }
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmW);
+        tma_prefetch_desc(&tmX);
+    }
+    if (warp == 1) tmem_alloc(&tmem_base, kGemmTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+
+    if (warp == 0) {
+        // ---- TMA producer
+        if (lane == 0) {
+            int it = 0;
+            for (int t = blockIdx.x; t < ntiles && !abort_flag; t += gridDim.x) {
+                const int m = t / a.n_tiles, n = t - m * a.n_tiles;
+                for (int kk = 0; kk < a.k_steps; ++kk, ++it) {
+                    const int s = it % kGemmStages;
+                    if (it >= kGemmStages &&
+                        !mbar_wait_bounded(&empty[s], uint32_t(it / kGemmStages - 1) & 1u, a.limit_ns)) {
+                        abort_flag = 1;
+                        break;
+                    }
+                    uint8_t* sa = gsm + s * kGemmStage;
+                    mbar_arrive_expect_tx(&full[s], kGemmStage);
+                    tma_load_2d(sa, &tmW, kk * kGemmBK, m * kGemmBM, &full[s]);
+                    tma_load_2d(sa + kGemmATile, &tmX, kk * kGemmBK, n * kGemmBN, &full[s]);
+                }
+            }
+            // copies still in flight land before the CTA can exit
+            for (int j = it > kGemmStages ? it - kGemmStages : 0; j < it; ++j)
+                (void)mbar_wait_bounded(&full[j % kGemmStages], uint32_t(j / kGemmStages) & 1u, a.limit_ns);
+        }
+    } else if (warp == 1) {
+        // ---- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = umma_idesc_f16_f32(kGemmBM, kGemmBN);
+            int it = 0, tl = 0;
+            for (int t = blockIdx.x; t < ntiles && !abort_flag; t += gridDim.x, ++tl) {
+                const int b = tl & 1;
+                if (tl >= 2 && !mbar_wait_bounded(&acce[b], uint32_t(tl / 2 - 1) & 1u, a.limit_ns)) {
+                    abort_flag = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + uint32_t(b * kGemmBN);
+                bool ok = true;
+                for (int kk = 0; kk < a.k_steps; ++kk, ++it) {
+                    const int s = it % kGemmStages;
+                    if (!mbar_wait_bounded(&full[s], uint32_t(it / kGemmStages) & 1u, a.limit_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(gsm + s * kGemmStage);
+#pragma unroll
+                    for (int k4 = 0; k4 < kGemmBK / 16; ++k4)
+                        umma_f16(d, umma_desc_sw128(sa + 32u * k4), umma_desc_sw128(sa + kGemmATile + 32u * k4), idesc,
+                                 kk > 0 || k4 > 0);
+                    umma_commit(&empty[s]);  // the stage is free once these MMAs have read it
+                }
+                if (!ok) {
+                    abort_flag = 1;
+                    break;
+                }
+                umma_commit(&accf[b]);  // the tile's accumulator is complete
+            }
+            // the last commits land before TMEM is freed
+            if (it > 0) {
+                const int j = it - 1;
+                (void)mbar_wait_bounded(&empty[j % kGemmStages], uint32_t(j / kGemmStages) & 1u, a.limit_ns);
+            }
+        }
+    } else {
+        // ---- epilogue: TMEM lanes 32*(warp%4) .. +31 = weight rows of the tile
+        const int q = warp & 3;
+        const uint32_t lane_base = uint32_t(q * 32) << 16;
+        int tl = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tl) {
+            const int b = tl & 1;
+            const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&accf[b], uint32_t(tl / 2) & 1u, a.limit_ns));
+            if (!ok || abort_flag) {
+                if (lane == 0) abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            const int m = t / a.n_tiles, n = t - m * a.n_tiles;
+            const int r = m * kGemmBM + q * 32 + lane;
+            const int t0 = n * kGemmBN;
+#pragma unroll 1
+            for (int c0 = 0; c0 < kGemmBN; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_base + uint32_t(b * kGemmBN + c0), v);
+                tmem_ld_wait();
+                if (r < a.R) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int tok = t0 + c0 + j;
+                        if (tok < a.T) Y[size_t(tok) * a.R + r] = __uint_as_float(v[j]);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&acce[b]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (abort_flag && threadIdx.x == 0) atomicOr(status, MQ_DEV_TIMEOUT);
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kGemmTmemCols);
+    }
+}
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 2-D tensor map of a row-major f16 matrix [rows][K], box {64, box_rows}, 128-byte swizzle
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t K, int box_rows)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(K) * 2};
+    const cuuint32_t box[2] = {cuuint32_t(kGemmBK), cuuint32_t(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t set_gemm_attributes(int max_smem)
+{
+    (void)max_smem;
+    return cudaFuncSetAttribute(gemm_f16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+}
+
+// returns cudaErrorInvalidValue when the tensor maps cannot be built
+cudaError_t launch_gemm_f16(const void* W16, const void* X16, float* Y, int R, int K, int T, int num_sms,
+                            unsigned* status, cudaStream_t s)
+{
+    CUtensorMap tmW, tmX;
+    if (!make_map(&tmW, W16, R, K, kGemmBM) || !make_map(&tmX, X16, T, K, kGemmBN)) return cudaErrorInvalidValue;
+    GemmArgs a;
+    a.R = R;
+    a.K = K;
+    a.T = T;
+    a.m_tiles = (R + kGemmBM - 1) / kGemmBM;
+    a.n_tiles = (T + kGemmBN - 1) / kGemmBN;
+    a.k_steps = K / kGemmBK;
+    a.limit_ns = uint64_t(fault_policy() == FAULT_NONE ? 2000 : 50) * 1000000ull;
+    const int ntiles = a.m_tiles * a.n_tiles;
+    const int grid = ntiles < num_sms ? ntiles : num_sms;
+    gemm_f16_kernel<<<grid, kGemmThreads, kGemmSmem, s>>>(tmW, tmX, Y, a, status);
+    return cudaGetLastError();
+}
+
+}  // namespace mq

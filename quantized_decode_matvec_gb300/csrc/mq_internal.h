@@ -36,27 +36,52 @@ struct MvPlan {
 };
 
 // Plan of the persistent step kernel: one ring plan per phase (qkv, o, gate/up,
-// down) sharing the ring geometry and shared-memory layout of ph[0].
+// down) sharing the ring geometry and shared-memory layout of the phases.
 // Persistent-step workspace (bytes): [0, 256) control words (word 1: abort),
 // [256, 4352) one phase flag (u32) per CTA, then the h records: per column
 // 40 * (I/128) records of 8 bytes (a 32-bit word of the activation's unit
-// layout and the phase that wrote it).
+// layout and the phase that wrote it); for a chained step, then the output
+// records of the qkv, o and down phases: per phase ncols * rows records of 8
+// bytes (an fp32 output and the phase that wrote it), column-major, each
+// phase's area rounded up to 32 bytes.
 constexpr int kWsFlagsOff = 256;
 constexpr int kWsMaxCtas = 1024;
 constexpr int kWsRecOff = kWsFlagsOff + 4 * kWsMaxCtas;
 static_assert(kWsRecOff == MQ_STEP_WORKSPACE_BYTES, "workspace layout and header disagree");
-inline size_t step_workspace_bytes(int ncols, int I) { return size_t(kWsRecOff) + size_t(ncols) * (I / 128) * 40 * 8; }
+
+struct StepWorkspace {
+    size_t bytes;
+    int64_t yrec_off[4];  // byte offset of phase ph's output records (-1: none; gate/up never has any)
+};
+
+inline StepWorkspace step_workspace(const mq_step_shape& h)
+{
+    StepWorkspace w;
+    size_t off = size_t(kWsRecOff) + size_t(h.ncols) * (h.I / 128) * 40 * 8;
+    const int64_t rows[4] = {h.qkv_rows, h.o_rows, 0, h.H};
+    for (int ph = 0; ph < 4; ++ph) {
+        w.yrec_off[ph] = -1;
+        if ((h.flags & MQ_STEP_CHAINED) && rows[ph] > 0) {
+            w.yrec_off[ph] = int64_t(off);
+            off += (size_t(h.ncols) * size_t(rows[ph]) * 8 + 31) / 32 * 32;  // records are read 16 bytes at a time
+        }
+    }
+    w.bytes = off;
+    return w;
+}
 
 struct StepPlan {
     size_t ws_bytes;  // workspace the launch zeroes and uses
     MvPlan ph[4];
     int K[4];      // reduction length per phase
-    int R[4];      // rows per phase (gate/up: I)
+    int R[4];      // rows per phase (gate/up: I); 0 = phase left out
     int n_layers;
     int pf_tiles;  // tiles the producer prefetches into L2 beyond its next ring copy
     int nwc;       // consumer warps of the kernel (phases may use fewer)
     int grid;
     int smem;
+    int chained;              // MQ_STEP_CHAINED: inputs are the previous phase's output records
+    int64_t yrec_off[4];      // byte offsets of the output records in the workspace (-1: none)
 };
 
 // test-only fault injection (mq_debug_set_fault)
@@ -106,6 +131,11 @@ cudaError_t launch_block_sums(const mq_mv_desc* d, int rows, int K, int ncols, i
                               int smem, unsigned* status, cudaStream_t s);
 // raises the dynamic shared memory limit of every kernel on the current device
 cudaError_t set_kernel_attributes(int max_smem);
+// prefill operands and GEMM (dequant.cu, gemm.cu)
+cudaError_t launch_dequant_q4K_f16(const void* W, void* W16, int64_t nblocks, int num_sms, cudaStream_t s);
+cudaError_t launch_f32_to_f16(const float* x, void* y, int64_t n, int num_sms, cudaStream_t s);
+cudaError_t launch_gemm_f16(const void* W16, const void* X16, float* Y, int R, int K, int T, int num_sms,
+                            unsigned* status, cudaStream_t s);
 // looks up the device address of the no-alloc FFN's fixed scratch on device
 // `dev` (current) and caches it
 cudaError_t noalloc_setup(int dev);

@@ -18,6 +18,7 @@
 #pragma once
 
 #include "mq_device.cuh"
+#include "mq_tma.cuh"
 
 namespace mq {
 
@@ -151,23 +152,18 @@ __device__ __forceinline__ void stage_units_q8(const uint8_t* __restrict__ xq, i
     }
 }
 
-// From fp32 x: q8_0 quantization straight into the unit layout (the same
-// quantizer as the stand-alone kernel, hence bit-identical).  Optionally
-// also writes the q8_0 blocks to xq_out (2-byte aligned) and the code sums
-// to sumq_out.  Lane l loads values 4l..4l+3 of the unit (one 16-byte load
-// when x is 16-byte aligned).
-template <int NC>
-__device__ __forceinline__ void stage_units_x(const float* __restrict__ x, int K, UnitAct s,
-                                              uint8_t* __restrict__ xq_out, int32_t* sumq_out, int tid, int nthr)
+// From fp32 values: q8_0 quantization straight into the unit layout (the same
+// quantizer as the stand-alone kernel, hence bit-identical).  Optionally also
+// writes the q8_0 blocks to xq_out (2-byte aligned) and the code sums to
+// sumq_out.  `load(c, u)` gives this lane's values 4l..4l+3 of unit u of
+// column c (lane l = tid & 31).
+template <int NC, typename Loader>
+__device__ __forceinline__ void stage_units_f32(Loader load, int K, UnitAct s, uint8_t* __restrict__ xq_out,
+                                                int32_t* sumq_out, int tid, int nthr)
 {
     const int lane = tid & 31, warp = tid >> 5, nw = nthr >> 5;
     const int nq = K / kQK8, U = s.U;
     const int slot = lane >> 3, g = lane & 7;
-    const bool vec = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
-    auto load = [&](const float* p) {
-        return vec ? __ldg(reinterpret_cast<const float4*>(p))
-                   : make_float4(__ldg(p), __ldg(p + 1), __ldg(p + 2), __ldg(p + 3));
-    };
     auto amax8 = [](float4 v) {  // max |x| over the lane's 4 values, then its block's 8 lanes
         float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
@@ -192,12 +188,11 @@ __device__ __forceinline__ void stage_units_x(const float* __restrict__ x, int K
         qs = q0 + q1 + q2 + q3;
     };
     for (int c = 0; c < NC; ++c) {
-        const float* col = x + size_t(c) * K + 4 * lane;
         const UnitLaneOut out(s, c, lane);
         // two units per step, both loads first (a warp's last step may repeat its unit)
         for (int u = warp; u < U; u += 2 * nw) {
             const int u2 = u + nw < U ? u + nw : u;
-            const float4 va = load(col + size_t(u) * kUnitElems), vb = load(col + size_t(u2) * kUnitElems);
+            const float4 va = load(c, u), vb = load(c, u2);
             const float ma = amax8(va), mb = amax8(vb);
             const Q8Scale sa = q8_scale_of(ma), sb = q8_scale_of(mb);
             uint32_t ca, cb2;
@@ -230,6 +225,60 @@ __device__ __forceinline__ void stage_units_x(const float* __restrict__ x, int K
             }
         }
     }
+}
+
+// From fp32 x [NC][K] in global memory (one 16-byte load per lane and unit
+// when x is 16-byte aligned).
+template <int NC>
+__device__ __forceinline__ void stage_units_x(const float* __restrict__ x, int K, UnitAct s,
+                                              uint8_t* __restrict__ xq_out, int32_t* sumq_out, int tid, int nthr)
+{
+    const int lane = tid & 31;
+    const bool vec = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+    auto load = [&](int c, int u) {
+        const float* p = x + size_t(c) * K + size_t(u) * kUnitElems + 4 * lane;
+        return vec ? __ldg(reinterpret_cast<const float4*>(p))
+                   : make_float4(__ldg(p), __ldg(p + 1), __ldg(p + 2), __ldg(p + 3));
+    };
+    stage_units_f32<NC>(load, K, s, xq_out, sumq_out, tid, nthr);
+}
+
+// From fp32 values written earlier in the same launch as tagged records
+// (value bits in the low half, the writer's tag in the high half; record
+// c*ld + i holds element i of column c; rec 32-byte aligned, ld % 4 == 0).
+// A lane loads its four records with two 16-byte loads and reads again until
+// all four carry `tag`, bounded in time: one load both reads a value and
+// proves it written.  False (on every lane of the warp) after a timeout or
+// when another CTA raised the abort word; the staged values are then garbage.
+template <int NC>
+__device__ __forceinline__ bool stage_units_yrec(const uint64_t* __restrict__ rec, int ld, int K, UnitAct s,
+                                                 uint8_t* __restrict__ xq_out, uint32_t tag,
+                                                 const unsigned* abort_word, uint64_t limit_ns, int tid, int nthr)
+{
+    const int lane = tid & 31;
+    bool bad = false;
+    auto load = [&](int c, int u) {
+        const uint64_t* p = rec + size_t(c) * ld + size_t(u) * kUnitElems + 4 * lane;
+        uint64_t a0, a1, b0, b1;
+        ld_tagged2(p, a0, a1);
+        ld_tagged2(p + 2, b0, b1);
+        uint64_t t0 = 0;
+        for (uint32_t it = 0; !bad; ++it) {
+            const bool ok = uint32_t(a0 >> 32) == tag && uint32_t(a1 >> 32) == tag && uint32_t(b0 >> 32) == tag &&
+                            uint32_t(b1 >> 32) == tag;
+            if (ok) break;
+            if (it == 0)
+                t0 = global_timer_ns();
+            else if ((it & 15u) == 0 && (ld_relaxed_u32(abort_word) != 0 || global_timer_ns() - t0 > limit_ns))
+                bad = true;
+            ld_tagged2(p, a0, a1);
+            ld_tagged2(p + 2, b0, b1);
+        }
+        return make_float4(__uint_as_float(uint32_t(a0)), __uint_as_float(uint32_t(a1)), __uint_as_float(uint32_t(b0)),
+                           __uint_as_float(uint32_t(b1)));
+    };
+    stage_units_f32<NC>(load, K, s, xq_out, nullptr, tid, nthr);
+    return !__any_sync(0xffffffffu, bad);
 }
 
 // 16 bytes from shared memory (the ring's stages are written by the bulk-copy

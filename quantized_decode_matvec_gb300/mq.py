@@ -40,6 +40,7 @@ MQ_ERR_NOT_INITIALIZED = 6
 MQ_DEV_DESC_MISMATCH = 1
 MQ_DEV_DESC_ALIGN = 2
 MQ_DEV_TIMEOUT = 4
+MQ_DEV_ALIAS = 8
 MQ_VARIANT_AUTO = 0
 MQ_VARIANT_FORCE_REGISTER = 1
 MQ_FAULT_NONE = 0
@@ -53,6 +54,7 @@ MQ_MAX_K = 131072
 MQ_MAX_K_TIMES_NCOLS = 163840
 MQ_STEP_PDL = 1
 MQ_STEP_PERSISTENT = 2
+MQ_STEP_CHAINED = 4
 MQ_STEP_WORKSPACE_BYTES = 4352
 MQ_NOALLOC_HQ8_MAX_BYTES = 131072
 
@@ -107,6 +109,9 @@ _sig("mq_ffn_gate_up", c_i32, c_vp, c_i32, c_i32, c_i32, c_vp)
 _sig("mq_step", c_i32, c_vp, ctypes.POINTER(StepShape), c_vp)
 _sig("mq_step_workspace_bytes", c_i32, ctypes.POINTER(StepShape), ctypes.POINTER(ctypes.c_size_t))
 _sig("mq_ffn_gu_silu_down_noalloc", c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_vp)
+_sig("mq_dequant_q4K_f16", c_i32, c_vp, c_vp, c_i64, c_i64, c_vp)
+_sig("mq_convert_f32_f16", c_i32, c_vp, c_vp, c_i64, c_vp)
+_sig("mq_gemm_f16", c_i32, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_vp)
 _sig("mq_debug_block_sums_q4K_q8_0", c_i32, c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp)
 _sig("mq_debug_set_variant", c_i32, c_i32)
 _sig("mq_debug_set_fault", c_i32, c_i32)
@@ -116,7 +121,7 @@ EXPORTS = ["mq_status_string", "mq_abi_version", "mq_last_cuda_error", "mq_init"
            "mq_q4K_row_bytes", "mq_q8_0_bytes", "mq_quant_block_elems", "mq_quant_block_bytes",
            "mq_concat_rows_feasible", "mq_concat_rows", "mq_quantize_q8_0", "mq_check_mv_desc",
            "mq_matvec_q4K_q8_0", "mq_matvec_q4_0_q8_0", "mq_matvec_q8_0_q8_0", "mq_check_ffn_desc", "mq_ffn_gu_silu_down", "mq_ffn_gate_up", "mq_step", "mq_step_workspace_bytes",
-           "mq_ffn_gu_silu_down_noalloc",
+           "mq_ffn_gu_silu_down_noalloc", "mq_dequant_q4K_f16", "mq_convert_f32_f16", "mq_gemm_f16",
            "mq_debug_block_sums_q4K_q8_0", "mq_debug_set_variant", "mq_debug_set_fault"]
 
 
@@ -235,6 +240,18 @@ def mq_ffn_gu_silu_down_noalloc(W_gu: int, W_down: int, x: int, xq: int, y: int,
                                 y_ld: int, stream: int = 0) -> int:
     return _lib.mq_ffn_gu_silu_down_noalloc(c_vp(W_gu), c_vp(W_down), c_vp(x), c_vp(xq), c_vp(y), H, I, ncols,
                                             y_ld, c_vp(stream))
+
+
+def mq_dequant_q4K_f16(W: int, W16: int, rows: int, K: int, stream: int = 0) -> int:
+    return _lib.mq_dequant_q4K_f16(c_vp(W), c_vp(W16), rows, K, c_vp(stream))
+
+
+def mq_convert_f32_f16(x: int, y: int, n: int, stream: int = 0) -> int:
+    return _lib.mq_convert_f32_f16(c_vp(x), c_vp(y), n, c_vp(stream))
+
+
+def mq_gemm_f16(W16: int, X16: int, Y: int, R: int, K: int, T: int, stream: int = 0) -> int:
+    return _lib.mq_gemm_f16(c_vp(W16), c_vp(X16), c_vp(Y), R, K, T, c_vp(stream))
 
 
 def mq_debug_block_sums_q4K_q8_0(d_desc: int, rows: int, K: int, ncols: int, sumi: int, sumq: int,
@@ -405,24 +422,63 @@ def ffn_gu_silu_down_noalloc(W_gu, W_down, H: int, I: int, x=None, xq=None, y=No
     return y
 
 
+def dequant_q4K_f16(W, rows: int, K: int, out=None, stream=None):
+    """The resident f16 weight cache: uint8 q4_K [rows, K/256*144] -> f16 [rows, K]."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty((rows, K), dtype=torch.float16, device=W.device)
+    _check(mq_dequant_q4K_f16(_ptr(W), _ptr(out), rows, K, _stream(stream)), "mq_dequant_q4K_f16")
+    return out
+
+
+def convert_f32_f16(x, out=None, stream=None):
+    """fp32 tensor -> f16 tensor of the same shape (round to nearest-even)."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.float16, device=x.device)
+    _check(mq_convert_f32_f16(_ptr(x), _ptr(out), x.numel(), _stream(stream)), "mq_convert_f32_f16")
+    return out
+
+
+def gemm_f16(W16, X16, out=None, stream=None):
+    """Prefill GEMM on the tensor cores: Y [T, R] fp32 = X16 [T, K] . W16 [R, K]^T."""
+    torch = _torch()
+    R, K = W16.shape
+    T = X16.shape[0]
+    if out is None:
+        out = torch.empty((T, R), dtype=torch.float32, device=W16.device)
+    _check(mq_gemm_f16(_ptr(W16), _ptr(X16), _ptr(out), R, K, T, _stream(stream)), "mq_gemm_f16")
+    return out
+
+
 class StepBuffers:
     """Device buffers and the descriptor table of one layer stack for mq_step.
 
     weights: per layer dict with 'qkv' (concatenated q|k|v rows), 'o', 'gu', 'down'
-    (uint8 cuda tensors).  Inputs a/b/c and outputs are allocated here, one buffer
-    per layer, so a captured graph reads fresh inputs from the same addresses on
-    every replay.
+    (uint8 cuda tensors); a stack of FFN layers only (qkv_rows == o_rows == 0)
+    needs only 'gu' and 'down'.  Inputs a/b/c and outputs are allocated here, one
+    buffer per layer, so a captured graph reads fresh inputs from the same
+    addresses on every replay.
+
+    chained: build the descriptors of a decode chain (MQ_STEP_CHAINED): the o
+    projection reads the q|k|v output (its first o_K values), the FFN reads the
+    o output, and layer l+1's q|k|v reads layer l's FFN output; only layer 0's
+    first input (a[0], or c[0] for an FFN-only stack) comes from the caller.
     """
 
     def __init__(self, weights: List[Dict[str, "torch.Tensor"]], H: int, I: int, qkv_rows: int, o_rows: int,
-                 o_K: int, ncols: int = 1, device=None, debug: bool = False):
+                 o_K: int, ncols: int = 1, device=None, debug: bool = False, chained: bool = False):
         torch = _torch()
         self.n_layers = len(weights)
         self.H, self.I, self.qkv_rows, self.o_rows, self.o_K, self.ncols = H, I, qkv_rows, o_rows, o_K, ncols
-        dev = device if device is not None else weights[0]["qkv"].device
+        self.chained = chained
+        dev = device if device is not None else weights[0]["gu"].device
         self.device = dev
         n = self.n_layers
         self.weights = weights
+        if chained and ncols > 1 and ((qkv_rows and o_rows and qkv_rows != o_K) or (o_rows and o_rows != H)
+                                      or (qkv_rows and not o_rows and qkv_rows != H)):
+            raise ValueError("a chain of ncols > 1 needs each producer's rows equal to its consumer's K")
         # inputs [layer, ncols, K]: views of one buffer, so that a step's inputs
         # arrive in one host-to-device copy (each view starts on a 16-byte
         # boundary: H and o_K are multiples of 256)
@@ -443,23 +499,36 @@ class StepBuffers:
             self.xq_a = torch.zeros((n, ncols, H // 32 * 34), dtype=torch.uint8, device=dev)
             self.xq_b = torch.zeros((n, ncols, o_K // 32 * 34), dtype=torch.uint8, device=dev)
         table = (LayerDesc * n)()
+        prev = None  # the fp32 output the next phase of a chain reads
         for l, w in enumerate(weights):
-            table[l].qkv = mv_desc(w["qkv"], qkv_rows, H, self.y_qkv[l], x=self.a[l],
-                                   xq_out=self.xq_a[l] if debug else None, ncols=ncols, y_ld=qkv_rows)
-            table[l].o = mv_desc(w["o"], o_rows, o_K, self.y_o[l], x=self.b[l],
-                                 xq_out=self.xq_b[l] if debug else None, ncols=ncols, y_ld=o_rows)
-            table[l].ffn = ffn_desc(w["gu"], w["down"], H, I, self.h_q8[l], self.y_ffn[l], x=self.c[l],
+            if qkv_rows:
+                xa = prev if (chained and prev is not None) else self.a[l]
+                table[l].qkv = mv_desc(w["qkv"], qkv_rows, H, self.y_qkv[l], x=xa,
+                                       xq_out=self.xq_a[l] if debug else None, ncols=ncols, y_ld=qkv_rows)
+                prev = self.y_qkv[l]
+            if o_rows:
+                xb = prev if (chained and prev is not None) else self.b[l]
+                table[l].o = mv_desc(w["o"], o_rows, o_K, self.y_o[l], x=xb,
+                                     xq_out=self.xq_b[l] if debug else None, ncols=ncols, y_ld=o_rows)
+                prev = self.y_o[l]
+            xc = prev if (chained and prev is not None) else self.c[l]
+            table[l].ffn = ffn_desc(w["gu"], w["down"], H, I, self.h_q8[l], self.y_ffn[l], x=xc,
                                     ncols=ncols, y_ld=H)
-            for part in (table[l].qkv, table[l].o):
-                _check(mq_check_mv_desc(part), "mq_check_mv_desc")
+            prev = self.y_ffn[l]
+            for rows, part in ((qkv_rows, table[l].qkv), (o_rows, table[l].o)):
+                if rows:
+                    _check(mq_check_mv_desc(part), "mq_check_mv_desc")
             _check(mq_check_ffn_desc(table[l].ffn), "mq_check_ffn_desc")
         self.table_host = table
         self.table = upload_struct(bytes(table), dev)
-        # dependency words and h records of the persistent step (zeroed by mq_step itself)
-        nbytes = mq_step_workspace_bytes(StepShape(n, H, I, qkv_rows, o_rows, o_K, ncols, 0, None))
+        # dependency words and records of the persistent step (zeroed by mq_step itself)
+        nbytes = mq_step_workspace_bytes(StepShape(n, H, I, qkv_rows, o_rows, o_K, ncols,
+                                                   MQ_STEP_CHAINED if chained else 0, None))
         self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
 
     def shape(self, flags: int = 0) -> StepShape:
+        if self.chained:
+            flags |= MQ_STEP_CHAINED
         return StepShape(self.n_layers, self.H, self.I, self.qkv_rows, self.o_rows, self.o_K, self.ncols, flags,
                          _ptr(self.workspace))
 

@@ -177,16 +177,27 @@ def ffn_layer_input(case: FfnCase, layer: int, ncols: int | None = None) -> np.n
     return activation(case.H, nc, case.seed, tag, layer)
 
 
-def step_layer_weights(case: StepCase, layer: int) -> Dict[str, np.ndarray]:
-    """The six q4_K projections of one layer (q, k, v, o, ffn_gu, down)."""
+def step_layer_weights(case: StepCase, layer: int, d_scale: float = 1.0,
+                       dmin_scale: float | None = None) -> Dict[str, np.ndarray]:
+    """The six q4_K projections of one layer (q, k, v, o, ffn_gu, down).
+
+    d_scale and dmin_scale multiply the standard deviations of d and dmin
+    (1.0: the workloads' |N(0, 2e-3)| and |N(0, 1e-3)|; dmin_scale defaults to
+    d_scale).  A chain of layers with no normalization between them changes
+    its scale by a factor per projection that is proportional to them; with
+    the workloads' draws the weights' mean is d*31.5*7.5 - dmin*31.5 > 0, a
+    component common to every row that grows by about K times that mean per
+    projection.  A chain test takes dmin_scale = 15 * d_scale (mean about zero)
+    and a small d_scale, which keeps a short chain's values of order one."""
     H, I = case.H, case.I
+    kw = dict(d_sigma=2e-3 * d_scale, dmin_sigma=1e-3 * (d_scale if dmin_scale is None else dmin_scale))
     return {
-        "q": q4K_matrix(case.q_rows, H, case.seed, TAG_Q, layer),
-        "k": q4K_matrix(case.kv_rows, H, case.seed, TAG_K, layer),
-        "v": q4K_matrix(case.kv_rows, H, case.seed, TAG_V, layer),
-        "o": q4K_matrix(H, case.q_rows, case.seed, TAG_O, layer),
-        "gu": q4K_matrix(2 * I, H, case.seed, TAG_GU, layer),
-        "down": q4K_matrix(H, I, case.seed, TAG_DOWN, layer),
+        "q": q4K_matrix(case.q_rows, H, case.seed, TAG_Q, layer, **kw),
+        "k": q4K_matrix(case.kv_rows, H, case.seed, TAG_K, layer, **kw),
+        "v": q4K_matrix(case.kv_rows, H, case.seed, TAG_V, layer, **kw),
+        "o": q4K_matrix(H, case.q_rows, case.seed, TAG_O, layer, **kw),
+        "gu": q4K_matrix(2 * I, H, case.seed, TAG_GU, layer, **kw),
+        "down": q4K_matrix(H, I, case.seed, TAG_DOWN, layer, **kw),
     }
 
 

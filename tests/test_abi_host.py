@@ -156,3 +156,34 @@ def test_step_workspace_bytes(mq_lib):
     assert lib.mq_step_workspace_bytes(ctypes.byref(shape), None) == m.MQ_ERR_INVALID_ARG
     shape.I = 1000  # not a multiple of 256
     assert lib.mq_step_workspace_bytes(ctypes.byref(shape), ctypes.byref(n)) == m.MQ_ERR_SHAPE
+
+
+def test_chained_step_workspace_bytes(mq_lib):
+    m = mq_lib
+    # a chained step adds the output records of q|k|v, o and down: 8 bytes per output and column
+    base = 4352 + 18944 // 128 * 320
+    shape = m.StepShape(28, 3584, 18944, 4608, 3584, 3584, 1, m.MQ_STEP_PERSISTENT | m.MQ_STEP_CHAINED, None)
+    assert m.mq_step_workspace_bytes(shape) == base + 8 * (4608 + 3584 + 3584)
+    shape.ncols = 2
+    assert m.mq_step_workspace_bytes(shape) == 4352 + 2 * (18944 // 128) * 320 + 16 * (4608 + 3584 + 3584)
+    # an FFN-only chain: only down's outputs
+    shape = m.StepShape(24, 1024, 4864, 0, 0, 0, 1, m.MQ_STEP_PERSISTENT | m.MQ_STEP_CHAINED, None)
+    assert m.mq_step_workspace_bytes(shape) == 4352 + 4864 // 128 * 320 + 8 * 1024
+
+
+def test_step_shapes_on_the_host(mq_lib):
+    m = mq_lib
+    # a stack of FFN layers only (q|k|v and o left out) is a valid shape; o_K is then ignored
+    shape = m.StepShape(24, 1024, 4864, 0, 0, 0, 1, 0, None)
+    assert m.mq_step_workspace_bytes(shape) == 4352 + 4864 // 128 * 320
+    # negative rows and unknown flags are refused before any device work
+    shape.qkv_rows = -1
+    assert m.mq_step(0x1000, shape) == m.MQ_ERR_SHAPE
+    shape.qkv_rows = 0
+    shape.flags = 64
+    assert m.mq_step(0x1000, shape) == m.MQ_ERR_INVALID_ARG
+    # a projection that is present still needs a valid K
+    shape = m.StepShape(2, 1000, 4864, 512, 0, 0, 1, 0, None)
+    assert m.mq_step(0x1000, shape) == m.MQ_ERR_SHAPE
+    shape = m.StepShape(2, 1024, 4864, 0, 512, 1000, 1, 0, None)
+    assert m.mq_step(0x1000, shape) == m.MQ_ERR_SHAPE
