@@ -285,6 +285,28 @@ mq_status mq_step(const mq_layer_desc* d_layers, const mq_step_shape* h_shape, v
  * see the workspace's size: a smaller workspace is the caller's error. */
 mq_status mq_step_workspace_bytes(const mq_step_shape* h_shape, size_t* bytes);
 
+/* ---- more columns: the q4_K x q8_0 matmul on the tensor cores ("MMQ") ----------------
+ * "07 . R3 -- Small-model per-token overhead", section 5: past the decode
+ * matvec the engine's next work was MMQ, the quantized matmul for more
+ * tokens.  y[c][r] = sum over K of W[r] . q8_0(x)[c] for 1..MQ_MMQ_MAX_NCOLS
+ * columns (meant for 9 and more; the decode kernels serve 1..8), the same
+ * descriptor and result as mq_matvec_q4K_q8_0: the q8_0 codes and every
+ * 32-element sub-block's integer sum are exact (binary16 operands of the
+ * tensor-core MMA, fp32 accumulation of integers below 2^24), and the scales
+ * are applied per sub-block in fp32.  Float results match the oracle within
+ * the same tolerance as the decode kernels (not bit for bit: the order of the
+ * float operations differs).
+ *   workspace: caller-owned device memory, 128-byte aligned, of at least
+ *   mq_mmq_workspace_bytes(rows, K, ncols) bytes (the activation laid out for
+ *   the MMA, and partial sums when a matrix has few 128-row tiles); two calls
+ *   that overlap on the GPU must not share it.
+ * Three launches at most on `stream` (activation, matmul, partial sums).
+ * MQ_ERR_INVALID_ARG for a workspace smaller than needed. */
+#define MQ_MMQ_MAX_NCOLS 64
+mq_status mq_mmq_workspace_bytes(int32_t rows, int32_t K, int32_t ncols, size_t* bytes);
+mq_status mq_mmq_q4K_q8_0(const mq_mv_desc* d_desc, int32_t rows, int32_t K, int32_t ncols, void* workspace,
+                          size_t ws_bytes, void* stream);
+
 /* ---- prefill: the resident f16 weight cache and the tensor-core GEMM -----------------
  * "07 . R3 -- Small-model per-token overhead", section 1: 7B prefill at 2K
  * tokens runs a half-precision tensor-core GEMM over a resident f16 copy of

@@ -17,6 +17,7 @@ cudaError_t set_step_attributes(int max_smem);
 cudaError_t set_wring_attributes(int max_smem);
 cudaError_t set_ring_cols_attributes(int max_smem);
 cudaError_t set_gemm_attributes(int max_smem);
+cudaError_t set_mmq_attributes(int max_smem);
 void plan_ring(MvPlan& q, int64_t units, int kind, int nc, const DeviceInfo& dev, int64_t unit_bytes,
                bool allow_cols);
 }  // namespace mq
@@ -356,6 +357,7 @@ cudaError_t set_kernel_attributes(int max_smem)
     if (e == cudaSuccess) e = set_wring_attributes(max_smem);
     if (e == cudaSuccess) e = set_ring_cols_attributes(max_smem);
     if (e == cudaSuccess) e = set_gemm_attributes(max_smem);
+    if (e == cudaSuccess) e = set_mmq_attributes(max_smem);
     return e;
 }
 
@@ -706,6 +708,42 @@ mq_status mq_step(const mq_layer_desc* d_layers, const mq_step_shape* h, void* s
         if (e != cudaSuccess) return cuda_fail(e);
     }
     return MQ_OK;
+}
+
+static mq_status check_mmq_shape(int64_t rows, int64_t K, int64_t ncols)
+{
+    if (rows < 0 || K <= 0 || ncols < 0 || K % 256 || ncols > MQ_MMQ_MAX_NCOLS) return MQ_ERR_SHAPE;
+    if (K > MQ_MAX_K || rows > INT32_MAX) return MQ_ERR_UNSUPPORTED;
+    return MQ_OK;
+}
+
+mq_status mq_mmq_workspace_bytes(int32_t rows, int32_t K, int32_t ncols, size_t* bytes)
+{
+    if (!bytes) return MQ_ERR_INVALID_ARG;
+    mq_status st = check_mmq_shape(rows, K, ncols);
+    if (st != MQ_OK) return st;
+    const mq::DeviceInfo* dev = nullptr;
+    if ((st = current_dev(&dev)) != MQ_OK) return st;
+    *bytes = (rows == 0 || ncols == 0) ? 0 : mq::plan_mmq(rows, K, ncols, dev->num_sms, dev->max_smem_optin).ws_bytes;
+    return MQ_OK;
+}
+
+mq_status mq_mmq_q4K_q8_0(const mq_mv_desc* d_desc, int32_t rows, int32_t K, int32_t ncols, void* workspace,
+                          size_t ws_bytes, void* stream)
+{
+    mq_status st = check_mmq_shape(rows, K, ncols);
+    if (st != MQ_OK) return st;
+    if (rows == 0 || ncols == 0) return MQ_OK;
+    if (!d_desc || !workspace) return MQ_ERR_INVALID_ARG;
+    if (!aligned(d_desc, 8) || !aligned(workspace, 128)) return MQ_ERR_ALIGN;
+    const mq::DeviceInfo* dev = nullptr;
+    if ((st = current_dev(&dev)) != MQ_OK) return st;
+    const mq::MmqPlan p = mq::plan_mmq(rows, K, ncols, dev->num_sms, dev->max_smem_optin);
+    if (p.stages < 2) return MQ_ERR_UNSUPPORTED;
+    if (ws_bytes < p.ws_bytes) return MQ_ERR_INVALID_ARG;
+    cudaError_t e = mq::launch_mmq(d_desc, rows, K, ncols, p, workspace, dev->num_sms, dev->status,
+                                   as_stream(stream));
+    return e == cudaSuccess ? MQ_OK : cuda_fail(e);
 }
 
 mq_status mq_dequant_q4K_f16(const void* W, void* W16, int64_t rows, int64_t K, void* stream)

@@ -7,15 +7,16 @@
 //   Y[t][r] = sum_k X[t][k] * W[r][k]      X f16 [T][K], W f16 [R][K], Y fp32 [T][R]
 //
 // with fp32 accumulation in tensor memory.  One CTA per SM walks output tiles
-// of 128 weight rows x 256 tokens (persistent, static round robin; tiles that
+// of 128 weight rows x BN tokens, BN = 256 (or 128 where that fills the last
+// wave of CTAs clearly better), persistent, static round robin; tiles that
 // share a weight block run at the same time, so each block comes from HBM
-// about once and from L2 for the other token tiles).  Per CTA:
+// about once and from L2 for the other token tiles.  Per CTA:
 //
-// * warp 0, one lane: TMA loads of 128x64 weight and 256x64 activation tiles
+// * warp 0, one lane: TMA loads of 128x64 weight and BNx64 activation tiles
 //   (128-byte swizzle) into a ring of shared-memory stages, tracked by
 //   mbarriers;
-// * warp 1: allocates 512 TMEM columns (two 128x256 fp32 accumulators); one
-//   lane issues four tcgen05.mma (M=128, N=256, K=16) per stage and commits
+// * warp 1: allocates 2*BN TMEM columns (two 128xBN fp32 accumulators); one
+//   lane issues four tcgen05.mma (M=128, N=BN, K=16) per stage and commits
 //   each stage back to the producer, and each finished tile to the epilogue;
 // * warps 2..5: the epilogue reads its 32 TMEM lanes (32 weight rows) with
 //   tcgen05.ld and stores fp32 Y, coalesced across the rows, while the MMAs
@@ -33,15 +34,20 @@
 namespace mq {
 
 constexpr int kGemmBM = 128;                          // weight rows per tile (TMEM lanes)
-constexpr int kGemmBN = 256;                          // tokens per tile (accumulator columns)
 constexpr int kGemmBK = 64;                           // f16 per 128-byte swizzled row
-constexpr int kGemmStages = 4;
 constexpr int kGemmATile = kGemmBM * kGemmBK * 2;     // 16 KB
-constexpr int kGemmBTile = kGemmBN * kGemmBK * 2;     // 32 KB
-constexpr int kGemmStage = kGemmATile + kGemmBTile;   // 48 KB
 constexpr int kGemmThreads = 192;
-constexpr uint32_t kGemmTmemCols = 512;
-constexpr int kGemmSmem = kGemmStages * kGemmStage + 1024;  // + alignment slack
+
+// tokens per tile BN (256, or 128 where 256-token tiles would leave the last
+// wave of CTAs mostly idle); a stage holds one A and one B tile
+template <int BN>
+struct GemmTile {
+    static constexpr int kBTile = BN * kGemmBK * 2;
+    static constexpr int kStage = kGemmATile + kBTile;
+    static constexpr int kStages = BN == 256 ? 4 : 6;
+    static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators
+    static constexpr int kSmem = kStages * kStage + 1024;  // + alignment slack
+};
 
 struct GemmArgs {
     int R, K, T;
@@ -49,10 +55,14 @@ struct GemmArgs {
     uint64_t limit_ns;
 };
 
+template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_f16_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                     float* __restrict__ Y, const GemmArgs a, unsigned* status)
 {
+    using G = GemmTile<BN>;
+    constexpr int kGemmBN = BN, kGemmStages = G::kStages, kGemmStage = G::kStage;
+    constexpr uint32_t kGemmTmemCols = G::kTmemCols;
     extern __shared__ uint8_t gsm_raw[];
     __shared__ __align__(8) uint64_t full[kGemmStages], empty[kGemmStages], accf[2], acce[2];
     __shared__ uint32_t tmem_base;
@@ -156,8 +166,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         int tl = 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tl) {
             const int b = tl & 1;
-            const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&accf[b], uint32_t(tl / 2) & 1u, a.limit_ns));
-            if (!ok || abort_flag) {
+            // one decision for the whole warp
+            const bool ok = __all_sync(0xffffffffu,
+                                       mbar_wait_bounded(&accf[b], uint32_t(tl / 2) & 1u, a.limit_ns) && !abort_flag);
+            if (!ok) {
                 if (lane == 0) abort_flag = 1;
                 break;
             }
@@ -226,26 +238,46 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t K, int box
 cudaError_t set_gemm_attributes(int max_smem)
 {
     (void)max_smem;
-    return cudaFuncSetAttribute(gemm_f16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+    cudaError_t e = cudaFuncSetAttribute(gemm_f16_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         GemmTile<256>::kSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemm_f16_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 GemmTile<128>::kSmem);
+    return e;
+}
+
+// the share of the CTAs' tile slots that holds a tile: tiles / (waves * grid)
+static double wave_use(int64_t tiles, int num_sms)
+{
+    const int64_t grid = tiles < num_sms ? tiles : num_sms;
+    const int64_t waves = (tiles + grid - 1) / grid;
+    return double(tiles) / double(waves * grid);
 }
 
 // returns cudaErrorInvalidValue when the tensor maps cannot be built
 cudaError_t launch_gemm_f16(const void* W16, const void* X16, float* Y, int R, int K, int T, int num_sms,
                             unsigned* status, cudaStream_t s)
 {
+    const int m_tiles = (R + kGemmBM - 1) / kGemmBM;
+    // 256-token tiles unless 128-token tiles fill the CTAs' waves clearly better
+    const int64_t t256 = int64_t(m_tiles) * ((T + 255) / 256), t128 = int64_t(m_tiles) * ((T + 127) / 128);
+    const int BN = wave_use(t128, num_sms) > wave_use(t256, num_sms) + 0.05 ? 128 : 256;
     CUtensorMap tmW, tmX;
-    if (!make_map(&tmW, W16, R, K, kGemmBM) || !make_map(&tmX, X16, T, K, kGemmBN)) return cudaErrorInvalidValue;
+    if (!make_map(&tmW, W16, R, K, kGemmBM) || !make_map(&tmX, X16, T, K, BN)) return cudaErrorInvalidValue;
     GemmArgs a;
     a.R = R;
     a.K = K;
     a.T = T;
-    a.m_tiles = (R + kGemmBM - 1) / kGemmBM;
-    a.n_tiles = (T + kGemmBN - 1) / kGemmBN;
+    a.m_tiles = m_tiles;
+    a.n_tiles = (T + BN - 1) / BN;
     a.k_steps = K / kGemmBK;
     a.limit_ns = uint64_t(fault_policy() == FAULT_NONE ? 2000 : 50) * 1000000ull;
     const int ntiles = a.m_tiles * a.n_tiles;
     const int grid = ntiles < num_sms ? ntiles : num_sms;
-    gemm_f16_kernel<<<grid, kGemmThreads, kGemmSmem, s>>>(tmW, tmX, Y, a, status);
+    if (BN == 256)
+        gemm_f16_kernel<256><<<grid, kGemmThreads, GemmTile<256>::kSmem, s>>>(tmW, tmX, Y, a, status);
+    else
+        gemm_f16_kernel<128><<<grid, kGemmThreads, GemmTile<128>::kSmem, s>>>(tmW, tmX, Y, a, status);
     return cudaGetLastError();
 }
 

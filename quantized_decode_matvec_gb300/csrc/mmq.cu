@@ -1,0 +1,527 @@
+// mmq.cu -- the q4_K x q8_0 matmul for 9..64 activation columns on the 5th-
+// generation tensor cores ("07 . R3 -- Small-model per-token overhead",
+// section 5: past the decode matvec, the "MMQ" work for more tokens).
+//
+// Beyond a few columns the matvec becomes a contraction, and the dp4a work of
+// the decode kernels grows with the columns while the weight stream does not.
+// Here the integer dot products run on tcgen05.mma of kind::f16 with operands
+// that are exact in binary16:
+//   A = the weights' 4-bit quants q (0..15; the high nibbles as 16*q),
+//   B = the activation's q8_0 codes (-127..127),
+// so every product is an integer and every 32-element sub-block sum
+//   S[r][j][c] = sum over the sub-block of q * code   (|S| < 2^20)
+// is exact in the fp32 accumulator.  Each sub-block has its own accumulator
+// slot in tensor memory (the weights' scale sc_j and the activation's dq_j
+// change every 32 elements), and the epilogue applies the scales per
+// sub-block as the decode kernels do:
+//   y[r][c] += d*sc_j * (dq_jc * S) - dmin*m_j * (dq_jc * sumq_jc)
+//
+// Launches: (1) the activation is quantized to q8_0 (the same quantizer as
+// every other path) and laid out for the MMA: codes as f16 in the 128-byte-
+// swizzled K-major image of each 256-element step, with (dq, dq*sumq) per
+// block and column; (2) the matmul; (3) for matrices with few row tiles, the
+// K range is split over CTAs and a fixed-order sum combines the partials.
+//
+// The matmul CTA (persistent over its work items, 10 warps):
+//   warp 0     bulk copies (TMA) of each step's 128 weight rows (144 bytes
+//              each), the step's activation image and its scales, into a ring
+//              of stages
+//   warp 1     TMEM allocation; one lane issues two MMAs (M=128, N=ncols
+//              rounded up to 16, K=16) per sub-block into the sub-block's slot
+//   warps 2-5  convert each row's quants to the f16 A image (thread = row)
+//   warps 6-9  epilogue (thread = row = TMEM lane): per sub-block, read the
+//              slot, free it, apply the scales into fp32 registers
+// Every wait is bounded in time; a timeout records MQ_DEV_TIMEOUT and the
+// roles stop (the producer waits, bounded, for its copies in flight).
+#include <cuda_fp16.h>
+
+#include "mq_job.cuh"
+#include "mq_umma.cuh"
+
+namespace mq {
+
+constexpr int kMmqBM = 128;                          // weight rows per tile
+constexpr int kMmqThreads = 320;
+constexpr int kMmqAtom = kMmqBM * 128;               // one 128 x 64 f16 swizzled atom: 16 KB
+constexpr int kMmqAImage = 4 * kMmqAtom;             // 256 K of A: 64 KB
+constexpr int kMmqRaw = kMmqBM * kQ4KBytes;          // 128 rows x 144 bytes
+constexpr uint32_t kMmqTmemCols = 512;
+
+__host__ __device__ constexpr int mmq_np(int nc) { return (nc + 15) / 16 * 16; }
+// stage: raw weights | activation image (4 atoms of NP rows x 128 B) | scales [8][NP] (dq, dq*sumq)
+__host__ __device__ constexpr int mmq_stage_bytes(int NP) { return kMmqRaw + NP * 512 + 8 * NP * 8; }
+__host__ __device__ constexpr int mmq_round1k(int b) { return (b + 1023) / 1024 * 1024; }
+
+struct MmqArgs {
+    int R, K, ncols;
+    int m_tiles, ksplit, nkb;
+    int stages;
+    int stage_bytes;          // 1024-aligned
+    const uint8_t* bimg;      // activation images, nkb x NP*512 bytes
+    const float2* sc;         // [K/32][NP] (dq, dq*sumq)
+    float* part;              // [ksplit][ncols][R] partial sums (ksplit > 1)
+    uint64_t limit_ns;
+};
+
+// ---- (1) activation: q8_0, then the MMA image -----------------------------------------
+// One warp per (column, 32-block); lane l is element 32J + l.
+template <int NP>
+__global__ void mmq_stage_act_kernel(const mq_mv_desc* __restrict__ desc, int rows_h, int K_h, int nc_h,
+                                     uint8_t* __restrict__ bimg, float2* __restrict__ sc, unsigned* status)
+{
+    const MvJob j = read_job<KIND_MV>(desc);
+    const unsigned bad = check_job(j, rows_h, K_h, nc_h);
+    if (bad) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(status, bad);
+        return;
+    }
+    const int lane = threadIdx.x & 31;
+    const int nq = K_h / kQK8;
+    const int64_t nwarps = int64_t(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t w = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); w < int64_t(NP) * nq;
+         w += nwarps) {
+        const int c = int(w / nq), J = int(w - int64_t(c) * nq);
+        int q = 0;
+        float dq = 0.0f;
+        if (c < nc_h) {
+            if (j.x) {
+                float d;
+                q = q8_quantize_lane(j.x[size_t(c) * K_h + size_t(J) * kQK8 + lane], &d);
+                const __half dh = __float2half_rn(d);
+                dq = __half2float(dh);
+                if (j.xq_out) {  // the q8_0 blocks too, for the bit-exact check
+                    uint8_t* ob = j.xq_out + (size_t(c) * nq + J) * kQ8Bytes;
+                    if (lane == 0) *reinterpret_cast<uint16_t*>(ob) = __half_as_ushort(dh);
+                    ob[2 + lane] = uint8_t(int8_t(q));
+                }
+            } else {
+                const uint8_t* blk = j.xq + (size_t(c) * nq + J) * kQ8Bytes;
+                dq = __half2float(__ushort_as_half(uint16_t(blk[0] | (blk[1] << 8))));
+                q = int(int8_t(blk[2 + lane]));
+            }
+        }
+        const int sq = __reduce_add_sync(0xffffffffu, q);
+        const int k = J * kQK8 + lane, kb = k >> 8, a = (k >> 6) & 3, e = k & 63;
+        const size_t off = size_t(kb) * (NP * 512) + size_t(a) * (NP * 128) + size_t(c) * 128 +
+                           size_t(((e >> 3) ^ (c & 7)) << 4) + size_t(e & 7) * 2;
+        *reinterpret_cast<__half*>(bimg + off) = __int2half_rn(q);
+        if (lane == 0) sc[size_t(J) * NP + c] = make_float2(dq, dq * float(sq));
+    }
+}
+
+// ---- (2) the matmul ------------------------------------------------------------------------
+// quants -> f16 pairs: bytes (b0, b1) of w selected by sel into the two
+// halves, the low nibbles as 1024 + n or the high nibbles as 1024 + 16n
+// (exact binary16), minus 1024
+__device__ __forceinline__ uint32_t nib_pair(uint32_t w, uint32_t sel, uint32_t mask)
+{
+    uint32_t u = (__byte_perm(w, 0u, sel) & mask) | 0x64006400u;
+    __half2 h = *reinterpret_cast<__half2*>(&u);
+    h = __hsub2(h, __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 16 consecutive fp32 columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
+{
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <int NP>
+__global__ void __launch_bounds__(kMmqThreads, 1)
+    mmq_kernel(const mq_mv_desc* __restrict__ desc, const MmqArgs a, unsigned* status)
+{
+    constexpr int NSLOT = int(kMmqTmemCols) / NP;  // accumulator slots of NP columns
+    extern __shared__ uint8_t msm_raw[];
+    __shared__ __align__(8) uint64_t full[4], empty[4], a_full, a_free, slot_full[32], slot_free[32];
+    __shared__ uint32_t tmem_base;
+    __shared__ volatile int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t raw_addr = smem_u32(msm_raw);
+    uint8_t* const sm = msm_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    uint8_t* const aimg = sm;                 // 64 KB, 1024-aligned
+    uint8_t* const stages = sm + kMmqAImage;  // a.stages x a.stage_bytes
+    {
+        // the activation launch checked the descriptor too; a bad one stops this launch as well
+        const unsigned bad = check_job(read_job<KIND_MV>(desc), a.R, a.K, a.ncols);
+        if (bad) return;
+    }
+    const uint8_t* W = static_cast<const uint8_t*>(desc->W);
+    float* Y = desc->y;
+    const int y_ld = desc->y_ld;
+    const size_t row_bytes = size_t(a.nkb) * kQ4KBytes;
+    const int nitems = a.m_tiles * a.ksplit;
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int s = 0; s < a.stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 4 + 1 + 4);  // converter warps, the MMA commit, epilogue warps
+        }
+        mbar_init(&a_full, 4);
+        mbar_init(&a_free, 1);
+        for (int i = 0; i < NSLOT; ++i) {
+            mbar_init(&slot_full[i], 1);
+            mbar_init(&slot_free[i], 4);
+        }
+        fence_barrier_init();
+    }
+    if (warp == 1) tmem_alloc(&tmem_base, kMmqTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+
+    // the SB range of work item it: tile m, K split ks
+    auto item = [&](int it, int& m, int& kb0, int& kb1) {
+        m = it / a.ksplit;
+        const int ks = it - m * a.ksplit;
+        kb0 = int(int64_t(ks) * a.nkb / a.ksplit);
+        kb1 = int(int64_t(ks + 1) * a.nkb / a.ksplit);
+    };
+
+    if (warp == 0) {
+        // ---- producer: every lane issues row copies; lane 0 the barrier and the activation
+        int g = 0;
+        for (int it = blockIdx.x; it < nitems; it += gridDim.x) {
+            if (__shfl_sync(0xffffffffu, abort_flag, 0)) break;  // one decision for the whole warp
+            int m, kb0, kb1;
+            item(it, m, kb0, kb1);
+            const int r0 = m * kMmqBM, nrow = min(kMmqBM, a.R - r0);
+            for (int kb = kb0; kb < kb1; ++kb, ++g) {
+                const int s = g % a.stages;
+                bool ok = true;
+                if (lane == 0 && g >= a.stages)
+                    ok = mbar_wait_bounded(&empty[s], uint32_t(g / a.stages - 1) & 1u, a.limit_ns);
+                if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
+                    if (lane == 0) abort_flag = 1;
+                    break;
+                }
+                uint8_t* st = stages + size_t(s) * a.stage_bytes;
+                if (lane == 0)
+                    mbar_arrive_expect_tx(&full[s], uint32_t(nrow * kQ4KBytes + NP * 512 + 8 * NP * 8));
+                __syncwarp();
+                for (int r = lane; r < nrow; r += 32)
+                    bulk_copy_g2s(st + r * kQ4KBytes, W + size_t(r0 + r) * row_bytes + size_t(kb) * kQ4KBytes,
+                                  kQ4KBytes, &full[s]);
+                if (lane == 0) {
+                    bulk_copy_g2s(st + kMmqRaw, a.bimg + size_t(kb) * (NP * 512), NP * 512, &full[s]);
+                    bulk_copy_g2s(st + kMmqRaw + NP * 512, a.sc + size_t(kb) * 8 * NP, 8 * NP * 8, &full[s]);
+                }
+            }
+        }
+        if (lane == 0)  // copies still in flight land before the CTA exits
+            for (int j = g > a.stages ? g - a.stages : 0; j < g; ++j)
+                (void)mbar_wait_bounded(&full[j % a.stages], uint32_t(j / a.stages) & 1u, a.limit_ns);
+    } else if (warp == 1) {
+        // ---- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = umma_idesc_f16_f32(kMmqBM, NP);
+            const uint32_t aaddr = smem_u32(aimg);
+            int g = 0, v = 0;  // steps and slot uses so far
+            for (int it = blockIdx.x; it < nitems && !abort_flag; it += gridDim.x) {
+                int m, kb0, kb1;
+                item(it, m, kb0, kb1);
+                for (int kb = kb0; kb < kb1; ++kb, ++g) {
+                    const int s = g % a.stages;
+                    if (!mbar_wait_bounded(&a_full, uint32_t(g) & 1u, a.limit_ns) ||
+                        !mbar_wait_bounded(&full[s], uint32_t(g / a.stages) & 1u, a.limit_ns)) {
+                        abort_flag = 1;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t baddr = smem_u32(stages + size_t(s) * a.stage_bytes + kMmqRaw);
+                    bool ok = true;
+                    for (int j = 0; j < 8; ++j, ++v) {
+                        const int slot = v % NSLOT;
+                        if (v >= NSLOT &&
+                            !mbar_wait_bounded(&slot_free[slot], uint32_t(v / NSLOT - 1) & 1u, a.limit_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t koff = uint32_t(j & 1) * 64;
+                        const uint32_t ab = aaddr + uint32_t(j >> 1) * kMmqAtom + koff;
+                        const uint32_t bb = baddr + uint32_t(j >> 1) * (NP * 128) + koff;
+                        const uint32_t d = tmem + uint32_t(slot * NP);
+                        umma_f16(d, umma_desc_sw128(ab), umma_desc_sw128(bb), idesc, false);
+                        umma_f16(d, umma_desc_sw128(ab + 32), umma_desc_sw128(bb + 32), idesc, true);
+                        umma_commit(&slot_full[slot]);
+                    }
+                    if (!ok) {
+                        abort_flag = 1;
+                        break;
+                    }
+                    umma_commit(&a_free);    // the A image may be rewritten
+                    umma_commit(&empty[s]);  // this step's activation image has been read
+                }
+                if (abort_flag) break;
+            }
+            if (v > 0)  // the last MMAs complete before TMEM is freed
+                (void)mbar_wait_bounded(&slot_full[(v - 1) % NSLOT], uint32_t((v - 1) / NSLOT) & 1u, a.limit_ns);
+        }
+    } else if (warp < 6) {
+        // ---- converters: thread = row r of the tile
+        const int r = (warp & 3) * 32 + lane;
+        const uint32_t arow = smem_u32(aimg) + uint32_t(r) * 128;
+        const uint32_t sw = uint32_t(r & 7);
+        int g = 0;
+        for (int it = blockIdx.x; it < nitems; it += gridDim.x) {
+            int m, kb0, kb1;
+            item(it, m, kb0, kb1);
+            const bool live = m * kMmqBM + r < a.R;
+            for (int kb = kb0; kb < kb1; ++kb, ++g) {
+                const int s = g % a.stages;
+                bool ok = mbar_wait_bounded(&full[s], uint32_t(g / a.stages) & 1u, a.limit_ns);
+                if (ok && g > 0) ok = mbar_wait_bounded(&a_free, uint32_t(g - 1) & 1u, a.limit_ns);
+                if (!__all_sync(0xffffffffu, ok && !abort_flag)) {
+                    if (lane == 0) abort_flag = 1;
+                    it = nitems;  // stop
+                    break;
+                }
+                const uint8_t* raw = stages + size_t(s) * a.stage_bytes + size_t(r) * kQ4KBytes;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    // quant bytes 32cc..32cc+31: sub-block 2cc (low nibbles), 2cc+1 (high nibbles)
+                    uint4 q0 = make_uint4(0, 0, 0, 0), q1 = q0;
+                    if (live) {
+                        q0 = *reinterpret_cast<const uint4*>(raw + 16 + 32 * cc);
+                        q1 = *reinterpret_cast<const uint4*>(raw + 32 + 32 * cc);
+                    }
+                    const uint32_t wq[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                    const uint32_t atom = arow + uint32_t(cc) * kMmqAtom;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        // chunk c: elements 8c..8c+7 of the atom's 64: low nibbles of bytes
+                        // 8c.. (c < 4) or high nibbles of bytes 8(c-4).. (c >= 4)
+                        const uint32_t m4 = c < 4 ? 0x000F000Fu : 0x00F000F0u;
+                        const uint32_t w0 = wq[2 * (c & 3)], w1 = wq[2 * (c & 3) + 1];
+                        sts128(atom + ((uint32_t(c) ^ sw) << 4), nib_pair(w0, 0x4140u, m4), nib_pair(w0, 0x4342u, m4),
+                               nib_pair(w1, 0x4140u, m4), nib_pair(w1, 0x4342u, m4));
+                    }
+                }
+                fence_proxy_async_smem();  // the A image is read by the tensor cores
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&a_full);
+                    mbar_arrive(&empty[s]);
+                }
+            }
+        }
+    } else {
+        // ---- epilogue: thread = TMEM lane = row r of the tile
+        const int q = warp & 3, r = q * 32 + lane;
+        const uint32_t lane_base = uint32_t(q * 32) << 16;
+        int g = 0, v = 0;
+        bool stop = false;
+        for (int it = blockIdx.x; it < nitems && !stop; it += gridDim.x) {
+            int m, kb0, kb1;
+            item(it, m, kb0, kb1);
+            const int row = m * kMmqBM + r;
+            float y[NP];
+#pragma unroll
+            for (int c = 0; c < NP; ++c) y[c] = 0.0f;
+            for (int kb = kb0; kb < kb1 && !stop; ++kb, ++g) {
+                const int s = g % a.stages;
+                const uint8_t* st = stages + size_t(s) * a.stage_bytes;
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[s], uint32_t(g / a.stages) & 1u, a.limit_ns))) {
+                    stop = true;
+                    break;
+                }
+                // this row's scales from its super-block header (rows past the end: zeros)
+                float ds[8], dm[8];
+                {
+                    uint4 hd = make_uint4(0, 0, 0, 0);
+                    if (row < a.R) hd = *reinterpret_cast<const uint4*>(st + size_t(r) * kQ4KBytes);
+                    const float d = __half2float(__ushort_as_half(uint16_t(hd.x)));
+                    const float dmin = __half2float(__ushort_as_half(uint16_t(hd.x >> 16)));
+                    const uint32_t S[3] = {hd.y, hd.z, hd.w};
+                    auto byte = [&](int i) { return int((S[i >> 2] >> (8 * (i & 3))) & 0xffu); };
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) {
+                        int scv, mv;
+                        if (jj < 4) {
+                            scv = byte(jj) & 63;
+                            mv = byte(jj + 4) & 63;
+                        } else {
+                            scv = (byte(jj + 4) & 15) | ((byte(jj - 4) >> 6) << 4);
+                            mv = (byte(jj + 4) >> 4) | ((byte(jj) >> 6) << 4);
+                        }
+                        // odd sub-blocks come from the high nibbles, taken as 16*q
+                        ds[jj] = d * float(scv) * ((jj & 1) ? 0.0625f : 1.0f);
+                        dm[jj] = dmin * float(mv);
+                    }
+                }
+                const float4* scj = reinterpret_cast<const float4*>(st + kMmqRaw + NP * 512);
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj, ++v) {
+                    const int slot = v % NSLOT;
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait_bounded(&slot_full[slot], uint32_t(v / NSLOT) & 1u, a.limit_ns))) {
+                        stop = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    float S[NP];
+#pragma unroll
+                    for (int c0 = 0; c0 < NP; c0 += 16) {
+                        float t[16];
+                        tmem_ld16(tmem + lane_base + uint32_t(slot * NP + c0), t);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) S[c0 + i] = t[i];
+                    }
+                    tmem_ld_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&slot_free[slot]);
+#pragma unroll
+                    for (int c = 0; c < NP; c += 2) {
+                        const float4 p = scj[(jj * NP + c) >> 1];  // (dq, dq*sumq) of columns c, c+1
+                        y[c] = fmaf(-dm[jj], p.y, fmaf(ds[jj], p.x * S[c], y[c]));
+                        y[c + 1] = fmaf(-dm[jj], p.w, fmaf(ds[jj], p.z * S[c + 1], y[c + 1]));
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+            }
+            if (stop) break;
+            if (row < a.R) {
+                const int ks = it - m * a.ksplit;
+                if (a.ksplit == 1) {
+#pragma unroll
+                    for (int c = 0; c < NP; ++c)
+                        if (c < a.ncols) Y[size_t(c) * y_ld + row] = y[c];
+                } else {
+#pragma unroll
+                    for (int c = 0; c < NP; ++c)
+                        if (c < a.ncols) a.part[(size_t(ks) * a.ncols + c) * a.R + row] = y[c];
+                }
+            }
+        }
+        if (stop && lane == 0) abort_flag = 1;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (abort_flag && threadIdx.x == 0) atomicOr(status, MQ_DEV_TIMEOUT);
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kMmqTmemCols);
+    }
+}
+
+// ---- (3) fixed-order sum of the K-split partials ---------------------------------------------
+__global__ void mmq_reduce_kernel(const mq_mv_desc* __restrict__ desc, const float* __restrict__ part, int ksplit,
+                                  int R, int ncols)
+{
+    float* Y = desc->y;
+    const int y_ld = desc->y_ld;
+    const int64_t n = int64_t(ncols) * R;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x) {
+        const int c = int(i / R), r = int(i - int64_t(c) * R);
+        float s = 0.0f;
+        for (int ks = 0; ks < ksplit; ++ks) s += part[(size_t(ks) * ncols + c) * R + r];
+        Y[size_t(c) * y_ld + r] = s;
+    }
+}
+
+// ---- host side ----------------------------------------------------------------------------------
+MmqPlan plan_mmq(int rows, int K, int ncols, int num_sms, int max_smem)
+{
+    MmqPlan p{};
+    p.np = mmq_np(ncols);
+    p.nkb = K / kQK;
+    p.m_tiles = (rows + kMmqBM - 1) / kMmqBM;
+    int ks = num_sms / p.m_tiles;
+    p.ksplit = ks < 1 ? 1 : (ks > p.nkb ? p.nkb : ks);
+    p.stage_bytes = mmq_round1k(mmq_stage_bytes(p.np));
+    int st = (max_smem - 1024 - 256 - kMmqAImage) / p.stage_bytes;
+    p.stages = st > 4 ? 4 : st;
+    p.smem = 1024 + kMmqAImage + p.stages * p.stage_bytes;
+    const int items = p.m_tiles * p.ksplit;
+    p.grid = items < num_sms ? items : num_sms;
+    p.bimg_bytes = (size_t(p.nkb) * p.np * 512 + 127) / 128 * 128;
+    p.sc_bytes = (size_t(K / kQK8) * p.np * 8 + 127) / 128 * 128;
+    p.part_bytes = p.ksplit > 1 ? size_t(p.ksplit) * ncols * rows * 4 : 0;
+    p.ws_bytes = p.bimg_bytes + p.sc_bytes + p.part_bytes;
+    return p;
+}
+
+template <int NP>
+static cudaError_t launch_mmq_np(const mq_mv_desc* d, int rows, int K, int ncols, const MmqPlan& p, uint8_t* ws,
+                                 int num_sms, unsigned* status, cudaStream_t s)
+{
+    uint8_t* bimg = ws;
+    float2* sc = reinterpret_cast<float2*>(ws + p.bimg_bytes);
+    float* part = reinterpret_cast<float*>(ws + p.bimg_bytes + p.sc_bytes);
+    const int64_t warps = int64_t(NP) * (K / kQK8);
+    const int64_t want = (warps + 7) / 8;
+    const int g1 = int(want < int64_t(num_sms) * 16 ? want : int64_t(num_sms) * 16);
+    mmq_stage_act_kernel<NP><<<g1, 256, 0, s>>>(d, rows, K, ncols, bimg, sc, status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    MmqArgs a;
+    a.R = rows;
+    a.K = K;
+    a.ncols = ncols;
+    a.m_tiles = p.m_tiles;
+    a.ksplit = p.ksplit;
+    a.nkb = p.nkb;
+    a.stages = p.stages;
+    a.stage_bytes = p.stage_bytes;
+    a.bimg = bimg;
+    a.sc = sc;
+    a.part = part;
+    a.limit_ns = uint64_t(fault_policy() == FAULT_NONE ? 2000 : 50) * 1000000ull;
+    mmq_kernel<NP><<<p.grid, kMmqThreads, p.smem, s>>>(d, a, status);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || p.ksplit == 1) return e;
+    const int64_t n = int64_t(ncols) * rows;
+    const int64_t w2 = (n + 255) / 256;
+    mmq_reduce_kernel<<<int(w2 < int64_t(num_sms) * 8 ? w2 : int64_t(num_sms) * 8), 256, 0, s>>>(d, part, p.ksplit,
+                                                                                                rows, ncols);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mmq(const mq_mv_desc* d, int rows, int K, int ncols, const MmqPlan& p, void* ws, int num_sms,
+                       unsigned* status, cudaStream_t s)
+{
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    switch (p.np) {
+        case 16: return launch_mmq_np<16>(d, rows, K, ncols, p, w, num_sms, status, s);
+        case 32: return launch_mmq_np<32>(d, rows, K, ncols, p, w, num_sms, status, s);
+        case 48: return launch_mmq_np<48>(d, rows, K, ncols, p, w, num_sms, status, s);
+        case 64: return launch_mmq_np<64>(d, rows, K, ncols, p, w, num_sms, status, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t set_mmq_attributes(int max_smem)
+{
+    cudaError_t e = cudaSuccess;
+    const void* k[4] = {reinterpret_cast<const void*>(mmq_kernel<16>), reinterpret_cast<const void*>(mmq_kernel<32>),
+                        reinterpret_cast<const void*>(mmq_kernel<48>), reinterpret_cast<const void*>(mmq_kernel<64>)};
+    for (int i = 0; i < 4 && e == cudaSuccess; ++i) e = set_max_dyn_smem(k[i], max_smem);
+    return e;
+}
+
+}  // namespace mq

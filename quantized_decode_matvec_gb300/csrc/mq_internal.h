@@ -131,6 +131,18 @@ cudaError_t launch_block_sums(const mq_mv_desc* d, int rows, int K, int ncols, i
                               int smem, unsigned* status, cudaStream_t s);
 // raises the dynamic shared memory limit of every kernel on the current device
 cudaError_t set_kernel_attributes(int max_smem);
+// small-batch matmul on the tensor cores (mmq.cu)
+struct MmqPlan {
+    int np;           // columns rounded up to 16 (the MMA's N)
+    int nkb;          // super-blocks per row
+    int m_tiles;      // 128-row tiles
+    int ksplit;       // K ranges per tile (partials summed in a fixed order)
+    int stages, stage_bytes, smem, grid;
+    size_t bimg_bytes, sc_bytes, part_bytes, ws_bytes;  // workspace: activation image, scales, partials
+};
+MmqPlan plan_mmq(int rows, int K, int ncols, int num_sms, int max_smem);
+cudaError_t launch_mmq(const mq_mv_desc* d, int rows, int K, int ncols, const MmqPlan& p, void* ws, int num_sms,
+                       unsigned* status, cudaStream_t s);
 // prefill operands and GEMM (dequant.cu, gemm.cu)
 cudaError_t launch_dequant_q4K_f16(const void* W, void* W16, int64_t nblocks, int num_sms, cudaStream_t s);
 cudaError_t launch_f32_to_f16(const float* x, void* y, int64_t n, int num_sms, cudaStream_t s);

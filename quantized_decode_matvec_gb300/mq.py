@@ -57,6 +57,7 @@ MQ_STEP_PERSISTENT = 2
 MQ_STEP_CHAINED = 4
 MQ_STEP_WORKSPACE_BYTES = 4352
 MQ_NOALLOC_HQ8_MAX_BYTES = 131072
+MQ_MMQ_MAX_NCOLS = 64
 
 
 class MvDesc(ctypes.Structure):
@@ -109,6 +110,8 @@ _sig("mq_ffn_gate_up", c_i32, c_vp, c_i32, c_i32, c_i32, c_vp)
 _sig("mq_step", c_i32, c_vp, ctypes.POINTER(StepShape), c_vp)
 _sig("mq_step_workspace_bytes", c_i32, ctypes.POINTER(StepShape), ctypes.POINTER(ctypes.c_size_t))
 _sig("mq_ffn_gu_silu_down_noalloc", c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_vp)
+_sig("mq_mmq_workspace_bytes", c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(ctypes.c_size_t))
+_sig("mq_mmq_q4K_q8_0", c_i32, c_vp, c_i32, c_i32, c_i32, c_vp, ctypes.c_size_t, c_vp)
 _sig("mq_dequant_q4K_f16", c_i32, c_vp, c_vp, c_i64, c_i64, c_vp)
 _sig("mq_convert_f32_f16", c_i32, c_vp, c_vp, c_i64, c_vp)
 _sig("mq_gemm_f16", c_i32, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_vp)
@@ -122,6 +125,7 @@ EXPORTS = ["mq_status_string", "mq_abi_version", "mq_last_cuda_error", "mq_init"
            "mq_concat_rows_feasible", "mq_concat_rows", "mq_quantize_q8_0", "mq_check_mv_desc",
            "mq_matvec_q4K_q8_0", "mq_matvec_q4_0_q8_0", "mq_matvec_q8_0_q8_0", "mq_check_ffn_desc", "mq_ffn_gu_silu_down", "mq_ffn_gate_up", "mq_step", "mq_step_workspace_bytes",
            "mq_ffn_gu_silu_down_noalloc", "mq_dequant_q4K_f16", "mq_convert_f32_f16", "mq_gemm_f16",
+           "mq_mmq_workspace_bytes", "mq_mmq_q4K_q8_0",
            "mq_debug_block_sums_q4K_q8_0", "mq_debug_set_variant", "mq_debug_set_fault"]
 
 
@@ -240,6 +244,17 @@ def mq_ffn_gu_silu_down_noalloc(W_gu: int, W_down: int, x: int, xq: int, y: int,
                                 y_ld: int, stream: int = 0) -> int:
     return _lib.mq_ffn_gu_silu_down_noalloc(c_vp(W_gu), c_vp(W_down), c_vp(x), c_vp(xq), c_vp(y), H, I, ncols,
                                             y_ld, c_vp(stream))
+
+
+def mq_mmq_workspace_bytes(rows: int, K: int, ncols: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_lib.mq_mmq_workspace_bytes(rows, K, ncols, ctypes.byref(n)), "mq_mmq_workspace_bytes")
+    return int(n.value)
+
+
+def mq_mmq_q4K_q8_0(d_desc: int, rows: int, K: int, ncols: int, workspace: int, ws_bytes: int,
+                    stream: int = 0) -> int:
+    return _lib.mq_mmq_q4K_q8_0(c_vp(d_desc), rows, K, ncols, c_vp(workspace), ws_bytes, c_vp(stream))
 
 
 def mq_dequant_q4K_f16(W: int, W16: int, rows: int, K: int, stream: int = 0) -> int:
@@ -420,6 +435,26 @@ def ffn_gu_silu_down_noalloc(W_gu, W_down, H: int, I: int, x=None, xq=None, y=No
     _check(mq_ffn_gu_silu_down_noalloc(_ptr(W_gu), _ptr(W_down), _ptr(x), _ptr(xq), _ptr(y), H, I, ncols,
                                        y.shape[-1], _stream(stream)), "mq_ffn_gu_silu_down_noalloc")
     return y
+
+
+def mmq_q4K_q8_0(W, rows: int, K: int, x=None, xq=None, y=None, xq_out=None, ncols: Optional[int] = None,
+                 workspace=None, stream=None):
+    """The matmul for more columns on the tensor cores: y [ncols, rows] fp32 = W . q8_0(x) (or W . xq).
+    Returns (y, desc_buffer, workspace)."""
+    torch = _torch()
+    act = x if x is not None else xq
+    if ncols is None:
+        ncols = act.shape[0] if act.dim() == 2 else 1
+    if y is None:
+        y = torch.empty((ncols, rows), dtype=torch.float32, device=W.device)
+    nbytes = mq_mmq_workspace_bytes(rows, K, ncols)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 128), dtype=torch.uint8, device=W.device)
+    d = mv_desc(W, rows, K, y, x=x, xq=xq, xq_out=xq_out, ncols=ncols, y_ld=y.shape[-1])
+    dd = upload_struct(d, W.device)
+    _check(mq_mmq_q4K_q8_0(_ptr(dd), rows, K, ncols, _ptr(workspace), workspace.numel(), _stream(stream)),
+           "mq_mmq_q4K_q8_0")
+    return y, dd, workspace
 
 
 def dequant_q4K_f16(W, rows: int, K: int, out=None, stream=None):
