@@ -566,6 +566,34 @@ def config_suite(mq, device, oracle_arms=True):
         del copies, descs
         ora(f"{wt}_weights_4096x{K}",
             lambda a: a.matvec_w(wt, W_np, oracle.quantize_q8_0(x_np), synth.KSWEEP_ROWS, K))
+    # more columns: the MMQ matmul on the tensor cores at the 7B FFN shapes (rotated weight copies),
+    # beside the decode kernel (MMVQ, dp4a) where both apply
+    f = synth.FFN_7B
+    for name, (R, K, tag) in {"gu": (2 * f.I, f.H, synth.TAG_GU), "down": (f.H, f.I, synth.TAG_DOWN)}.items():
+        W0 = torch.from_numpy(synth.q4K_matrix(R, K, seed=f.seed, tag=tag)).to(device)
+        copies = [W0] + [W0.clone() for _ in range(l2 // W0.numel() + 1)]
+        for nc in (8, 16, 32, 64):
+            x = torch.from_numpy(synth.activation(K, nc, seed=92)).to(device)
+            y = torch.empty((nc, R), dtype=torch.float32, device=device)
+            ws = torch.empty(max(mq.mq_mmq_workspace_bytes(R, K, nc), 128), dtype=torch.uint8, device=device)
+            descs = [mq.upload_struct(mq.mv_desc(Wc, R, K, y, x=x, ncols=nc), device) for Wc in copies]
+
+            def mk(d, nc=nc, ws=ws):
+                return lambda: mq._check(mq.mq_mmq_q4K_q8_0(d.data_ptr(), R, K, nc, ws.data_ptr(), ws.numel(),
+                                                            torch.cuda.current_stream().cuda_stream), "mmq")
+            ms = timed([mk(d) for d in descs], 5)
+            rec(f"mmq_{name}_{R}x{K}_ncols{nc}", ms, W0.numel(), copies=len(copies),
+                int_tops=round(2.0 * R * K * nc / (ms / 1e3) / 1e12, 1),
+                kernel="mmq_kernel (tcgen05.mma kind::f16 on exact nibble and q8_0 codes)")
+            if nc == 8:  # the decode kernel on the same call
+                calls, keep = mv_calls(copies, R, K, x, y)
+                rec(f"mmvq_{name}_{R}x{K}_ncols8", timed(calls, 5), W0.numel(), copies=len(copies),
+                    kernel="ring_kernel (dp4a)")
+                del calls, keep
+            del descs, ws
+        del copies, W0
+    assert mq.mq_read_device_status(0) == 0
+
     # prefill on the tensor cores: one 7B-class layer's GEMMs at 2048 tokens over the resident
     # f16 weight cache (built by mq_dequant_q4K_f16), activations converted once to f16
     tflops_peak = measured_bf16_peak()
@@ -639,6 +667,44 @@ def chained_arm(mq, case, layers, stream, g_default, shift=11, rounds=3, reps=5)
     del gc, cb, wc
     torch.cuda.empty_cache()
     return out
+
+
+def run_kernel_case(args):
+    """One kernel on one small, fixed case, a few launches: a target for ncu captures (one kernel,
+    few launches, a few hundred MB on the device).  Prints one JSON line with the mean launch time."""
+    import torch
+    from quantized_decode_matvec_gb300 import build as mqbuild
+    mqbuild.build()
+    from quantized_decode_matvec_gb300 import mq, synth
+    device = torch.device("cuda", torch.cuda.current_device())
+    mq.init(device.index)
+    f = synth.FFN_7B
+    R, K = 2 * f.I, f.H  # the 7B ffn_gu projection
+    W = torch.from_numpy(synth.q4K_matrix(R, K, seed=f.seed, tag=synth.TAG_GU)).to(device)
+    if args.kernel_case.startswith("gemm"):
+        T = 2048
+        W16 = mq.dequant_q4K_f16(W, R, K)
+        X16 = mq.convert_f32_f16(torch.from_numpy(synth.activation(K, T, seed=91)).to(device))
+        Y = torch.empty((T, R), dtype=torch.float32, device=device)
+        run = lambda: mq.gemm_f16(W16, X16, out=Y)
+        work = {"tflops_per_launch": 2.0 * T * R * K / 1e12}
+    else:
+        nc = int(args.kernel_case.split("ncols")[1])
+        x = torch.from_numpy(synth.activation(K, nc, seed=92)).to(device)
+        y = torch.empty((nc, R), dtype=torch.float32, device=device)
+        ws = torch.empty(max(mq.mq_mmq_workspace_bytes(R, K, nc), 128), dtype=torch.uint8, device=device)
+        d = mq.upload_struct(mq.mv_desc(W, R, K, y, x=x, ncols=nc), device)
+        run = lambda: mq._check(mq.mq_mmq_q4K_q8_0(d.data_ptr(), R, K, nc, ws.data_ptr(), ws.numel(),
+                                                    torch.cuda.current_stream().cuda_stream), "mmq")
+        work = {"weight_bytes_per_launch": W.numel()}
+    for _ in range(args.warmup):
+        run()
+    torch.cuda.synchronize()
+    t = time_replays(run, torch.cuda.current_stream(), args.steps)
+    assert mq.mq_read_device_status(0) == 0
+    print(json.dumps({"kernel_case": args.kernel_case, "launches": args.steps, "mean_us": 1e3 * sum(t) / len(t),
+                      **work}), flush=True)
+    return 0
 
 
 def run_ours(args):
@@ -822,6 +888,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-config timings (context only)")
     ap.add_argument("--no-chained-arm", action="store_true", help="skip the chained-step arm (context only)")
+    ap.add_argument("--kernel-case", choices=["gemm_gu_T2048", "mmq_gu_ncols16", "mmq_gu_ncols64"], default=None,
+                    help="run one kernel on a fixed small case a few times (a target for ncu), not the benchmark")
     ap.add_argument("--layers", type=int, default=28,
                     help="layers of the 7B stack (28 = the bench workload; fewer only for small profiling runs)")
     args = ap.parse_args(argv)
@@ -829,6 +897,8 @@ def main(argv=None):
         ap.error("at least 3 warm-up steps")
     if args.impl == "reference":
         return run_reference(args)
+    if args.kernel_case:
+        return run_kernel_case(args)
     return run_ours(args)
 
 

@@ -7,8 +7,8 @@
 //   Y[t][r] = sum_k X[t][k] * W[r][k]      X f16 [T][K], W f16 [R][K], Y fp32 [T][R]
 //
 // with fp32 accumulation in tensor memory.  One CTA per SM walks output tiles
-// of 128 weight rows x BN tokens, BN = 256 (or 128 where that fills the last
-// wave of CTAs clearly better), persistent, static round robin; tiles that
+// of 128 weight rows x BN tokens, BN = 256 (128 for at most 128 tokens),
+// persistent, static round robin; tiles that
 // share a weight block run at the same time, so each block comes from HBM
 // about once and from L2 for the other token tiles.  Per CTA:
 //
@@ -246,22 +246,16 @@ cudaError_t set_gemm_attributes(int max_smem)
     return e;
 }
 
-// the share of the CTAs' tile slots that holds a tile: tiles / (waves * grid)
-static double wave_use(int64_t tiles, int num_sms)
-{
-    const int64_t grid = tiles < num_sms ? tiles : num_sms;
-    const int64_t waves = (tiles + grid - 1) / grid;
-    return double(tiles) / double(waves * grid);
-}
 
 // returns cudaErrorInvalidValue when the tensor maps cannot be built
 cudaError_t launch_gemm_f16(const void* W16, const void* X16, float* Y, int R, int K, int T, int num_sms,
                             unsigned* status, cudaStream_t s)
 {
     const int m_tiles = (R + kGemmBM - 1) / kGemmBM;
-    // 256-token tiles unless 128-token tiles fill the CTAs' waves clearly better
-    const int64_t t256 = int64_t(m_tiles) * ((T + 255) / 256), t128 = int64_t(m_tiles) * ((T + 127) / 128);
-    const int BN = wave_use(t128, num_sms) > wave_use(t256, num_sms) + 0.05 ? 128 : 256;
+    // 256-token tiles (128-token tiles, which fill the last wave of CTAs better for
+    // the 3584-row matrices at 2048 tokens, measured slower there on GB300: o
+    // 63 against 48 us, down 275 against 219 us); 128 only for at most 128 tokens
+    const int BN = T <= 128 ? 128 : 256;
     CUtensorMap tmW, tmX;
     if (!make_map(&tmW, W16, R, K, kGemmBM) || !make_map(&tmX, X16, T, K, BN)) return cudaErrorInvalidValue;
     GemmArgs a;

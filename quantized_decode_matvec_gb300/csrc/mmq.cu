@@ -22,15 +22,18 @@
 // block and column; (2) the matmul; (3) for matrices with few row tiles, the
 // K range is split over CTAs and a fixed-order sum combines the partials.
 //
-// The matmul CTA (persistent over its work items, 10 warps):
-//   warp 0     bulk copies (TMA) of each step's 128 weight rows (144 bytes
-//              each), the step's activation image and its scales, into a ring
-//              of stages
-//   warp 1     TMEM allocation; one lane issues two MMAs (M=128, N=ncols
-//              rounded up to 16, K=16) per sub-block into the sub-block's slot
-//   warps 2-5  convert each row's quants to the f16 A image (thread = row)
-//   warps 6-9  epilogue (thread = row = TMEM lane): per sub-block, read the
-//              slot, free it, apply the scales into fp32 registers
+// The matmul CTA (persistent over its work items, 14 warps):
+//   warp 0      bulk copies (TMA) of each step's 128 weight rows (144 bytes
+//               each), the step's activation image and its scales, into a
+//               ring of stages
+//   warp 1      TMEM allocation; one lane issues two MMAs (M=128, N=ncols
+//               rounded up to 16, K=16) per sub-block into the sub-block's slot
+//   warps 2-9   convert the rows' quants to the f16 A image (thread = row;
+//               warps 2-5 the first half of each step, 6-9 the second), into a
+//               ring of half-step buffers, so conversion overlaps the MMAs
+//   warps 10-13 epilogue (thread = row = TMEM lane): per sub-block, read the
+//               slot, apply the scales into fp32 registers (packed f32x2
+//               arithmetic), free the slot
 // Every wait is bounded in time; a timeout records MQ_DEV_TIMEOUT and the
 // roles stop (the producer waits, bounded, for its copies in flight).
 #include <cuda_fp16.h>
@@ -41,14 +44,14 @@
 namespace mq {
 
 constexpr int kMmqBM = 128;                          // weight rows per tile
-constexpr int kMmqThreads = 320;
+constexpr int kMmqThreads = 448;
 constexpr int kMmqAtom = kMmqBM * 128;               // one 128 x 64 f16 swizzled atom: 16 KB
-constexpr int kMmqAImage = 4 * kMmqAtom;             // 256 K of A: 64 KB
+constexpr int kMmqAHalf = 2 * kMmqAtom;              // half a step of A (128 K): 32 KB
 constexpr int kMmqRaw = kMmqBM * kQ4KBytes;          // 128 rows x 144 bytes
 constexpr uint32_t kMmqTmemCols = 512;
 
 __host__ __device__ constexpr int mmq_np(int nc) { return (nc + 15) / 16 * 16; }
-// stage: raw weights | activation image (4 atoms of NP rows x 128 B) | scales [8][NP] (dq, dq*sumq)
+// stage: raw weights | activation image (4 atoms of NP rows x 128 B) | scales [8][2][NP] (dq, dq*sumq)
 __host__ __device__ constexpr int mmq_stage_bytes(int NP) { return kMmqRaw + NP * 512 + 8 * NP * 8; }
 __host__ __device__ constexpr int mmq_round1k(int b) { return (b + 1023) / 1024 * 1024; }
 
@@ -56,9 +59,10 @@ struct MmqArgs {
     int R, K, ncols;
     int m_tiles, ksplit, nkb;
     int stages;
+    int nab;                  // half-step A buffers
     int stage_bytes;          // 1024-aligned
     const uint8_t* bimg;      // activation images, nkb x NP*512 bytes
-    const float2* sc;         // [K/32][NP] (dq, dq*sumq)
+    const float* sc;          // [K/32][2][NP]: dq, then dq*sumq
     float* part;              // [ksplit][ncols][R] partial sums (ksplit > 1)
     uint64_t limit_ns;
 };
@@ -67,7 +71,7 @@ struct MmqArgs {
 // One warp per (column, 32-block); lane l is element 32J + l.
 template <int NP>
 __global__ void mmq_stage_act_kernel(const mq_mv_desc* __restrict__ desc, int rows_h, int K_h, int nc_h,
-                                     uint8_t* __restrict__ bimg, float2* __restrict__ sc, unsigned* status)
+                                     uint8_t* __restrict__ bimg, float* __restrict__ sc, unsigned* status)
 {
     const MvJob j = read_job<KIND_MV>(desc);
     const unsigned bad = check_job(j, rows_h, K_h, nc_h);
@@ -105,7 +109,10 @@ __global__ void mmq_stage_act_kernel(const mq_mv_desc* __restrict__ desc, int ro
         const size_t off = size_t(kb) * (NP * 512) + size_t(a) * (NP * 128) + size_t(c) * 128 +
                            size_t(((e >> 3) ^ (c & 7)) << 4) + size_t(e & 7) * 2;
         *reinterpret_cast<__half*>(bimg + off) = __int2half_rn(q);
-        if (lane == 0) sc[size_t(J) * NP + c] = make_float2(dq, dq * float(sq));
+        if (lane == 0) {
+            sc[size_t(2 * J) * NP + c] = dq;
+            sc[size_t(2 * J + 1) * NP + c] = dq * float(sq);
+        }
     }
 }
 
@@ -146,21 +153,37 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// packed fp32 pairs: (lo, hi) in one 64-bit register for the f32x2 instructions
+__device__ __forceinline__ uint64_t pack2(float lo, float hi)
+{
+    return uint64_t(__float_as_uint(lo)) | (uint64_t(__float_as_uint(hi)) << 32);
+}
+
+// y += ds * (dq * S) - dm * dqs on two columns at once (each lane of the pair
+// rounds exactly as the scalar fmaf chain would)
+__device__ __forceinline__ void epi2(uint64_t& y, uint64_t S, uint64_t dq, uint64_t dqs, uint64_t ds2, uint64_t ndm2)
+{
+    uint64_t t;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(t) : "l"(dq), "l"(S));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(y) : "l"(ds2), "l"(t));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(y) : "l"(ndm2), "l"(dqs));
+}
+
 template <int NP>
 __global__ void __launch_bounds__(kMmqThreads, 1)
     mmq_kernel(const mq_mv_desc* __restrict__ desc, const MmqArgs a, unsigned* status)
 {
     constexpr int NSLOT = int(kMmqTmemCols) / NP;  // accumulator slots of NP columns
     extern __shared__ uint8_t msm_raw[];
-    __shared__ __align__(8) uint64_t full[4], empty[4], a_full, a_free, slot_full[32], slot_free[32];
+    __shared__ __align__(8) uint64_t full[4], empty[4], a_full[4], a_free[4], slot_full[32], slot_free[32];
     __shared__ uint32_t tmem_base;
     __shared__ volatile int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t raw_addr = smem_u32(msm_raw);
     uint8_t* const sm = msm_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-    uint8_t* const aimg = sm;                 // 64 KB, 1024-aligned
-    uint8_t* const stages = sm + kMmqAImage;  // a.stages x a.stage_bytes
+    uint8_t* const abuf = sm;                                     // a.nab x 32 KB, 1024-aligned
+    uint8_t* const stages = sm + size_t(a.nab) * kMmqAHalf;       // a.stages x a.stage_bytes
     {
         // the activation launch checked the descriptor too; a bad one stops this launch as well
         const unsigned bad = check_job(read_job<KIND_MV>(desc), a.R, a.K, a.ncols);
@@ -176,10 +199,12 @@ __global__ void __launch_bounds__(kMmqThreads, 1)
         abort_flag = 0;
         for (int s = 0; s < a.stages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 4 + 1 + 4);  // converter warps, the MMA commit, epilogue warps
+            mbar_init(&empty[s], 8 + 1 + 4);  // converter warps, the MMA commit, epilogue warps
         }
-        mbar_init(&a_full, 4);
-        mbar_init(&a_free, 1);
+        for (int b = 0; b < a.nab; ++b) {
+            mbar_init(&a_full[b], 4);  // the four warps of a half's converter group
+            mbar_init(&a_free[b], 1);  // MMA commit
+        }
         for (int i = 0; i < NSLOT; ++i) {
             mbar_init(&slot_full[i], 1);
             mbar_init(&slot_free[i], 4);
@@ -226,7 +251,7 @@ __global__ void __launch_bounds__(kMmqThreads, 1)
                                   kQ4KBytes, &full[s]);
                 if (lane == 0) {
                     bulk_copy_g2s(st + kMmqRaw, a.bimg + size_t(kb) * (NP * 512), NP * 512, &full[s]);
-                    bulk_copy_g2s(st + kMmqRaw + NP * 512, a.sc + size_t(kb) * 8 * NP, 8 * NP * 8, &full[s]);
+                    bulk_copy_g2s(st + kMmqRaw + NP * 512, a.sc + size_t(kb) * 16 * NP, 8 * NP * 8, &full[s]);
                 }
             }
         }
@@ -237,79 +262,76 @@ __global__ void __launch_bounds__(kMmqThreads, 1)
         // ---- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = umma_idesc_f16_f32(kMmqBM, NP);
-            const uint32_t aaddr = smem_u32(aimg);
+            const uint32_t aaddr = smem_u32(abuf);
             int g = 0, v = 0;  // steps and slot uses so far
-            for (int it = blockIdx.x; it < nitems && !abort_flag; it += gridDim.x) {
+            bool ok = true;
+            for (int it = blockIdx.x; it < nitems && ok && !abort_flag; it += gridDim.x) {
                 int m, kb0, kb1;
                 item(it, m, kb0, kb1);
-                for (int kb = kb0; kb < kb1; ++kb, ++g) {
+                for (int kb = kb0; kb < kb1 && ok; ++kb, ++g) {
                     const int s = g % a.stages;
-                    if (!mbar_wait_bounded(&a_full, uint32_t(g) & 1u, a.limit_ns) ||
-                        !mbar_wait_bounded(&full[s], uint32_t(g / a.stages) & 1u, a.limit_ns)) {
-                        abort_flag = 1;
-                        break;
-                    }
-                    tc_fence_after();
+                    ok = mbar_wait_bounded(&full[s], uint32_t(g / a.stages) & 1u, a.limit_ns);
                     const uint32_t baddr = smem_u32(stages + size_t(s) * a.stage_bytes + kMmqRaw);
-                    bool ok = true;
-                    for (int j = 0; j < 8; ++j, ++v) {
-                        const int slot = v % NSLOT;
-                        if (v >= NSLOT &&
-                            !mbar_wait_bounded(&slot_free[slot], uint32_t(v / NSLOT - 1) & 1u, a.limit_ns)) {
-                            ok = false;
-                            break;
-                        }
+                    for (int h = 0; h < 2 && ok; ++h) {
+                        const int u = 2 * g + h, b = u % a.nab;
+                        ok = mbar_wait_bounded(&a_full[b], uint32_t(u / a.nab) & 1u, a.limit_ns);
                         tc_fence_after();
-                        const uint32_t koff = uint32_t(j & 1) * 64;
-                        const uint32_t ab = aaddr + uint32_t(j >> 1) * kMmqAtom + koff;
-                        const uint32_t bb = baddr + uint32_t(j >> 1) * (NP * 128) + koff;
-                        const uint32_t d = tmem + uint32_t(slot * NP);
-                        umma_f16(d, umma_desc_sw128(ab), umma_desc_sw128(bb), idesc, false);
-                        umma_f16(d, umma_desc_sw128(ab + 32), umma_desc_sw128(bb + 32), idesc, true);
-                        umma_commit(&slot_full[slot]);
+                        const uint32_t ah = aaddr + uint32_t(b) * kMmqAHalf;
+                        for (int jj = 0; jj < 4 && ok; ++jj, ++v) {
+                            const int j = 4 * h + jj;  // sub-block of the step
+                            const int slot = v % NSLOT;
+                            if (v >= NSLOT)
+                                ok = mbar_wait_bounded(&slot_free[slot], uint32_t(v / NSLOT - 1) & 1u, a.limit_ns);
+                            if (!ok) break;
+                            tc_fence_after();
+                            const uint32_t koff = uint32_t(j & 1) * 64;
+                            const uint32_t ab = ah + uint32_t(jj >> 1) * kMmqAtom + koff;
+                            const uint32_t bb = baddr + uint32_t(j >> 1) * (NP * 128) + koff;
+                            const uint32_t d = tmem + uint32_t(slot * NP);
+                            umma_f16(d, umma_desc_sw128(ab), umma_desc_sw128(bb), idesc, false);
+                            umma_f16(d, umma_desc_sw128(ab + 32), umma_desc_sw128(bb + 32), idesc, true);
+                            umma_commit(&slot_full[slot]);
+                        }
+                        if (ok) umma_commit(&a_free[b]);  // this half's A buffer may be rewritten
                     }
-                    if (!ok) {
-                        abort_flag = 1;
-                        break;
-                    }
-                    umma_commit(&a_free);    // the A image may be rewritten
-                    umma_commit(&empty[s]);  // this step's activation image has been read
+                    if (ok) umma_commit(&empty[s]);  // this step's activation image has been read
                 }
-                if (abort_flag) break;
             }
+            if (!ok) abort_flag = 1;
             if (v > 0)  // the last MMAs complete before TMEM is freed
                 (void)mbar_wait_bounded(&slot_full[(v - 1) % NSLOT], uint32_t((v - 1) / NSLOT) & 1u, a.limit_ns);
         }
-    } else if (warp < 6) {
-        // ---- converters: thread = row r of the tile
+    } else if (warp < 10) {
+        // ---- converters: thread = row r of the tile; group h converts half h of every step
+        // (quant bytes 64h..64h+63: sub-blocks 4h..4h+3) into the half-step buffer
+        const int h = (warp - 2) >> 2;
         const int r = (warp & 3) * 32 + lane;
-        const uint32_t arow = smem_u32(aimg) + uint32_t(r) * 128;
         const uint32_t sw = uint32_t(r & 7);
         int g = 0;
-        for (int it = blockIdx.x; it < nitems; it += gridDim.x) {
+        bool ok = true;
+        for (int it = blockIdx.x; it < nitems && ok; it += gridDim.x) {
             int m, kb0, kb1;
             item(it, m, kb0, kb1);
             const bool live = m * kMmqBM + r < a.R;
             for (int kb = kb0; kb < kb1; ++kb, ++g) {
                 const int s = g % a.stages;
-                bool ok = mbar_wait_bounded(&full[s], uint32_t(g / a.stages) & 1u, a.limit_ns);
-                if (ok && g > 0) ok = mbar_wait_bounded(&a_free, uint32_t(g - 1) & 1u, a.limit_ns);
-                if (!__all_sync(0xffffffffu, ok && !abort_flag)) {
-                    if (lane == 0) abort_flag = 1;
-                    it = nitems;  // stop
-                    break;
-                }
+                const int u = 2 * g + h, b = u % a.nab, n = u / a.nab;
+                bool w = mbar_wait_bounded(&full[s], uint32_t(g / a.stages) & 1u, a.limit_ns);
+                if (w && n > 0) w = mbar_wait_bounded(&a_free[b], uint32_t(n - 1) & 1u, a.limit_ns);
+                ok = __all_sync(0xffffffffu, w && !abort_flag);  // one decision for the whole warp
+                if (!ok) break;
                 const uint8_t* raw = stages + size_t(s) * a.stage_bytes + size_t(r) * kQ4KBytes;
+                const uint32_t arow = smem_u32(abuf) + uint32_t(b) * kMmqAHalf + uint32_t(r) * 128;
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    // quant bytes 32cc..32cc+31: sub-block 2cc (low nibbles), 2cc+1 (high nibbles)
+                for (int ca = 0; ca < 2; ++ca) {
+                    const int cc = 2 * h + ca;  // quant bytes 32cc..32cc+31: sub-blocks 2cc (low), 2cc+1 (high)
                     uint4 q0 = make_uint4(0, 0, 0, 0), q1 = q0;
                     if (live) {
                         q0 = *reinterpret_cast<const uint4*>(raw + 16 + 32 * cc);
                         q1 = *reinterpret_cast<const uint4*>(raw + 32 + 32 * cc);
                     }
                     const uint32_t wq[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                    const uint32_t atom = arow + uint32_t(cc) * kMmqAtom;
+                    const uint32_t atom = arow + uint32_t(ca) * kMmqAtom;
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
                         // chunk c: elements 8c..8c+7 of the atom's 64: low nibbles of bytes
@@ -323,11 +345,12 @@ __global__ void __launch_bounds__(kMmqThreads, 1)
                 fence_proxy_async_smem();  // the A image is read by the tensor cores
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(&a_full);
+                    mbar_arrive(&a_full[b]);
                     mbar_arrive(&empty[s]);
                 }
             }
         }
+        if (!ok && lane == 0) abort_flag = 1;
     } else {
         // ---- epilogue: thread = TMEM lane = row r of the tile
         const int q = warp & 3, r = q * 32 + lane;
@@ -338,9 +361,9 @@ __global__ void __launch_bounds__(kMmqThreads, 1)
             int m, kb0, kb1;
             item(it, m, kb0, kb1);
             const int row = m * kMmqBM + r;
-            float y[NP];
+            uint64_t y2[NP / 2];  // column pairs (2c, 2c+1)
 #pragma unroll
-            for (int c = 0; c < NP; ++c) y[c] = 0.0f;
+            for (int c = 0; c < NP / 2; ++c) y2[c] = 0;
             for (int kb = kb0; kb < kb1 && !stop; ++kb, ++g) {
                 const int s = g % a.stages;
                 const uint8_t* st = stages + size_t(s) * a.stage_bytes;
@@ -382,39 +405,41 @@ __global__ void __launch_bounds__(kMmqThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    float S[NP];
+                    const uint64_t ds2 = pack2(ds[jj], ds[jj]), ndm2 = pack2(-dm[jj], -dm[jj]);
+                    const float4* dqv = scj + (2 * jj) * (NP / 4);       // dq of the sub-block's columns
+                    const float4* dqsv = scj + (2 * jj + 1) * (NP / 4);  // dq*sumq
 #pragma unroll
                     for (int c0 = 0; c0 < NP; c0 += 16) {
                         float t[16];
                         tmem_ld16(tmem + lane_base + uint32_t(slot * NP + c0), t);
+                        tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) S[c0 + i] = t[i];
+                        for (int i = 0; i < 16; i += 4) {
+                            const float4 dq = dqv[(c0 + i) >> 2], dqs = dqsv[(c0 + i) >> 2];
+                            epi2(y2[(c0 + i) >> 1], pack2(t[i], t[i + 1]), pack2(dq.x, dq.y), pack2(dqs.x, dqs.y), ds2,
+                                 ndm2);
+                            epi2(y2[((c0 + i) >> 1) + 1], pack2(t[i + 2], t[i + 3]), pack2(dq.z, dq.w),
+                                 pack2(dqs.z, dqs.w), ds2, ndm2);
+                        }
                     }
-                    tmem_ld_wait();
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&slot_free[slot]);
-#pragma unroll
-                    for (int c = 0; c < NP; c += 2) {
-                        const float4 p = scj[(jj * NP + c) >> 1];  // (dq, dq*sumq) of columns c, c+1
-                        y[c] = fmaf(-dm[jj], p.y, fmaf(ds[jj], p.x * S[c], y[c]));
-                        y[c + 1] = fmaf(-dm[jj], p.w, fmaf(ds[jj], p.z * S[c + 1], y[c + 1]));
-                    }
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[s]);
+                if (lane == 0 && !stop) mbar_arrive(&empty[s]);
             }
             if (stop) break;
             if (row < a.R) {
                 const int ks = it - m * a.ksplit;
-                if (a.ksplit == 1) {
 #pragma unroll
-                    for (int c = 0; c < NP; ++c)
-                        if (c < a.ncols) Y[size_t(c) * y_ld + row] = y[c];
-                } else {
-#pragma unroll
-                    for (int c = 0; c < NP; ++c)
-                        if (c < a.ncols) a.part[(size_t(ks) * a.ncols + c) * a.R + row] = y[c];
+                for (int c = 0; c < NP; ++c) {
+                    if (c >= a.ncols) break;
+                    const float yc = __uint_as_float(uint32_t(y2[c >> 1] >> (32 * (c & 1))));
+                    if (a.ksplit == 1)
+                        Y[size_t(c) * y_ld + row] = yc;
+                    else
+                        a.part[(size_t(ks) * a.ncols + c) * a.R + row] = yc;
                 }
             }
         }
@@ -454,9 +479,15 @@ MmqPlan plan_mmq(int rows, int K, int ncols, int num_sms, int max_smem)
     int ks = num_sms / p.m_tiles;
     p.ksplit = ks < 1 ? 1 : (ks > p.nkb ? p.nkb : ks);
     p.stage_bytes = mmq_round1k(mmq_stage_bytes(p.np));
-    int st = (max_smem - 1024 - 256 - kMmqAImage) / p.stage_bytes;
-    p.stages = st > 4 ? 4 : st;
-    p.smem = 1024 + kMmqAImage + p.stages * p.stage_bytes;
+    // the most half-step A buffers (4, 3, 2) that still leave two stages; up to 4 stages
+    // (the kernel's static shared memory, under 2 KB, comes off the opt-in maximum)
+    p.stages = 0;
+    for (int nab = 4; nab >= 2 && p.stages < 2; --nab) {
+        const int st = (max_smem - 2048 - 1024 - nab * kMmqAHalf) / p.stage_bytes;
+        p.nab = nab;
+        p.stages = st > 4 ? 4 : st;
+    }
+    p.smem = 1024 + p.nab * kMmqAHalf + p.stages * p.stage_bytes;
     const int items = p.m_tiles * p.ksplit;
     p.grid = items < num_sms ? items : num_sms;
     p.bimg_bytes = (size_t(p.nkb) * p.np * 512 + 127) / 128 * 128;
@@ -471,7 +502,7 @@ static cudaError_t launch_mmq_np(const mq_mv_desc* d, int rows, int K, int ncols
                                  int num_sms, unsigned* status, cudaStream_t s)
 {
     uint8_t* bimg = ws;
-    float2* sc = reinterpret_cast<float2*>(ws + p.bimg_bytes);
+    float* sc = reinterpret_cast<float*>(ws + p.bimg_bytes);
     float* part = reinterpret_cast<float*>(ws + p.bimg_bytes + p.sc_bytes);
     const int64_t warps = int64_t(NP) * (K / kQK8);
     const int64_t want = (warps + 7) / 8;
@@ -487,6 +518,7 @@ static cudaError_t launch_mmq_np(const mq_mv_desc* d, int rows, int K, int ncols
     a.ksplit = p.ksplit;
     a.nkb = p.nkb;
     a.stages = p.stages;
+    a.nab = p.nab;
     a.stage_bytes = p.stage_bytes;
     a.bimg = bimg;
     a.sc = sc;

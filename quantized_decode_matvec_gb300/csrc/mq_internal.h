@@ -138,6 +138,7 @@ struct MmqPlan {
     int m_tiles;      // 128-row tiles
     int ksplit;       // K ranges per tile (partials summed in a fixed order)
     int stages, stage_bytes, smem, grid;
+    int nab;          // half-step A buffers
     size_t bimg_bytes, sc_bytes, part_bytes, ws_bytes;  // workspace: activation image, scales, partials
 };
 MmqPlan plan_mmq(int rows, int K, int ncols, int num_sms, int max_smem);
