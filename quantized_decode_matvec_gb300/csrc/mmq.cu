@@ -23,9 +23,10 @@
 // K range is split over CTAs and a fixed-order sum combines the partials.
 //
 // The matmul CTA (persistent over its work items, 14 warps):
-//   warp 0      bulk copies (TMA) of each step's 128 weight rows (144 bytes
-//               each), the step's activation image and its scales, into a
-//               ring of stages
+//   warp 0      each step's 128 weight rows (144 bytes each) by 16-byte
+//               asynchronous copies spread over the lanes, the step's
+//               activation image and its scales by two bulk copies (TMA), into
+//               a ring of stages
 //   warp 1      TMEM allocation; one lane issues two MMAs (M=128, N=ncols
 //               rounded up to 16, K=16) per sub-block into the sub-block's slot
 //   warps 2-9   convert the rows' quants to the f16 A image (thread = row;
@@ -133,6 +134,19 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
+// 16 bytes global -> shared, through L2 only; completion tracked per thread
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// the mbarrier receives one arrival (counted in its expected count) once every
+// cp.async this thread issued before has completed
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -174,8 +188,9 @@ __global__ void __launch_bounds__(kMmqThreads, 1)
     mmq_kernel(const mq_mv_desc* __restrict__ desc, const MmqArgs a, unsigned* status)
 {
     constexpr int NSLOT = int(kMmqTmemCols) / NP;  // accumulator slots of NP columns
+    constexpr int NGRP = NSLOT / 8;                   // steps whose eight slots fit at once
     extern __shared__ uint8_t msm_raw[];
-    __shared__ __align__(8) uint64_t full[4], empty[4], a_full[4], a_free[4], slot_full[32], slot_free[32];
+    __shared__ __align__(8) uint64_t full[4], empty[4], a_full[4], a_free[4], acc_full[4], slot_free[32];
     __shared__ uint32_t tmem_base;
     __shared__ volatile int abort_flag;
 
@@ -198,17 +213,15 @@ __global__ void __launch_bounds__(kMmqThreads, 1)
     if (threadIdx.x == 0) {
         abort_flag = 0;
         for (int s = 0; s < a.stages; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], 32 + 1);      // the producer's lanes' row copies, and its activation copies
             mbar_init(&empty[s], 8 + 1 + 4);  // converter warps, the MMA commit, epilogue warps
         }
         for (int b = 0; b < a.nab; ++b) {
             mbar_init(&a_full[b], 4);  // the four warps of a half's converter group
             mbar_init(&a_free[b], 1);  // MMA commit
         }
-        for (int i = 0; i < NSLOT; ++i) {
-            mbar_init(&slot_full[i], 1);
-            mbar_init(&slot_free[i], 4);
-        }
+        for (int i = 0; i < NGRP; ++i) mbar_init(&acc_full[i], 1);  // MMA commit, once per step
+        for (int i = 0; i < NSLOT; ++i) mbar_init(&slot_free[i], 4);  // epilogue warps, per slot
         fence_barrier_init();
     }
     if (warp == 1) tmem_alloc(&tmem_base, kMmqTmemCols);
@@ -243,16 +256,21 @@ __global__ void __launch_bounds__(kMmqThreads, 1)
                     break;
                 }
                 uint8_t* st = stages + size_t(s) * a.stage_bytes;
-                if (lane == 0)
-                    mbar_arrive_expect_tx(&full[s], uint32_t(nrow * kQ4KBytes + NP * 512 + 8 * NP * 8));
-                __syncwarp();
-                for (int r = lane; r < nrow; r += 32)
-                    bulk_copy_g2s(st + r * kQ4KBytes, W + size_t(r0 + r) * row_bytes + size_t(kb) * kQ4KBytes,
-                                  kQ4KBytes, &full[s]);
-                if (lane == 0) {
+                if (lane == 0) {  // the activation image and its scales: two bulk copies
+                    mbar_arrive_expect_tx(&full[s], uint32_t(NP * 512 + 8 * NP * 8));
                     bulk_copy_g2s(st + kMmqRaw, a.bimg + size_t(kb) * (NP * 512), NP * 512, &full[s]);
                     bulk_copy_g2s(st + kMmqRaw + NP * 512, a.sc + size_t(kb) * 16 * NP, 8 * NP * 8, &full[s]);
                 }
+                // the rows' 144-byte blocks: nine 16-byte chunks each, consecutive chunks on
+                // consecutive lanes (one bulk copy per row would queue 128 small copies on the
+                // copy engine, which handles them one after another)
+                const uint8_t* src = W + size_t(r0) * row_bytes + size_t(kb) * kQ4KBytes;
+                const uint32_t dst = smem_u32(st);
+                for (int i = lane; i < nrow * 9; i += 32) {
+                    const int r = i / 9, c = i - r * 9;
+                    cp_async16(dst + uint32_t(i) * 16, src + size_t(r) * row_bytes + 16 * c);
+                }
+                cp_async_arrive_noinc(&full[s]);  // arrives once this lane's copies have landed
             }
         }
         if (lane == 0)  // copies still in flight land before the CTA exits
@@ -277,29 +295,38 @@ __global__ void __launch_bounds__(kMmqThreads, 1)
                         ok = mbar_wait_bounded(&a_full[b], uint32_t(u / a.nab) & 1u, a.limit_ns);
                         tc_fence_after();
                         const uint32_t ah = aaddr + uint32_t(b) * kMmqAHalf;
-                        for (int jj = 0; jj < 4 && ok; ++jj, ++v) {
+                        // the half's four slots free, then one fence for its eight MMAs
+                        for (int jj = 0; jj < 4 && ok; ++jj) {
+                            const int vv = v + jj;
+                            if (vv >= NSLOT)
+                                ok = mbar_wait_bounded(&slot_free[vv % NSLOT], uint32_t(vv / NSLOT - 1) & 1u,
+                                                       a.limit_ns);
+                        }
+                        if (!ok) break;
+                        tc_fence_after();
+                        for (int jj = 0; jj < 4; ++jj, ++v) {
                             const int j = 4 * h + jj;  // sub-block of the step
                             const int slot = v % NSLOT;
-                            if (v >= NSLOT)
-                                ok = mbar_wait_bounded(&slot_free[slot], uint32_t(v / NSLOT - 1) & 1u, a.limit_ns);
-                            if (!ok) break;
-                            tc_fence_after();
                             const uint32_t koff = uint32_t(j & 1) * 64;
                             const uint32_t ab = ah + uint32_t(jj >> 1) * kMmqAtom + koff;
                             const uint32_t bb = baddr + uint32_t(j >> 1) * (NP * 128) + koff;
                             const uint32_t d = tmem + uint32_t(slot * NP);
                             umma_f16(d, umma_desc_sw128(ab), umma_desc_sw128(bb), idesc, false);
                             umma_f16(d, umma_desc_sw128(ab + 32), umma_desc_sw128(bb + 32), idesc, true);
-                            umma_commit(&slot_full[slot]);
                         }
                         if (ok) umma_commit(&a_free[b]);  // this half's A buffer may be rewritten
                     }
-                    if (ok) umma_commit(&empty[s]);  // this step's activation image has been read
+                    if (ok) {
+                        // one commit per step for its eight slots (a commit per sub-block
+                        // serialized the issue of these small MMAs), and the stage
+                        umma_commit(&acc_full[g % NGRP]);
+                        umma_commit(&empty[s]);  // this step's activation image has been read
+                    }
                 }
             }
             if (!ok) abort_flag = 1;
-            if (v > 0)  // the last MMAs complete before TMEM is freed
-                (void)mbar_wait_bounded(&slot_full[(v - 1) % NSLOT], uint32_t((v - 1) / NSLOT) & 1u, a.limit_ns);
+            if (g > 0)  // the last MMAs complete before TMEM is freed
+                (void)mbar_wait_bounded(&acc_full[(g - 1) % NGRP], uint32_t((g - 1) / NGRP) & 1u, a.limit_ns);
         }
     } else if (warp < 10) {
         // ---- converters: thread = row r of the tile; group h converts half h of every step
@@ -396,15 +423,15 @@ __global__ void __launch_bounds__(kMmqThreads, 1)
                     }
                 }
                 const float4* scj = reinterpret_cast<const float4*>(st + kMmqRaw + NP * 512);
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait_bounded(&acc_full[g % NGRP], uint32_t(g / NGRP) & 1u, a.limit_ns))) {
+                    stop = true;
+                    break;
+                }
+                tc_fence_after();
 #pragma unroll
                 for (int jj = 0; jj < 8; ++jj, ++v) {
                     const int slot = v % NSLOT;
-                    if (!__all_sync(0xffffffffu,
-                                    mbar_wait_bounded(&slot_full[slot], uint32_t(v / NSLOT) & 1u, a.limit_ns))) {
-                        stop = true;
-                        break;
-                    }
-                    tc_fence_after();
                     const uint64_t ds2 = pack2(ds[jj], ds[jj]), ndm2 = pack2(-dm[jj], -dm[jj]);
                     const float4* dqv = scj + (2 * jj) * (NP / 4);       // dq of the sub-block's columns
                     const float4* dqsv = scj + (2 * jj + 1) * (NP / 4);  // dq*sumq
