@@ -161,10 +161,11 @@ def measured_bf16_peak():
         return 1900.0
 
 
-def kernel_source_sha() -> str:
+def kernel_source_sha(files=None) -> str:
+    """Hash of the named kernel source files (default: every file of csrc/)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "quantized_decode_matvec_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(files if files else os.listdir(csrc)):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
@@ -172,7 +173,8 @@ def kernel_source_sha() -> str:
 
 
 def recorded_traffic(profile_name: str):
-    """DRAM bytes per launch recorded from an ncu capture, if taken on the current kernel source."""
+    """DRAM bytes per launch from an ncu capture summarized in profiles/, if the source files the
+    summary lists (its `source_files` line) still hash to its `kernel_source_sha`; else None."""
     path = os.path.join(ROOT, "profiles", profile_name)
     try:
         fields = {}
@@ -181,11 +183,12 @@ def recorded_traffic(profile_name: str):
                 if ":" in line and line.strip().startswith("- "):
                     k, v = line.strip()[2:].split(":", 1)
                     fields[k.strip()] = v.strip().strip("`")
-        if fields.get("kernel_source_sha") == kernel_source_sha():
-            return float(fields["dram_bytes_per_launch"])
+        files = [x.strip() for x in fields.get("source_files", "").split(",") if x.strip()] or None
+        if fields.get("kernel_source_sha") == kernel_source_sha(files):
+            return float(fields["dram_bytes_per_launch"]), fields.get("traffic_note")
     except Exception:
         pass
-    return None
+    return None, None
 
 
 def build_step(case, device, mq, host=None):
@@ -782,11 +785,13 @@ def run_ours(args):
     peak, peak_kind = measured_hbm_peak()
     act_bytes = case.n_layers * (3 * case.H * 4 + case.I // 32 * 34 * 2) * case.ncols
     out_bytes = case.n_layers * (case.qkv_rows + case.H + case.H) * 4 * case.ncols
+    traffic_step, traffic_note_step = recorded_traffic("step_kernel_7B.md")
     if args.mode == "persistent":
         step_bytes = wbytes + act_bytes + out_bytes
         gbs = step_bytes / (ms_local / 1e3) / 1e9
         roofline = {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
-                    "traffic": recorded_traffic("step_kernel_7B.md"),
+                    "traffic": traffic_step,
+                    "traffic_source": traffic_note_step,
                     "kernel": "step_kernel<1> (persistent: all 28 layers, one launch per step)",
                     "peak_kind": f"{peak_kind} (copy bandwidth)", "avg_launch_us": ms_local * 1e3,
                     "algorithmic_bytes_per_launch": step_bytes}
@@ -808,7 +813,7 @@ def run_ours(args):
                     + case.I // 32 * 34 * case.ncols)
         gu_gbs = gu_bytes / (gu_ms / 1e3) / 1e9
         roofline = {"bound": "hbm", "achieved": gu_gbs, "peak": peak, "unit": "GB/s", "frac": gu_gbs / peak,
-                    "traffic": recorded_traffic("ffn_gate_up_7B.md"),
+                    "traffic": recorded_traffic("ffn_gate_up_7B.md")[0],
                     "kernel": "ring_kernel<1,GU> (ffn_gu matvec + SiLU*mul + q8_0 of h), 37888x3584",
                     "peak_kind": f"{peak_kind} (copy bandwidth)", "avg_launch_us": gu_ms * 1e3,
                     "algorithmic_bytes_per_launch": gu_bytes}
