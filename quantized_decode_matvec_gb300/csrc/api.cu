@@ -138,9 +138,41 @@ bool plan_mv(int64_t rows, int K, int nc, int kind, int I, const DeviceInfo& dev
 //    columns up, slower at 3 and 4, where the unit lanes' once-per-unit scale
 //    unpacking wins.)
 // Returns false when the segments do not fit in the warps.
+// 3..8 columns of q4_K weights as column groups where the split fits
+constexpr bool kColumnGroups = true;
+
 static bool unit_split(int C, int nc, bool allow_cols, MvPlan& q)
 {
     q.cmap = 0;
+    q.cgw = q.cgu = 0;
+    if (nc >= 3 && allow_cols && kColumnGroups) {
+        // column groups: (nc+1)/2 groups of 15/groups warps, each group split as
+        // the two-column consumer would split its warps
+        const int ng = (nc + 1) / 2, wpg = 15 / ng;
+        double best = 0.0;
+        for (const int L : {32, 16, 8, 4}) {
+            int nseg = (C + L - 1) / L;
+            const int S = (C + nseg - 1) / nseg;
+            nseg = (C + S - 1) / S;
+            if (nseg > wpg) continue;
+            const int used = nseg * (wpg / nseg);
+            const double score = double(C) / double(nseg * L) * double(used) / double(wpg);
+            if (score > best + 1e-9) {
+                best = score;
+                q.L = L;
+                q.nseg = nseg;
+                q.S = S;
+                q.cgu = used;
+            }
+        }
+        if (best > 0.0) {
+            q.cgw = wpg;
+            q.nwc = ng * wpg;
+            q.rg = (q.cgu / q.nseg) * (32 / q.L);
+            return true;
+        }
+        q.cgu = 0;
+    }
     if (nc >= 5 && allow_cols) {
         const int lu = 32 / (nc <= 4 ? 4 : 8);
         int nseg = (C + lu - 1) / lu;
@@ -615,7 +647,10 @@ static mq_status launch_ffn(const mq_ffn_desc* d_desc, int32_t H, int32_t I, int
     if (!mq::plan_mv(H, I, ncols, mq::KIND_DOWN, 0, *dev, &pd)) return MQ_ERR_UNSUPPORTED;
     cudaError_t e = mq::launch_gu(d_desc, H, I, ncols, pg, dev->status, s, pdl);
     if (e != cudaSuccess) return cuda_fail(e);
-    e = mq::launch_mv(d_desc, mq::KIND_DOWN, H, I, ncols, pd, dev->status, s, pdl);
+    // the down launch always under programmatic dependent launch: its weight
+    // copies start while gate/up drains, and it reads h only after its
+    // grid-dependency wait
+    e = mq::launch_mv(d_desc, mq::KIND_DOWN, H, I, ncols, pd, dev->status, s, true);
     return e == cudaSuccess ? MQ_OK : cuda_fail(e);
 }
 

@@ -33,6 +33,10 @@ struct MvPlan {
     int fault;         // test-only: FAULT_* injected by the ring kernels (0 = none)
     int wait_ms;       // limit of every mbarrier wait of the ring kernels
     int cmap;          // 1: column lanes (3..8 columns, ring_consume_cols), 0: unit lanes
+    // column groups (3..8 columns, q4_K): the consumer warps form groups of cgw
+    // warps, group g on columns 2g, 2g+1 with their activation in registers (the
+    // one- and two-column consumer), cgu of each group's warps with work; 0: off
+    int cgw, cgu;
 };
 
 // Plan of the persistent step kernel: one ring plan per phase (qkv, o, gate/up,

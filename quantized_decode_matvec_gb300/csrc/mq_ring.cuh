@@ -16,6 +16,7 @@ namespace mq {
 // kMode: 0 = unit lanes, the kernel built for 1..2 columns (16 warps) or the
 // 9-warp form; 1 = column lanes (16 warps); 2 = unit lanes for 3..8 columns
 // with 16 warps (activation columns read from shared memory per row pair)
+// 3 = column groups (16 warps; see ring_consume_groups)
 template <int NC, int kMode = 0>
 __host__ __device__ constexpr int ring_max_warps()
 {
@@ -67,11 +68,14 @@ struct ConsumeArgs {
     int nrows;      // the CTA's rows of this matrix
     int tile_base;  // ring position of the matrix's first tile
     int nwc_used;   // consumer warps with work (the others only hand tiles back)
+    // partials: part[(row * nseg + seg) * pcols + pc0 + c] for the consumer's
+    // columns c; warps are numbered from warp0 (a column group's first warp)
+    int pcols, pc0, warp0;
 };
 
-__device__ __forceinline__ ConsumeArgs consume_args(const MvPlan& p, int nrows, int tile_base, int nwc_used)
+__device__ __forceinline__ ConsumeArgs consume_args(const MvPlan& p, int nrows, int tile_base, int nwc_used, int pcols)
 {
-    return ConsumeArgs{p.C, p.L, p.nseg, p.S, p.rg, p.T, p.ns, p.stage_bytes, nrows, tile_base, nwc_used};
+    return ConsumeArgs{p.C, p.L, p.nseg, p.S, p.rg, p.T, p.ns, p.stage_bytes, nrows, tile_base, nwc_used, pcols, 0, 0};
 }
 
 // (not inlined: called once per matrix, it keeps its own register allocation
@@ -82,7 +86,7 @@ __device__ __noinline__ bool ring_consume_L(const ConsumeArgs p, const uint8_t* 
                                             uint64_t limit_ns)
 {
     const int nrows = p.nrows, nwc_used = p.nwc_used;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = (threadIdx.x >> 5) - p.warp0, lane = threadIdx.x & 31;
     const int nseg = p.nseg;
     const int seg = warp % nseg, jj = warp / nseg;
     constexpr int ipw = 32 / L;
@@ -119,7 +123,7 @@ __device__ __noinline__ bool ring_consume_L(const ConsumeArgs p, const uint8_t* 
     // lane L/2 row r + rg + sub's (group_sum2); one pointer, advanced per step
     const bool storer = l == 0 || l == (L >> 1);
     const int srow = sub + (l == 0 ? 0 : rg);
-    const int pstep = 2 * rg * nseg * NC;
+    const int pstep = 2 * rg * nseg * p.pcols;
 
     int s = p.tile_base % p.ns;  // ring stage and its parity, advanced per tile
     uint32_t par = uint32_t(p.tile_base / p.ns) & 1u;
@@ -128,7 +132,7 @@ __device__ __noinline__ bool ring_consume_L(const ConsumeArgs p, const uint8_t* 
         if (!ok) return false;
         const uint8_t* stage = ring + uint32_t(s) * uint32_t(p.stage_bytes);
         const int tn = min(p.T, nrows - tr0);
-        float* pq = part + (size_t(tr0 + rho0 + srow) * nseg + seg) * NC;
+        float* pq = part + (size_t(tr0 + rho0 + srow) * nseg + seg) * p.pcols + p.pc0;
         for (int r = warp_active ? rho0 : tn; r < tn; r += 2 * rg, pq += pstep) {  // r is warp-uniform
             const int ra = r + sub, rb = r + rg + sub;
             const bool st = storer && r + srow < tn;
@@ -251,13 +255,51 @@ __device__ __noinline__ bool ring_consume_cols(const ConsumeArgs p, const uint8_
     return true;
 }
 
-// kMode 1: the kernel was built for column lanes (its plans all have cmap = 1)
+// Column groups (3..8 columns): the consumer warps split into groups of
+// p.cgw warps; group g runs the one- or two-column consumer (activation in
+// registers, the row loop without branches) on columns 2g and 2g+1 of every
+// tile, so each group reads and unpacks the tile's weights once for its
+// columns.  Warps past the last group only hand the tiles back.  The unit
+// split, partials and combine order are those of the plan (the same for every
+// group).
+template <int NC, class Fmt>
+__device__ __forceinline__ bool ring_consume_groups(ConsumeArgs a, int cgw, const uint8_t* ring, uint64_t* full,
+                                                    uint64_t* empty, const UnitAct& act, float* __restrict__ part,
+                                                    uint64_t limit_ns)
+{
+    constexpr int NG = (NC + 1) / 2;
+    const int g = (int(threadIdx.x) >> 5) / cgw;
+    const int c0 = 2 * g;
+    a.pc0 = c0;
+    a.warp0 = g * cgw;
+    if (g >= NG) a.nwc_used = 0;
+    // the group's columns as a view of the activation (each column's planes and
+    // scales are contiguous in the unit layout)
+    const int gc = g < NG ? c0 : 0;
+    const UnitAct v{act.planes + size_t(gc) * 8 * act.U, act.scales + size_t(gc) * act.U * 2, act.U};
+    const bool two = g < NG && c0 + 1 < NC;
+#define MQ_GROUP_L(LL)                                                                      \
+    return two ? ring_consume_L<2, LL, Fmt>(a, ring, full, empty, v, part, limit_ns)        \
+               : ring_consume_L<1, LL, Fmt>(a, ring, full, empty, v, part, limit_ns);
+    if (a.L == 32) { MQ_GROUP_L(32) }
+    if (a.L == 16) { MQ_GROUP_L(16) }
+    if (a.L == 8) { MQ_GROUP_L(8) }
+    MQ_GROUP_L(4)
+#undef MQ_GROUP_L
+}
+
+// kMode 1: the kernel was built for column lanes (its plans all have cmap = 1);
+// kMode 3: for column groups (cgw > 0)
 template <int NC, class Fmt = FmtQ4K, int kMode = 0>
 __device__ __forceinline__ bool ring_consume(const MvPlan& p, int nrows, int tile_base, int nwc_used,
                                              const uint8_t* ring, uint64_t* full, uint64_t* empty,
                                              const UnitAct& act, float* __restrict__ part, uint64_t limit_ns)
 {
-    const ConsumeArgs a = consume_args(p, nrows, tile_base, nwc_used);
+    const ConsumeArgs a = consume_args(p, nrows, tile_base, nwc_used, NC);
+    if constexpr (kMode == 3) {
+        ConsumeArgs ag = consume_args(p, nrows, tile_base, p.cgu, NC);
+        return ring_consume_groups<NC, Fmt>(ag, p.cgw, ring, full, empty, act, part, limit_ns);
+    }
     if constexpr (kMode == 1) return ring_consume_cols<NC, Fmt>(a, ring, full, empty, act, part, limit_ns);
     if (p.L == 32) return ring_consume_L<NC, 32, Fmt>(a, ring, full, empty, act, part, limit_ns);
     if (p.L == 16) return ring_consume_L<NC, 16, Fmt>(a, ring, full, empty, act, part, limit_ns);

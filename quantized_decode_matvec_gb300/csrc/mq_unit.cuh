@@ -23,6 +23,10 @@
 namespace mq {
 
 constexpr int kUnitElems = 128;
+// q8_0 activations staged from global memory one thread per block (true) or
+// one warp per unit (fp32 activations: always one warp per unit, which
+// measured faster for them)
+constexpr bool kBlockStaging = true;
 
 struct UnitAct {
     uint4* planes;
@@ -61,6 +65,61 @@ __device__ __forceinline__ int group8_sum(int v)
     v += __shfl_xor_sync(0xffffffffu, v, 1);
     v += __shfl_xor_sync(0xffffffffu, v, 2);
     return v + __shfl_xor_sync(0xffffffffu, v, 4);
+}
+
+// One q8_0 block's place in the unit layout: block J of column c is slot J % 4
+// of unit J / 4; its 32 codes are planes 2*slot and 2*slot + 1 of that unit.
+__device__ __forceinline__ void put_block(UnitAct s, int c, int J, const uint32_t (&w)[8], float dq, int sq)
+{
+    const int u = J >> 2, slot = J & 3;
+    s.planes[size_t(c * 8 + 2 * slot) * s.U + u] = make_uint4(w[0], w[1], w[2], w[3]);
+    s.planes[size_t(c * 8 + 2 * slot + 1) * s.U + u] = make_uint4(w[4], w[5], w[6], w[7]);
+    float* S = reinterpret_cast<float*>(s.scales + (size_t(c) * s.U + u) * 2);
+    S[slot] = dq;
+    S[4 + slot] = dq * float(sq);
+}
+
+// From q8_0 blocks in global memory, one thread per block (xq 4-byte aligned,
+// K % 256 == 0): block J of a column starts at byte 34J, i.e. on a word
+// boundary (J even) or two bytes past one (J odd); nine aligned words hold it
+// either way.  A thread's blocks are loaded before any is used.
+// sumq_out (nullable, test export): int32 [NC][K/32].  (Not inlined: it keeps
+// its own register allocation, apart from the kernels' hot loops.)
+template <int NC>
+__device__ __noinline__ void stage_blocks_q8(const uint8_t* __restrict__ xq, int K, UnitAct s, int32_t* sumq_out,
+                                                int tid, int nthr)
+{
+    const int nq = K / kQK8, total = NC * nq;
+    constexpr int B = 2;
+    for (int t0 = tid; t0 < total; t0 += B * nthr) {
+        uint32_t w[B][9];
+#pragma unroll
+        for (int k = 0; k < B; ++k) {
+            const int t = t0 + k * nthr;
+            if (t < total) {
+                const uint32_t* p = reinterpret_cast<const uint32_t*>(xq + (size_t(t) * kQ8Bytes & ~size_t(3)));
+#pragma unroll
+                for (int i = 0; i < 9; ++i) w[k][i] = __ldg(p + i);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < B; ++k) {
+            const int t = t0 + k * nthr;
+            if (t >= total) break;
+            const int c = t / nq, J = t - c * nq;
+            const bool odd = (J & 1) != 0;
+            uint32_t cw[8];
+            int sq = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                cw[i] = odd ? w[k][i + 1] : __funnelshift_r(w[k][i], w[k][i + 1], 16);
+                sq = __dp4a(int(cw[i]), 0x01010101, sq);
+            }
+            const float dq = __half2float(__ushort_as_half(uint16_t(odd ? w[k][0] >> 16 : w[k][0])));
+            put_block(s, c, J, cw, dq, sq);
+            if (sumq_out) sumq_out[t] = sq;
+        }
+    }
 }
 
 // q8_0 blocks, one thread per block: the form for a 2-byte aligned xq.
@@ -104,6 +163,10 @@ __device__ __forceinline__ void stage_units_q8(const uint8_t* __restrict__ xq, i
 {
     if (reinterpret_cast<uintptr_t>(xq) & 3) {
         stage_units_q8_by_block<NC>(xq, K, s, sumq_out, tid, nthr);
+        return;
+    }
+    if (kBlockStaging) {
+        stage_blocks_q8<NC>(xq, K, s, sumq_out, tid, nthr);
         return;
     }
     const int lane = tid & 31, warp = tid >> 5, nw = nthr >> 5;

@@ -38,7 +38,7 @@ cudaError_t launch_ring(const void* desc, int kind, int a, int b, int ncols, con
                         cudaStream_t s, bool pdl)
 {
     // 3..8 columns beyond 8 consumer warps: the 16-warp instances
-    if (ncols >= 3 && (p.cmap || p.block > 32 * ring_max_warps<3>()))
+    if (ncols >= 3 && (p.cmap || p.cgw || p.block > 32 * ring_max_warps<3>()))
         return launch_ring_cols(desc, kind, a, b, ncols, p, status, s, pdl);
     if (p.block > 32 * (ncols <= 2 ? ring_max_warps<1>() : ring_max_warps<3>())) return cudaErrorInvalidConfiguration;
     switch (kind) {

@@ -1,7 +1,8 @@
 // ring_cols.cu -- the q4_K ring kernels for 3..8 activation columns, all with
-// 16 warps: column lanes (kMode 1, every column's activation in registers;
-// see ring_consume_cols) or unit lanes (kMode 2), in a translation unit of
-// their own.
+// 16 warps: column groups (kMode 3, two columns per warp group with their
+// activation in registers; see ring_consume_groups), column lanes (kMode 1,
+// every column's activation in registers; see ring_consume_cols) or unit lanes
+// (kMode 2), in a translation unit of their own.
 #include "mq_ring_kernel.cuh"
 
 namespace mq {
@@ -33,7 +34,13 @@ cudaError_t launch_ring_cols(const void* desc, int kind, int a, int b, int ncols
                              cudaStream_t s, bool pdl)
 {
     if (ncols < 3 || p.block > 32 * ring_max_warps<3, 1>()) return cudaErrorInvalidConfiguration;
-    if (p.cmap) {
+    if (p.cgw) {
+        switch (kind) {
+            case KIND_MV: return launch_cols_kind<KIND_MV, 3>(desc, a, b, ncols, p, status, s, pdl);
+            case KIND_DOWN: return launch_cols_kind<KIND_DOWN, 3>(desc, a, b, ncols, p, status, s, pdl);
+            case KIND_GU: return launch_cols_kind<KIND_GU, 3>(desc, a, b, ncols, p, status, s, pdl);
+        }
+    } else if (p.cmap) {
         switch (kind) {
             case KIND_MV: return launch_cols_kind<KIND_MV, 1>(desc, a, b, ncols, p, status, s, pdl);
             case KIND_DOWN: return launch_cols_kind<KIND_DOWN, 1>(desc, a, b, ncols, p, status, s, pdl);
@@ -56,7 +63,8 @@ cudaError_t set_ring_cols_attributes(int max_smem)
     if (e == cudaSuccess) e = set_max_dyn_smem(reinterpret_cast<const void*>(ring_kernel<N, K, FmtQ4K, M>), max_smem);
 #define MQ_SET(N)                                                                              \
     MQ_SET1(N, KIND_MV, 1) MQ_SET1(N, KIND_DOWN, 1) MQ_SET1(N, KIND_GU, 1) MQ_SET1(N, KIND_MV, 2) \
-        MQ_SET1(N, KIND_DOWN, 2) MQ_SET1(N, KIND_GU, 2)
+        MQ_SET1(N, KIND_DOWN, 2) MQ_SET1(N, KIND_GU, 2) MQ_SET1(N, KIND_MV, 3) MQ_SET1(N, KIND_DOWN, 3) \
+            MQ_SET1(N, KIND_GU, 3)
     MQ_SET(3) MQ_SET(4) MQ_SET(5) MQ_SET(6) MQ_SET(7) MQ_SET(8)
 #undef MQ_SET
 #undef MQ_SET1
