@@ -118,8 +118,29 @@ bool plan_mv(int64_t rows, int K, int nc, int kind, int I, const DeviceInfo& dev
     q.block = int(32 * nw);
     q.smem = int(smem);
     q.variant = 0;
+    q.ksplit = 1;
     if (ring_only || variant_policy() != VARIANT_FORCE_REGISTER)
         plan_ring(q, units, kind, nc, dev, unit_bytes, !ring_only);  // column lanes: q4_K only
+    if (q.variant == 0 && !ring_only && kind != KIND_GU && variant_policy() != VARIANT_FORCE_REGISTER) {
+        // the whole activation does not fit beside a ring (e.g. eight columns of
+        // K = 18944): split K into 2..4 equal parts of whole super-blocks, one
+        // ring launch each, one CTA per SM
+        const int sb = K / 256;  // super-blocks per row
+        for (int ks = 2; ks <= 4; ++ks) {
+            if (sb % ks) continue;
+            MvPlan qs = q;
+            qs.C = (K / ks) / 64;
+            qs.grid = int(units < dev.num_sms ? units : dev.num_sms);
+            qs.rows_per_cta = int((units + qs.grid - 1) / qs.grid);
+            plan_ring(qs, units, kind, nc, dev, unit_bytes, true);
+            if (qs.variant == 1) {
+                qs.ksplit = ks;
+                qs.kpn = sb / ks;
+                q = qs;
+                break;
+            }
+        }
+    }
     *p = q;
     return true;
 }

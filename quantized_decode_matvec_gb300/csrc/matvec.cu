@@ -126,6 +126,19 @@ static cudaError_t launch_mv_kind(const void* desc, int rows, int K, int ncols, 
 cudaError_t launch_mv(const void* desc, int kind, int rows, int K, int ncols, const MvPlan& p, unsigned* status,
                       cudaStream_t s, bool pdl)
 {
+    if (p.variant == 1 && p.ksplit > 1) {
+        // K split: the parts in stream order, each after its predecessor's
+        // grid-dependency wait (programmatic dependent launch), the later ones
+        // adding to y
+        for (int i = 0; i < p.ksplit; ++i) {
+            MvPlan pi = p;
+            pi.kp0 = i * p.kpn;
+            pi.kacc = i > 0 ? 1 : 0;
+            const cudaError_t e = launch_ring(desc, kind, rows, K, ncols, pi, status, s, i > 0 || pdl);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    }
     if (p.variant == 1) return launch_ring(desc, kind, rows, K, ncols, p, status, s, pdl);
     if (kind == KIND_MV) return launch_mv_kind<KIND_MV>(desc, rows, K, ncols, p, status, s, pdl);
     return launch_mv_kind<KIND_DOWN>(desc, rows, K, ncols, p, status, s, pdl);

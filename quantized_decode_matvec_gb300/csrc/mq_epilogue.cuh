@@ -10,16 +10,19 @@ namespace mq {
 // y[c][r0 + lr] = sum over segments, in segment order, of part[(lr*nseg+seg)*NC + c]
 // rec (nullable): each output also as a tagged record rec[c*R + r0 + lr] (the
 // value's bits and `tag` in one 8-byte store), for a reader in the same launch
+// acc: y += the sum (a later part of a K split; y holds the earlier parts' sum)
 template <int NC>
 __device__ __forceinline__ void mv_epilogue(const float* __restrict__ part, int nseg, int nrows, int r0,
                                             float* __restrict__ y, int y_ld, int tid, int nthr,
-                                            uint64_t* __restrict__ rec = nullptr, int R = 0, uint32_t tag = 0)
+                                            uint64_t* __restrict__ rec = nullptr, int R = 0, uint32_t tag = 0,
+                                            bool acc = false)
 {
     for (int t = tid; t < NC * nrows; t += nthr) {
         const int c = t / nrows, lr = t - c * nrows;
         float s = 0.0f;
         for (int g = 0; g < nseg; ++g) s += part[(lr * nseg + g) * NC + c];
-        y[size_t(c) * y_ld + r0 + lr] = s;
+        float* yp = y + size_t(c) * y_ld + r0 + lr;
+        *yp = acc ? *yp + s : s;
         if (rec) st_tagged(rec + size_t(c) * R + r0 + lr, __float_as_uint(s), tag);
     }
 }

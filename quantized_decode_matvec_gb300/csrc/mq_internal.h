@@ -37,6 +37,12 @@ struct MvPlan {
     // warps, group g on columns 2g, 2g+1 with their activation in registers (the
     // one- and two-column consumer), cgu of each group's warps with work; 0: off
     int cgw, cgu;
+    // K split (matvec and down, q4_K, when one launch cannot stage the whole
+    // activation): ksplit launches in stream order, each over kpn super-blocks
+    // of every row starting at super-block kp0; launch i > 0 adds its sums to y
+    // (kacc = 1), so y = ((part 0) + part 1) + ... in that order.  kpn = 0: the
+    // whole row in one launch.
+    int ksplit, kp0, kpn, kacc;
 };
 
 // Plan of the persistent step kernel: one ring plan per phase (qkv, o, gate/up,

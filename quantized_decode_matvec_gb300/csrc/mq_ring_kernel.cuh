@@ -102,6 +102,12 @@ __global__ void __launch_bounds__(32 * ring_max_warps<NC, kMode>(), 1)
             return int64_t(r0) + lr;
     };
     const size_t row_bytes = Fmt::row_bytes(K / kUnitElems);
+    // K split: this launch streams super-blocks [sb0, sb0 + nsb) of every row,
+    // one bulk copy per row into tile rows of tile_row bytes
+    const int sb0 = p.kpn ? p.kp0 : 0;
+    const bool split = p.kpn != 0;
+    const size_t tile_row = split ? Fmt::row_bytes(2 * p.kpn) : row_bytes;
+    const size_t src_off = Fmt::row_bytes(2 * sb0);
     const int ntiles = (nrows + p.T - 1) / p.T;
 
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -134,10 +140,15 @@ __global__ void __launch_bounds__(32 * ring_max_warps<NC, kMode>(), 1)
             if (i == withheld) return;
             const int s = i % p.ns;
             const int lr0 = i * p.T, tn = min(p.T, nrows - lr0);
-            mbar_arrive_expect_tx(&full[s], uint32_t(size_t(tn) * row_bytes));
+            mbar_arrive_expect_tx(&full[s], uint32_t(size_t(tn) * tile_row));
             uint8_t* dst = ring + size_t(s) * p.stage_bytes;
             int a = lr0;
             const int e = lr0 + tn;
+            if (split) {  // part of each row: one copy per row
+                for (; a < e; ++a)
+                    bulk_copy_g2s_evict_first(dst + size_t(a - lr0) * tile_row, W + size_t(rowmap(a)) * row_bytes + src_off,
+                                              uint32_t(tile_row), &full[s], wpolicy);
+            }
             while (a < e) {  // one copy per run of contiguous matrix rows (gate/up: at most two)
                 int stop = e;
                 if (KIND == KIND_GU && a < n && e > n) stop = n;
@@ -175,10 +186,17 @@ __global__ void __launch_bounds__(32 * ring_max_warps<NC, kMode>(), 1)
         // ---- consumers: activation first (it may come from the predecessor), then the ring
         griddep_wait();
         const int ctid = threadIdx.x, cthr = p.nwc * 32;
-        if (x)
-            stage_units_x<NC>(x, K, act, (KIND == KIND_MV && blockIdx.x == 0) ? xq_out : nullptr, nullptr, ctid, cthr);
-        else
+        uint8_t* const xo = (KIND == KIND_MV && blockIdx.x == 0) ? xq_out : nullptr;
+        if (split) {
+            if (x)
+                stage_units_x_range<NC>(x, K, sb0 * kQK, p.kpn * kQK, act, xo, ctid, cthr);
+            else
+                stage_q8_range<NC>(xq, K / kQK8, sb0 * (kQK / kQK8), p.kpn * (kQK / kQK8), act, ctid, cthr);
+        } else if (x) {
+            stage_units_x<NC>(x, K, act, xo, nullptr, ctid, cthr);
+        } else {
             stage_units_q8<NC>(xq, K, act, nullptr, ctid, cthr);
+        }
         named_barrier_sync(1, cthr);
         named_barrier_arrive(2, cthr + 32);  // release the producer's remaining ring tiles
         if (!ring_consume<NC, Fmt, kMode>(p, nrows, 0, p.nwc, ring, full, empty, act, part, limit_ns) && lane == 0)
@@ -196,7 +214,7 @@ __global__ void __launch_bounds__(32 * ring_max_warps<NC, kMode>(), 1)
         float* vals = reinterpret_cast<float*>(smem + p.off_vals);
         gu_epilogue<NC>(part, vals, p.nseg, n, i0, R, static_cast<uint8_t*>(fd->h_q8), fd->gu_dbg, fd->h_dbg);
     } else {
-        mv_epilogue<NC>(part, p.nseg, nrows, r0, y, y_ld, threadIdx.x, blockDim.x);
+        mv_epilogue<NC>(part, p.nseg, nrows, r0, y, y_ld, threadIdx.x, blockDim.x, nullptr, 0, 0, p.kacc != 0);
     }
 }
 

@@ -85,11 +85,13 @@ __device__ __forceinline__ void put_block(UnitAct s, int c, int J, const uint32_
 // either way.  A thread's blocks are loaded before any is used.
 // sumq_out (nullable, test export): int32 [NC][K/32].  (Not inlined: it keeps
 // its own register allocation, apart from the kernels' hot loops.)
+// Blocks [j0, j0 + nqr) of each column of nq_all blocks (K split: one part of
+// every row; otherwise j0 = 0, nqr = nq_all), staged as units 0 .. nqr/4 - 1.
 template <int NC>
-__device__ __noinline__ void stage_blocks_q8(const uint8_t* __restrict__ xq, int K, UnitAct s, int32_t* sumq_out,
-                                                int tid, int nthr)
+__device__ __noinline__ void stage_blocks_q8(const uint8_t* __restrict__ xq, int nq_all, int j0, int nqr, UnitAct s,
+                                                int32_t* sumq_out, int tid, int nthr)
 {
-    const int nq = K / kQK8, total = NC * nq;
+    const int nq = nqr, total = NC * nq;
     constexpr int B = 2;
     for (int t0 = tid; t0 < total; t0 += B * nthr) {
         uint32_t w[B][9];
@@ -97,7 +99,9 @@ __device__ __noinline__ void stage_blocks_q8(const uint8_t* __restrict__ xq, int
         for (int k = 0; k < B; ++k) {
             const int t = t0 + k * nthr;
             if (t < total) {
-                const uint32_t* p = reinterpret_cast<const uint32_t*>(xq + (size_t(t) * kQ8Bytes & ~size_t(3)));
+                const int c = t / nq;
+                const size_t tg = size_t(c) * nq_all + j0 + (t - c * nq);  // the block's index in xq
+                const uint32_t* p = reinterpret_cast<const uint32_t*>(xq + (tg * kQ8Bytes & ~size_t(3)));
 #pragma unroll
                 for (int i = 0; i < 9; ++i) w[k][i] = __ldg(p + i);
             }
@@ -107,7 +111,7 @@ __device__ __noinline__ void stage_blocks_q8(const uint8_t* __restrict__ xq, int
             const int t = t0 + k * nthr;
             if (t >= total) break;
             const int c = t / nq, J = t - c * nq;
-            const bool odd = (J & 1) != 0;
+            const bool odd = ((size_t(c) * nq_all + j0 + J) & 1) != 0;
             uint32_t cw[8];
             int sq = 0;
 #pragma unroll
@@ -124,13 +128,13 @@ __device__ __noinline__ void stage_blocks_q8(const uint8_t* __restrict__ xq, int
 
 // q8_0 blocks, one thread per block: the form for a 2-byte aligned xq.
 template <int NC>
-__device__ __forceinline__ void stage_units_q8_by_block(const uint8_t* __restrict__ xq, int K, UnitAct s,
-                                                        int32_t* sumq_out, int tid, int nthr)
+__device__ __forceinline__ void stage_units_q8_by_block(const uint8_t* __restrict__ xq, int nq_all, int j0, int nqr,
+                                                        UnitAct s, int32_t* sumq_out, int tid, int nthr)
 {
-    const int nq = K / kQK8;
+    const int nq = nqr;
     for (int t = tid; t < NC * nq; t += nthr) {
         const int c = t / nq, J = t - c * nq;
-        const uint16_t* h = reinterpret_cast<const uint16_t*>(xq + (size_t(c) * nq + J) * kQ8Bytes);
+        const uint16_t* h = reinterpret_cast<const uint16_t*>(xq + (size_t(c) * nq_all + j0 + J) * kQ8Bytes);
         uint16_t v[17];
 #pragma unroll
         for (int k = 0; k < 17; ++k) v[k] = __ldg(h + k);
@@ -162,11 +166,11 @@ __device__ __forceinline__ void stage_units_q8(const uint8_t* __restrict__ xq, i
                                                int tid, int nthr)
 {
     if (reinterpret_cast<uintptr_t>(xq) & 3) {
-        stage_units_q8_by_block<NC>(xq, K, s, sumq_out, tid, nthr);
+        stage_units_q8_by_block<NC>(xq, K / kQK8, 0, K / kQK8, s, sumq_out, tid, nthr);
         return;
     }
     if (kBlockStaging) {
-        stage_blocks_q8<NC>(xq, K, s, sumq_out, tid, nthr);
+        stage_blocks_q8<NC>(xq, K / kQK8, 0, K / kQK8, s, sumq_out, tid, nthr);
         return;
     }
     const int lane = tid & 31, warp = tid >> 5, nw = nthr >> 5;
@@ -222,8 +226,9 @@ __device__ __forceinline__ void stage_units_q8(const uint8_t* __restrict__ xq, i
 // column c (lane l = tid & 31).
 template <int NC, typename Loader>
 __device__ __forceinline__ void stage_units_f32(Loader load, int K, UnitAct s, uint8_t* __restrict__ xq_out,
-                                                int32_t* sumq_out, int tid, int nthr)
+                                                int32_t* sumq_out, int tid, int nthr, int xq_ld = 0)
 {
+    // xq_out: block j of column c at block c*xq_ld + j (xq_ld = 0: K/32)
     const int lane = tid & 31, warp = tid >> 5, nw = nthr >> 5;
     const int nq = K / kQK8, U = s.U;
     const int slot = lane >> 3, g = lane & 7;
@@ -277,7 +282,7 @@ __device__ __forceinline__ void stage_units_f32(Loader load, int K, UnitAct s, u
             }
             if (xq_out) {
                 auto put_q8 = [&](int uu, __half h, uint32_t cd) {
-                    uint8_t* ob = xq_out + (size_t(c) * nq + 4 * uu + slot) * kQ8Bytes;
+                    uint8_t* ob = xq_out + (size_t(c) * (xq_ld ? xq_ld : nq) + 4 * uu + slot) * kQ8Bytes;
                     if (g == 0) *reinterpret_cast<uint16_t*>(ob) = __half_as_ushort(h);
                     uint16_t* o = reinterpret_cast<uint16_t*>(ob + 2 + 4 * g);
                     o[0] = uint16_t(cd);
@@ -304,6 +309,35 @@ __device__ __forceinline__ void stage_units_x(const float* __restrict__ x, int K
                    : make_float4(__ldg(p), __ldg(p + 1), __ldg(p + 2), __ldg(p + 3));
     };
     stage_units_f32<NC>(load, K, s, xq_out, sumq_out, tid, nthr);
+}
+
+// From fp32 x [NC][ld] in global memory, elements [k0, k0 + Kr) of every
+// column (one part of a K split; k0 and Kr multiples of 256); xq_out (nullable)
+// gets the q8_0 blocks of that range at their place in [NC][ld/32] blocks.
+template <int NC>
+__device__ __forceinline__ void stage_units_x_range(const float* __restrict__ x, int ld, int k0, int Kr, UnitAct s,
+                                                    uint8_t* __restrict__ xq_out, int tid, int nthr)
+{
+    const int lane = tid & 31;
+    const bool vec = (reinterpret_cast<uintptr_t>(x) & 15) == 0 && (ld & 3) == 0;
+    auto load = [&](int c, int u) {
+        const float* p = x + size_t(c) * ld + k0 + size_t(u) * kUnitElems + 4 * lane;
+        return vec ? __ldg(reinterpret_cast<const float4*>(p))
+                   : make_float4(__ldg(p), __ldg(p + 1), __ldg(p + 2), __ldg(p + 3));
+    };
+    stage_units_f32<NC>(load, Kr, s, xq_out ? xq_out + size_t(k0 / kQK8) * kQ8Bytes : nullptr, nullptr, tid, nthr,
+                        ld / kQK8);
+}
+
+// q8_0 blocks [j0, j0 + nqr) of each column of nq_all blocks (one part of a K split)
+template <int NC>
+__device__ __forceinline__ void stage_q8_range(const uint8_t* __restrict__ xq, int nq_all, int j0, int nqr, UnitAct s,
+                                               int tid, int nthr)
+{
+    if (reinterpret_cast<uintptr_t>(xq) & 3)
+        stage_units_q8_by_block<NC>(xq, nq_all, j0, nqr, s, nullptr, tid, nthr);
+    else
+        stage_blocks_q8<NC>(xq, nq_all, j0, nqr, s, nullptr, tid, nthr);
 }
 
 // From fp32 values written earlier in the same launch as tagged records

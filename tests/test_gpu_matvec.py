@@ -170,3 +170,28 @@ def test_7b_down_matrix_full(cuda_ready, variant):
     y, _ = mq.matvec_q4K_q8_0(_to_dev(W), 3584, 18944, x=_to_dev(x))
     torch.cuda.synchronize()
     _check_y(y.cpu().numpy(), W, oracle.quantize_q8_0(x), 3584, 18944)
+
+
+@pytest.mark.parametrize("ncols", [8, 6])
+def test_matvec_k_split_matches_oracle_and_exports_xq(cuda_ready, ncols):
+    """Eight (or six) staged columns of K = 18944 leave no room for a ring in one
+    launch, so the matvec runs as a K split: one launch per half of every row,
+    the second adding its sums to y.  The result stays within tolerance of the
+    oracle, the fp32 and q8_0 inputs give the same bits, and the q8_0 export of
+    the activation is the whole activation, bit for bit."""
+    import torch
+    mq = cuda_ready
+    rows, K = 67, 18944
+    W = synth.q4K_matrix(rows, K, seed=91, tag=synth.TAG_W)
+    x = synth.activation(K, ncols, seed=92, tag=synth.TAG_X)
+    xq_np = oracle.quantize_q8_0(x)
+    Wd = _to_dev(W)
+    xq_out = torch.zeros((ncols, K // 32 * 34), dtype=torch.uint8, device="cuda")
+    y1, _ = mq.matvec_q4K_q8_0(Wd, rows, K, x=_to_dev(x), xq_out=xq_out)
+    y2, _ = mq.matvec_q4K_q8_0(Wd, rows, K, xq=_to_dev(xq_np))
+    torch.cuda.synchronize()
+    assert mq.mq_read_device_status(0) == 0
+    y1 = y1.cpu().numpy()
+    _check_y(y1, W, xq_np, rows, K)
+    assert np.array_equal(y1.view(np.uint32), y2.cpu().numpy().view(np.uint32))
+    assert np.array_equal(xq_out.cpu().numpy(), xq_np.reshape(ncols, -1))
