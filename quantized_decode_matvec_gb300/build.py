@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libmq.so")
 
-SOURCES = ["api.cu", "matvec.cu", "ffn.cu", "quantize.cu", "ring.cu", "step.cu", "noalloc.cu", "wtypes.cu", "ring_cols.cu",
+SOURCES = ["api.cu", "matvec.cu", "ffn.cu", "quantize.cu", "ring.cu", "step.cu", "noalloc.cu", "wtypes.cu", "ring_cols.cu", "ring_split.cu",
            "gemm.cu", "dequant.cu", "step_chained.cu", "mmq.cu"]
 HEADERS = ["mq_device.cuh", "mq_stream.cuh", "mq_internal.h", "mq_job.cuh", "mq_epilogue.cuh", "mq_tma.cuh", "mq_unit.cuh", "mq_ring.cuh", "mq_ring_kernel.cuh", "mq_umma.cuh", "mq_step_kernel.cuh"]
 

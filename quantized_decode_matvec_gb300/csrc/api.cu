@@ -16,6 +16,7 @@ cudaError_t set_ring_attributes(int max_smem);
 cudaError_t set_step_attributes(int max_smem);
 cudaError_t set_wring_attributes(int max_smem);
 cudaError_t set_ring_cols_attributes(int max_smem);
+cudaError_t set_ring_split_attributes(int max_smem);
 cudaError_t set_gemm_attributes(int max_smem);
 cudaError_t set_mmq_attributes(int max_smem);
 void plan_ring(MvPlan& q, int64_t units, int kind, int nc, const DeviceInfo& dev, int64_t unit_bytes,
@@ -409,6 +410,7 @@ cudaError_t set_kernel_attributes(int max_smem)
     if (e == cudaSuccess) e = set_step_attributes(max_smem);
     if (e == cudaSuccess) e = set_wring_attributes(max_smem);
     if (e == cudaSuccess) e = set_ring_cols_attributes(max_smem);
+    if (e == cudaSuccess) e = set_ring_split_attributes(max_smem);
     if (e == cudaSuccess) e = set_gemm_attributes(max_smem);
     if (e == cudaSuccess) e = set_mmq_attributes(max_smem);
     return e;

@@ -17,12 +17,20 @@ __device__ __forceinline__ void mv_epilogue(const float* __restrict__ part, int 
                                             uint64_t* __restrict__ rec = nullptr, int R = 0, uint32_t tag = 0,
                                             bool acc = false)
 {
+    if (acc) {  // a loop of its own: the plain store below must not wait on a load of y
+        for (int t = tid; t < NC * nrows; t += nthr) {
+            const int c = t / nrows, lr = t - c * nrows;
+            float s = 0.0f;
+            for (int g = 0; g < nseg; ++g) s += part[(lr * nseg + g) * NC + c];
+            y[size_t(c) * y_ld + r0 + lr] += s;
+        }
+        return;
+    }
     for (int t = tid; t < NC * nrows; t += nthr) {
         const int c = t / nrows, lr = t - c * nrows;
         float s = 0.0f;
         for (int g = 0; g < nseg; ++g) s += part[(lr * nseg + g) * NC + c];
-        float* yp = y + size_t(c) * y_ld + r0 + lr;
-        *yp = acc ? *yp + s : s;
+        y[size_t(c) * y_ld + r0 + lr] = s;
         if (rec) st_tagged(rec + size_t(c) * R + r0 + lr, __float_as_uint(s), tag);
     }
 }

@@ -41,7 +41,9 @@ constexpr int kEarlyTiles = 2;
 // each CTA prefetches its share of the activation's lines into L2 before the wait
 constexpr bool kPrefetchAct = true;
 
-template <int NC, int KIND, class Fmt = FmtQ4K, int kMode = 0>
+// kSplit: the instance for one part of a K split (p.kp0, p.kpn; a separate
+// instance, so the whole-row kernels carry none of its code)
+template <int NC, int KIND, class Fmt = FmtQ4K, int kMode = 0, bool kSplit = false>
 __global__ void __launch_bounds__(32 * ring_max_warps<NC, kMode>(), 1)
     ring_kernel(const void* __restrict__ desc, int a_h, int b_h, MvPlan p, unsigned* status)
 {
@@ -104,10 +106,9 @@ __global__ void __launch_bounds__(32 * ring_max_warps<NC, kMode>(), 1)
     const size_t row_bytes = Fmt::row_bytes(K / kUnitElems);
     // K split: this launch streams super-blocks [sb0, sb0 + nsb) of every row,
     // one bulk copy per row into tile rows of tile_row bytes
-    const int sb0 = p.kpn ? p.kp0 : 0;
-    const bool split = p.kpn != 0;
-    const size_t tile_row = split ? Fmt::row_bytes(2 * p.kpn) : row_bytes;
-    const size_t src_off = Fmt::row_bytes(2 * sb0);
+    const int sb0 = kSplit ? p.kp0 : 0;
+    const size_t tile_row = kSplit ? Fmt::row_bytes(2 * p.kpn) : row_bytes;
+    const size_t src_off = kSplit ? Fmt::row_bytes(2 * sb0) : 0;
     const int ntiles = (nrows + p.T - 1) / p.T;
 
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -144,7 +145,7 @@ __global__ void __launch_bounds__(32 * ring_max_warps<NC, kMode>(), 1)
             uint8_t* dst = ring + size_t(s) * p.stage_bytes;
             int a = lr0;
             const int e = lr0 + tn;
-            if (split) {  // part of each row: one copy per row
+            if constexpr (kSplit) {  // part of each row: one copy per row
                 for (; a < e; ++a)
                     bulk_copy_g2s_evict_first(dst + size_t(a - lr0) * tile_row, W + size_t(rowmap(a)) * row_bytes + src_off,
                                               uint32_t(tile_row), &full[s], wpolicy);
@@ -186,16 +187,18 @@ __global__ void __launch_bounds__(32 * ring_max_warps<NC, kMode>(), 1)
         // ---- consumers: activation first (it may come from the predecessor), then the ring
         griddep_wait();
         const int ctid = threadIdx.x, cthr = p.nwc * 32;
-        uint8_t* const xo = (KIND == KIND_MV && blockIdx.x == 0) ? xq_out : nullptr;
-        if (split) {
+        if constexpr (kSplit) {
+            uint8_t* const xo = (KIND == KIND_MV && blockIdx.x == 0) ? xq_out : nullptr;
             if (x)
                 stage_units_x_range<NC>(x, K, sb0 * kQK, p.kpn * kQK, act, xo, ctid, cthr);
             else
                 stage_q8_range<NC>(xq, K / kQK8, sb0 * (kQK / kQK8), p.kpn * (kQK / kQK8), act, ctid, cthr);
-        } else if (x) {
-            stage_units_x<NC>(x, K, act, xo, nullptr, ctid, cthr);
         } else {
-            stage_units_q8<NC>(xq, K, act, nullptr, ctid, cthr);
+            if (x)
+                stage_units_x<NC>(x, K, act, (KIND == KIND_MV && blockIdx.x == 0) ? xq_out : nullptr, nullptr, ctid,
+                                  cthr);
+            else
+                stage_units_q8<NC>(xq, K, act, nullptr, ctid, cthr);
         }
         named_barrier_sync(1, cthr);
         named_barrier_arrive(2, cthr + 32);  // release the producer's remaining ring tiles
@@ -214,7 +217,10 @@ __global__ void __launch_bounds__(32 * ring_max_warps<NC, kMode>(), 1)
         float* vals = reinterpret_cast<float*>(smem + p.off_vals);
         gu_epilogue<NC>(part, vals, p.nseg, n, i0, R, static_cast<uint8_t*>(fd->h_q8), fd->gu_dbg, fd->h_dbg);
     } else {
-        mv_epilogue<NC>(part, p.nseg, nrows, r0, y, y_ld, threadIdx.x, blockDim.x, nullptr, 0, 0, p.kacc != 0);
+        if constexpr (kSplit)
+            mv_epilogue<NC>(part, p.nseg, nrows, r0, y, y_ld, threadIdx.x, blockDim.x, nullptr, 0, 0, p.kacc != 0);
+        else
+            mv_epilogue<NC>(part, p.nseg, nrows, r0, y, y_ld, threadIdx.x, blockDim.x);
     }
 }
 

@@ -314,8 +314,10 @@ __device__ __forceinline__ void stage_units_x(const float* __restrict__ x, int K
 // From fp32 x [NC][ld] in global memory, elements [k0, k0 + Kr) of every
 // column (one part of a K split; k0 and Kr multiples of 256); xq_out (nullable)
 // gets the q8_0 blocks of that range at their place in [NC][ld/32] blocks.
+// (Not inlined, like stage_q8_range: code that only a K split runs stays out
+// of the kernels' bodies.)
 template <int NC>
-__device__ __forceinline__ void stage_units_x_range(const float* __restrict__ x, int ld, int k0, int Kr, UnitAct s,
+__device__ __noinline__ void stage_units_x_range(const float* __restrict__ x, int ld, int k0, int Kr, UnitAct s,
                                                     uint8_t* __restrict__ xq_out, int tid, int nthr)
 {
     const int lane = tid & 31;
@@ -331,7 +333,7 @@ __device__ __forceinline__ void stage_units_x_range(const float* __restrict__ x,
 
 // q8_0 blocks [j0, j0 + nqr) of each column of nq_all blocks (one part of a K split)
 template <int NC>
-__device__ __forceinline__ void stage_q8_range(const uint8_t* __restrict__ xq, int nq_all, int j0, int nqr, UnitAct s,
+__device__ __noinline__ void stage_q8_range(const uint8_t* __restrict__ xq, int nq_all, int j0, int nqr, UnitAct s,
                                                int tid, int nthr)
 {
     if (reinterpret_cast<uintptr_t>(xq) & 3)

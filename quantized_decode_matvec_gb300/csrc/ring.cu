@@ -34,9 +34,14 @@ static cudaError_t launch_ring_kind(const void* desc, int a, int b, int ncols, c
     return cudaErrorInvalidValue;
 }
 
+// one part of a K split (matvec and down), in ring_split.cu
+cudaError_t launch_ring_split(const void* desc, int kind, int a, int b, int ncols, const MvPlan& p, unsigned* status,
+                              cudaStream_t s, bool pdl);
+
 cudaError_t launch_ring(const void* desc, int kind, int a, int b, int ncols, const MvPlan& p, unsigned* status,
                         cudaStream_t s, bool pdl)
 {
+    if (p.kpn) return launch_ring_split(desc, kind, a, b, ncols, p, status, s, pdl);
     // 3..8 columns beyond 8 consumer warps: the 16-warp instances
     if (ncols >= 3 && (p.cmap || p.cgw || p.block > 32 * ring_max_warps<3>()))
         return launch_ring_cols(desc, kind, a, b, ncols, p, status, s, pdl);
