@@ -322,6 +322,61 @@ __device__ __noinline__ void stage_units_x_range(const float* __restrict__ x, in
 {
     const int lane = tid & 31;
     const bool vec = (reinterpret_cast<uintptr_t>(x) & 15) == 0 && (ld & 3) == 0;
+    if (vec) {
+        // many columns of a long row: one thread per q8_0 block (its 32 values
+        // loaded at once) takes fewer rounds than one warp per unit
+        const int nqr = Kr / kQK8, total = NC * nqr, nq_all = ld / kQK8, j0 = k0 / kQK8;
+        for (int t = tid; t < total; t += nthr) {
+            const int c = t / nqr, J = t - c * nqr;
+            const float4* p = reinterpret_cast<const float4*>(x + size_t(c) * ld + k0) + size_t(J) * 8;
+            float4 v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = __ldg(p + i);
+            float m = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                m = fmaxf(m, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
+            const Q8Scale sc = q8_scale_of(m);
+            int q[32];
+            bool ok = true;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                ok &= q8_code_fast(v[i].x, sc, &q[4 * i]);
+                ok &= q8_code_fast(v[i].y, sc, &q[4 * i + 1]);
+                ok &= q8_code_fast(v[i].z, sc, &q[4 * i + 2]);
+                ok &= q8_code_fast(v[i].w, sc, &q[4 * i + 3]);
+            }
+            if (!ok) {  // rare: the IEEE division decides
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    q[4 * i] = q8_code_exact(v[i].x, sc.d);
+                    q[4 * i + 1] = q8_code_exact(v[i].y, sc.d);
+                    q[4 * i + 2] = q8_code_exact(v[i].z, sc.d);
+                    q[4 * i + 3] = q8_code_exact(v[i].w, sc.d);
+                }
+            }
+            uint32_t cw[8];
+            int sq = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                cw[i] = (uint32_t(q[4 * i]) & 0xffu) | ((uint32_t(q[4 * i + 1]) & 0xffu) << 8) |
+                        ((uint32_t(q[4 * i + 2]) & 0xffu) << 16) | (uint32_t(q[4 * i + 3]) << 24);
+                sq += q[4 * i] + q[4 * i + 1] + q[4 * i + 2] + q[4 * i + 3];
+            }
+            const __half hd = __float2half_rn(sc.d);
+            put_block(s, c, J, cw, __half2float(hd), sq);
+            if (xq_out) {
+                uint16_t* o = reinterpret_cast<uint16_t*>(xq_out + (size_t(c) * nq_all + j0 + J) * kQ8Bytes);
+                o[0] = __half_as_ushort(hd);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    o[1 + 2 * i] = uint16_t(cw[i]);
+                    o[2 + 2 * i] = uint16_t(cw[i] >> 16);
+                }
+            }
+        }
+        return;
+    }
     auto load = [&](int c, int u) {
         const float* p = x + size_t(c) * ld + k0 + size_t(u) * kUnitElems + 4 * lane;
         return vec ? __ldg(reinterpret_cast<const float4*>(p))
