@@ -224,7 +224,9 @@ __device__ __forceinline__ void stage_units_q8(const uint8_t* __restrict__ xq, i
 // writes the q8_0 blocks to xq_out (2-byte aligned) and the code sums to
 // sumq_out.  `load(c, u)` gives this lane's values 4l..4l+3 of unit u of
 // column c (lane l = tid & 31).
-template <int NC, typename Loader>
+// kPair: the loader fetches a step's two units together, load.pair(c, u, u2,
+// va, vb) (a polling loader then waits for both in one loop)
+template <int NC, typename Loader, bool kPair = false>
 __device__ __forceinline__ void stage_units_f32(Loader load, int K, UnitAct s, uint8_t* __restrict__ xq_out,
                                                 int32_t* sumq_out, int tid, int nthr, int xq_ld = 0)
 {
@@ -260,7 +262,13 @@ __device__ __forceinline__ void stage_units_f32(Loader load, int K, UnitAct s, u
         // two units per step, both loads first (a warp's last step may repeat its unit)
         for (int u = warp; u < U; u += 2 * nw) {
             const int u2 = u + nw < U ? u + nw : u;
-            const float4 va = load(c, u), vb = load(c, u2);
+            float4 va, vb;
+            if constexpr (kPair) {
+                load.pair(c, u, u2, va, vb);
+            } else {
+                va = load(c, u);
+                vb = load(c, u2);
+            }
             const float ma = amax8(va), mb = amax8(vb);
             const Q8Scale sa = q8_scale_of(ma), sb = q8_scale_of(mb);
             uint32_t ca, cb2;
@@ -409,30 +417,48 @@ __device__ __forceinline__ bool stage_units_yrec(const uint64_t* __restrict__ re
                                                  uint8_t* __restrict__ xq_out, uint32_t tag,
                                                  const unsigned* abort_word, uint64_t limit_ns, int tid, int nthr)
 {
-    const int lane = tid & 31;
-    bool bad = false;
-    auto load = [&](int c, int u) {
-        const uint64_t* p = rec + size_t(c) * ld + size_t(u) * kUnitElems + 4 * lane;
-        uint64_t a0, a1, b0, b1;
-        ld_tagged2(p, a0, a1);
-        ld_tagged2(p + 2, b0, b1);
-        uint64_t t0 = 0;
-        for (uint32_t it = 0; !bad; ++it) {
-            const bool ok = uint32_t(a0 >> 32) == tag && uint32_t(a1 >> 32) == tag && uint32_t(b0 >> 32) == tag &&
-                            uint32_t(b1 >> 32) == tag;
-            if (ok) break;
-            if (it == 0)
-                t0 = global_timer_ns();
-            else if ((it & 15u) == 0 && (ld_relaxed_u32(abort_word) != 0 || global_timer_ns() - t0 > limit_ns))
-                bad = true;
-            ld_tagged2(p, a0, a1);
-            ld_tagged2(p + 2, b0, b1);
+    // a step's two units are read and polled together: one round trip per
+    // poll for both, not one after the other
+    struct PairLoader {
+        const uint64_t* rec;
+        int ld, lane;
+        uint32_t tag;
+        const unsigned* abort_word;
+        uint64_t limit_ns;
+        bool bad;
+        __device__ __forceinline__ void pair(int c, int u, int u2, float4& va, float4& vb)
+        {
+            const uint64_t* p = rec + size_t(c) * ld + size_t(u) * kUnitElems + 4 * lane;
+            const uint64_t* q = rec + size_t(c) * ld + size_t(u2) * kUnitElems + 4 * lane;
+            uint64_t r[8];
+            ld_tagged2(p, r[0], r[1]);
+            ld_tagged2(p + 2, r[2], r[3]);
+            ld_tagged2(q, r[4], r[5]);
+            ld_tagged2(q + 2, r[6], r[7]);
+            uint64_t t0 = 0;
+            for (uint32_t it = 0; !bad; ++it) {
+                bool ok = true;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) ok &= uint32_t(r[i] >> 32) == tag;
+                if (ok) break;
+                if (it == 0)
+                    t0 = global_timer_ns();
+                else if ((it & 15u) == 0 && (ld_relaxed_u32(abort_word) != 0 || global_timer_ns() - t0 > limit_ns))
+                    bad = true;
+                if (uint32_t(r[0] >> 32) != tag || uint32_t(r[1] >> 32) != tag) ld_tagged2(p, r[0], r[1]);
+                if (uint32_t(r[2] >> 32) != tag || uint32_t(r[3] >> 32) != tag) ld_tagged2(p + 2, r[2], r[3]);
+                if (uint32_t(r[4] >> 32) != tag || uint32_t(r[5] >> 32) != tag) ld_tagged2(q, r[4], r[5]);
+                if (uint32_t(r[6] >> 32) != tag || uint32_t(r[7] >> 32) != tag) ld_tagged2(q + 2, r[6], r[7]);
+            }
+            va = make_float4(__uint_as_float(uint32_t(r[0])), __uint_as_float(uint32_t(r[1])),
+                             __uint_as_float(uint32_t(r[2])), __uint_as_float(uint32_t(r[3])));
+            vb = make_float4(__uint_as_float(uint32_t(r[4])), __uint_as_float(uint32_t(r[5])),
+                             __uint_as_float(uint32_t(r[6])), __uint_as_float(uint32_t(r[7])));
         }
-        return make_float4(__uint_as_float(uint32_t(a0)), __uint_as_float(uint32_t(a1)), __uint_as_float(uint32_t(b0)),
-                           __uint_as_float(uint32_t(b1)));
     };
-    stage_units_f32<NC>(load, K, s, xq_out, nullptr, tid, nthr);
-    return !__any_sync(0xffffffffu, bad);
+    PairLoader load{rec, ld, tid & 31, tag, abort_word, limit_ns, false};
+    stage_units_f32<NC, PairLoader&, true>(load, K, s, xq_out, nullptr, tid, nthr);
+    return !__any_sync(0xffffffffu, load.bad);
 }
 
 // 16 bytes from shared memory (the ring's stages are written by the bulk-copy
