@@ -53,7 +53,13 @@ class StepGraph:
             self._capture(capture_hook)
 
     def _capture(self, hook):
-        g = torch.cuda.CUDAGraph()
+        # keep the captured cudaGraph_t (where this torch can) so that its nodes can be counted
+        try:
+            g = torch.cuda.CUDAGraph(keep_graph=True)
+            self._kept = True
+        except TypeError:
+            g = torch.cuda.CUDAGraph()
+            self._kept = False
         try:
             with torch.cuda.graph(g, stream=self.stream):
                 if hook is not None:
@@ -69,6 +75,12 @@ class StepGraph:
             except Exception:
                 pass
             return
+        if self._kept:
+            try:
+                self._nodes = _count_kernel_nodes(g.raw_cuda_graph())
+                g.instantiate()  # else the first replay instantiates it
+            except Exception as e:
+                log.info("graph node count unavailable: %s", e)
         self.graph = g
         self.captured = True
 
@@ -95,15 +107,30 @@ class StepGraph:
         """Kernel nodes in the captured graph (None if not captured or not queryable)."""
         if not self.captured:
             return None
-        try:
-            from cuda.bindings import runtime as rt  # optional: raw graph introspection
-            raw = self.graph.raw_cuda_graph() if hasattr(self.graph, "raw_cuda_graph") else None
-            if raw is None:
-                return None
-            err, _, n = rt.cudaGraphGetNodes(raw, 0)
-            return int(n)
-        except Exception:
+        return getattr(self, "_nodes", None)
+
+
+def _count_kernel_nodes(raw: int) -> Optional[int]:
+    """Kernel nodes of a cudaGraph_t (the driver's CUgraph), through the driver API;
+    None if the driver library or the call is not available."""
+    try:
+        import ctypes
+        cu = ctypes.CDLL("libcuda.so.1")
+        n = ctypes.c_size_t(0)
+        if cu.cuGraphGetNodes(ctypes.c_void_p(raw), None, ctypes.byref(n)) != 0:
             return None
+        nodes = (ctypes.c_void_p * max(n.value, 1))()
+        if cu.cuGraphGetNodes(ctypes.c_void_p(raw), nodes, ctypes.byref(n)) != 0:
+            return None
+        kinds = ctypes.c_int(0)
+        count = 0
+        for i in range(n.value):
+            if cu.cuGraphNodeGetType(ctypes.c_void_p(nodes[i]), ctypes.byref(kinds)) != 0:
+                return None
+            count += kinds.value == 0  # CU_GRAPH_NODE_TYPE_KERNEL
+        return count
+    except Exception:
+        return None
 
 
 class PinnedFeeder:
