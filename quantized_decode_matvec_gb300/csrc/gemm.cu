@@ -8,7 +8,8 @@
 //
 // with fp32 accumulation in tensor memory.  One CTA per SM walks output tiles
 // of 128 weight rows x BN tokens, BN = 256 (128 for at most 128 tokens),
-// persistent, static round robin; tiles that
+// persistent, static round robin, a last wave that would leave half the CTAs
+// idle split into BN/2-token tiles; tiles that
 // share a weight block run at the same time, so each block comes from HBM
 // about once and from L2 for the other token tiles.  Per CTA:
 //
@@ -52,13 +53,35 @@ struct GemmTile {
 struct GemmArgs {
     int R, K, T;
     int m_tiles, n_tiles, k_steps;
+    // the last wave of BN-token tiles split in two BN/2-token tiles when that
+    // fills at most a wave of CTAs: tiles [0, full_tiles) are BN wide, the
+    // ntiles - full_tiles after them BN/2 wide (full_tiles = ntiles: no split)
+    int full_tiles, ntiles;
     uint64_t limit_ns;
 };
+
+// output tile t: weight-row block m, first token tok0, width bn
+struct GemmTileAt {
+    int m, tok0, bn;
+};
+
+template <int BN>
+__device__ __forceinline__ GemmTileAt gemm_tile_at(int t, const GemmArgs& a)
+{
+    if (t < a.full_tiles) {
+        const int m = t / a.n_tiles;
+        return GemmTileAt{m, (t - m * a.n_tiles) * BN, BN};
+    }
+    const int u = t - a.full_tiles, t2 = a.full_tiles + (u >> 1);  // the BN tile it halves
+    const int m = t2 / a.n_tiles;
+    return GemmTileAt{m, (t2 - m * a.n_tiles) * BN + (u & 1) * (BN / 2), BN / 2};
+}
 
 template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_f16_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                    float* __restrict__ Y, const GemmArgs a, unsigned* status)
+                    const __grid_constant__ CUtensorMap tmXh, float* __restrict__ Y, const GemmArgs a,
+                    unsigned* status)
 {
     using G = GemmTile<BN>;
     constexpr int kGemmBN = BN, kGemmStages = G::kStages, kGemmStage = G::kStage;
@@ -72,7 +95,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // the swizzled tiles want 1024-byte alignment
     const uint32_t raw = smem_u32(gsm_raw);
     uint8_t* const gsm = gsm_raw + ((1024u - (raw & 1023u)) & 1023u);
-    const int ntiles = a.m_tiles * a.n_tiles;
+    const int ntiles = a.ntiles;
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
@@ -89,6 +112,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmW);
         tma_prefetch_desc(&tmX);
+        if (a.full_tiles < a.ntiles) tma_prefetch_desc(&tmXh);
     }
     if (warp == 1) tmem_alloc(&tmem_base, kGemmTmemCols);
     tc_fence_before();
@@ -101,7 +125,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (lane == 0) {
             int it = 0;
             for (int t = blockIdx.x; t < ntiles && !abort_flag; t += gridDim.x) {
-                const int m = t / a.n_tiles, n = t - m * a.n_tiles;
+                const GemmTileAt ti = gemm_tile_at<BN>(t, a);
+                const bool half = ti.bn != BN;
                 for (int kk = 0; kk < a.k_steps; ++kk, ++it) {
                     const int s = it % kGemmStages;
                     if (it >= kGemmStages &&
@@ -110,9 +135,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         break;
                     }
                     uint8_t* sa = gsm + s * kGemmStage;
-                    mbar_arrive_expect_tx(&full[s], kGemmStage);
-                    tma_load_2d(sa, &tmW, kk * kGemmBK, m * kGemmBM, &full[s]);
-                    tma_load_2d(sa + kGemmATile, &tmX, kk * kGemmBK, n * kGemmBN, &full[s]);
+                    mbar_arrive_expect_tx(&full[s], uint32_t(kGemmATile + ti.bn * kGemmBK * 2));
+                    tma_load_2d(sa, &tmW, kk * kGemmBK, ti.m * kGemmBM, &full[s]);
+                    tma_load_2d(sa + kGemmATile, half ? &tmXh : &tmX, kk * kGemmBK, ti.tok0, &full[s]);
                 }
             }
             // copies still in flight land before the CTA can exit
@@ -122,9 +147,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else if (warp == 1) {
         // ---- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = umma_idesc_f16_f32(kGemmBM, kGemmBN);
+            constexpr uint32_t idesc_full = umma_idesc_f16_f32(kGemmBM, kGemmBN);
+            constexpr uint32_t idesc_half = umma_idesc_f16_f32(kGemmBM, kGemmBN / 2);
             int it = 0, tl = 0;
             for (int t = blockIdx.x; t < ntiles && !abort_flag; t += gridDim.x, ++tl) {
+                const uint32_t idesc = t < a.full_tiles ? idesc_full : idesc_half;
                 const int b = tl & 1;
                 if (tl >= 2 && !mbar_wait_bounded(&acce[b], uint32_t(tl / 2 - 1) & 1u, a.limit_ns)) {
                     abort_flag = 1;
@@ -174,11 +201,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 break;
             }
             tc_fence_after();
-            const int m = t / a.n_tiles, n = t - m * a.n_tiles;
-            const int r = m * kGemmBM + q * 32 + lane;
-            const int t0 = n * kGemmBN;
+            const GemmTileAt ti = gemm_tile_at<BN>(t, a);
+            const int r = ti.m * kGemmBM + q * 32 + lane;
+            const int t0 = ti.tok0;
 #pragma unroll 1
-            for (int c0 = 0; c0 < kGemmBN; c0 += 32) {
+            for (int c0 = 0; c0 < ti.bn; c0 += 32) {
                 uint32_t v[32];
                 tmem_ld32(tmem + lane_base + uint32_t(b * kGemmBN + c0), v);
                 tmem_ld_wait();
@@ -256,8 +283,9 @@ cudaError_t launch_gemm_f16(const void* W16, const void* X16, float* Y, int R, i
     // the 3584-row matrices at 2048 tokens, measured slower there on GB300: o
     // 63 against 48 us, down 275 against 219 us); 128 only for at most 128 tokens
     const int BN = T <= 128 ? 128 : 256;
-    CUtensorMap tmW, tmX;
-    if (!make_map(&tmW, W16, R, K, kGemmBM) || !make_map(&tmX, X16, T, K, BN)) return cudaErrorInvalidValue;
+    CUtensorMap tmW, tmX, tmXh;
+    if (!make_map(&tmW, W16, R, K, kGemmBM) || !make_map(&tmX, X16, T, K, BN) || !make_map(&tmXh, X16, T, K, BN / 2))
+        return cudaErrorInvalidValue;
     GemmArgs a;
     a.R = R;
     a.K = K;
@@ -266,12 +294,21 @@ cudaError_t launch_gemm_f16(const void* W16, const void* X16, float* Y, int R, i
     a.n_tiles = (T + BN - 1) / BN;
     a.k_steps = K / kGemmBK;
     a.limit_ns = uint64_t(fault_policy() == FAULT_NONE ? 2000 : 50) * 1000000ull;
-    const int ntiles = a.m_tiles * a.n_tiles;
-    const int grid = ntiles < num_sms ? ntiles : num_sms;
+    const int tiles = a.m_tiles * a.n_tiles;
+    const int grid = tiles < num_sms ? tiles : num_sms;
+    // a last wave that fills at most half the CTAs runs as twice as many
+    // half-width tiles: 224 tiles on 152 CTAs take 1.5 tile times, not 2
+    const int rem = tiles % grid;
+    a.full_tiles = tiles;
+    a.ntiles = tiles;
+    if (BN == 256 && tiles > grid && rem > 0 && 2 * rem <= grid) {
+        a.full_tiles = tiles - rem;
+        a.ntiles = a.full_tiles + 2 * rem;
+    }
     if (BN == 256)
-        gemm_f16_kernel<256><<<grid, kGemmThreads, GemmTile<256>::kSmem, s>>>(tmW, tmX, Y, a, status);
+        gemm_f16_kernel<256><<<grid, kGemmThreads, GemmTile<256>::kSmem, s>>>(tmW, tmX, tmXh, Y, a, status);
     else
-        gemm_f16_kernel<128><<<grid, kGemmThreads, GemmTile<128>::kSmem, s>>>(tmW, tmX, Y, a, status);
+        gemm_f16_kernel<128><<<grid, kGemmThreads, GemmTile<128>::kSmem, s>>>(tmW, tmX, tmXh, Y, a, status);
     return cudaGetLastError();
 }
 

@@ -103,6 +103,22 @@ def test_gemm_f16_many_tiles_per_cta(cuda_ready):
     _check(Y.cpu().numpy(), W16, X16, K, rows, toks)
 
 
+@pytest.mark.parametrize("R,T", [(3584, 2048), (3544, 2000)])
+def test_gemm_f16_last_wave_split(cuda_ready, R, T):
+    # 224 tiles of 128 x 256 on 152 CTAs: the last 72 run as 144 tiles of 128 x 128
+    # (ragged rows and tokens in the second case); every output is checked, and the
+    # output starts as NaN so a tile left out shows
+    import torch
+    mq = cuda_ready
+    K = 256
+    W16, X16 = _gemm_case(R, K, T, seed=R + T)
+    Y = torch.full((T, R), float("nan"), dtype=torch.float32, device="cuda")
+    mq.gemm_f16(_dev(W16.view(np.float16)), _dev(X16.view(np.float16)), out=Y)
+    torch.cuda.synchronize()
+    assert mq.mq_read_device_status(0) == 0
+    _check(Y.cpu().numpy(), W16, X16, K)
+
+
 @pytest.mark.slow
 def test_prefill_7b_ffn_gu_sampled(cuda_ready):
     # the 7B ffn_gu projection at 2K tokens, the pages' prefill size: the cache built on
