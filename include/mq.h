@@ -225,8 +225,9 @@ typedef struct mq_layer_desc {
 #define MQ_STEP_PERSISTENT 2u  /* one persistent kernel for the whole stack (needs `workspace`) */
 #define MQ_STEP_CHAINED 4u     /* every phase reads the previous phase's output (a real decode chain) */
 
-/* bytes of the persistent step's fixed workspace words (abort word, per-CTA
- * phase flags); the whole workspace a shape needs is mq_step_workspace_bytes */
+/* bytes of the persistent step's fixed workspace words (abort word, phase
+ * counter, a reserved word per CTA); the whole workspace a shape needs is
+ * mq_step_workspace_bytes */
 #define MQ_STEP_WORKSPACE_BYTES 4352
 
 typedef struct mq_step_shape {
@@ -257,10 +258,10 @@ typedef struct mq_step_shape {
  *
  * Inputs of the persistent step:
  *  - default: every input (a_l, b_l, c_l or their q8_0 forms) is a buffer that
- *    no phase of the launch writes.  Each CTA publishes a phase flag once it
- *    has written a phase's outputs and the next phase waits for every CTA's
- *    flag, which orders the phases; no input is produced in the launch, so no
- *    input needs to be made visible.  The kernel checks every input against
+ *    no phase of the launch writes.  Each CTA adds one to a phase counter once
+ *    it has written a phase's outputs and the next phase waits until the
+ *    counter shows every CTA, which orders the phases; no input is produced in
+ *    the launch, so no input needs to be made visible.  The kernel checks every input against
  *    every output of the launch first; an overlap records MQ_DEV_ALIAS and
  *    nothing is written.
  *  - MQ_STEP_CHAINED: a decode chain.  The input of every qkv, o and FFN phase

@@ -392,7 +392,7 @@ bool plan_step(const mq_step_shape& h, const DeviceInfo& dev, StepPlan* out)
     sp.pf_tiles = int(pf < 0 ? 0 : (pf > 16 ? 16 : pf));
     sp.nwc = nwc_max;
     sp.grid = int(G);
-    if (sp.grid > kWsMaxCtas) return false;  // one phase flag per CTA in the workspace
+    if (sp.grid > kWsMaxCtas) return false;  // the workspace reserves one word per CTA
     sp.smem = int(off_vals + vals);
     const StepWorkspace w = step_workspace(h);
     sp.ws_bytes = w.bytes;

@@ -363,6 +363,12 @@ __device__ __forceinline__ void st_relaxed_u32(unsigned* p, unsigned v)
     asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// relaxed atomic add at GPU scope, no value returned
+__device__ __forceinline__ void red_relaxed_add_u32(unsigned* p, unsigned v)
+{
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p)
 {
     unsigned v;

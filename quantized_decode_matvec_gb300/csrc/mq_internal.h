@@ -47,13 +47,15 @@ struct MvPlan {
 
 // Plan of the persistent step kernel: one ring plan per phase (qkv, o, gate/up,
 // down) sharing the ring geometry and shared-memory layout of the phases.
-// Persistent-step workspace (bytes): [0, 256) control words (word 1: abort),
-// [256, 4352) one phase flag (u32) per CTA, then the h records: per column
+// Persistent-step workspace (bytes): [0, 256) control words (word 1: abort,
+// word 2: the phase counter), [256, 4352) reserved (one u32 per CTA), then the
+// h records: per column
 // 40 * (I/128) records of 8 bytes (a 32-bit word of the activation's unit
 // layout and the phase that wrote it); for a chained step, then the output
 // records of the qkv, o and down phases: per phase ncols * rows records of 8
 // bytes (an fp32 output and the phase that wrote it), column-major, each
 // phase's area rounded up to 32 bytes.
+constexpr int kWsCountWord = 2;  // the phase counter: every CTA adds one per finished phase
 constexpr int kWsFlagsOff = 256;
 constexpr int kWsMaxCtas = 1024;
 constexpr int kWsRecOff = kWsFlagsOff + 4 * kWsMaxCtas;

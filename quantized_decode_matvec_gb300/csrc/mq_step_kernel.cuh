@@ -19,14 +19,14 @@
 //   of the activation's unit layout and the phase, in one 8-byte store), and
 //   the down phase copies them into shared memory once every tag is there.
 //   By default the other inputs stand for results of the previous phase:
-//   after a phase's outputs are written each CTA publishes a phase flag, and
-//   the next phase waits for every CTA's flag.  In a chained step (a real
+//   after a phase's outputs are written each CTA adds one to a phase
+//   counter, and the next phase waits until the counter shows every CTA.  In a chained step (a real
 //   decode chain: each phase reads the previous phase's output) every fp32
 //   output is also written as tagged records and the next phase stages its
 //   input from them.  No fence sits on either path: the records carry their
-//   own readiness, and the flags only order phases whose inputs no CTA of
+//   own readiness, and the counter only orders phases whose inputs no CTA of
 //   this launch writes (the kernel checks that first);
-// * every wait (ring mbarriers, phase flags, h records) is bounded in time;
+// * every wait (ring mbarriers, phase counter, records) is bounded in time;
 //   on a timeout a CTA records MQ_DEV_TIMEOUT, raises the step's abort word so
 //   the other CTAs stop too, drains its own copies in flight and returns.
 //
@@ -48,24 +48,25 @@ namespace mq {
 constexpr int kRecBatch = 8;
 
 // Dependency points on the step workspace (zeroed by the host before each
-// launch): word 1 is the abort word, then one phase flag per CTA, then the h
-// records.  Tags and flags are "phase number + 1", so zero means "not yet".
+// launch): word 1 is the abort word, word 2 the phase counter (CTAs x phases
+// finished), then the h records.  Tags are "phase number + 1", so zero means
+// "not yet".
 
-// Wait until every CTA's phase flag is at least `target`; the consumer threads
-// share the CTAs' flags out between them.  False on a timeout or when another
-// CTA aborted.
-__device__ __forceinline__ bool wait_flags(const unsigned* flags, int G, unsigned target, const unsigned* abort_word,
-                                           uint64_t limit_ns, int tid, int nthr)
+// Wait until the phase counter (workspace word 2; every CTA adds one per
+// finished phase) reaches `target`.  Warp 0 polls the one word (its lanes' loads
+// of one address are one request); the other warps go on, and the barrier
+// after the activation staging holds them.  A counter instead of one flag per
+// CTA: 152 CTAs polling 152 flags put ~23K loads per round on five L2 lines.
+// False on a timeout or when another CTA aborted.
+__device__ __forceinline__ bool wait_count(const unsigned* count, unsigned target, const unsigned* abort_word,
+                                           uint64_t limit_ns, int tid)
 {
+    if (tid >= 32) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 0;; ++it) {
-        bool ready = true;
-        for (int i = tid; i < G; i += nthr) ready &= ld_relaxed_u32(flags + i) >= target;
-        if (__all_sync(0xffffffffu, ready)) return true;
-        if ((it & 15u) == 15u) {
-            const bool stop = ld_relaxed_u32(abort_word) != 0 || global_timer_ns() - t0 > limit_ns;
-            if (__any_sync(0xffffffffu, stop)) return false;
-        }
+        if (ld_relaxed_u32(count) >= target) return true;
+        if ((it & 15u) == 15u && (ld_relaxed_u32(abort_word) != 0 || global_timer_ns() - t0 > limit_ns))
+            return false;
     }
 }
 
@@ -422,7 +423,7 @@ __global__ void __launch_bounds__(32 * ring_max_warps<NC, 1>(), 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nwc = sp.nwc;
     const uint64_t limit_ns = uint64_t(P0.wait_ms) * 1000000ull;
-    unsigned* const flags = ws + kWsFlagsOff / 4;
+    unsigned* const count = ws + kWsCountWord;
     uint64_t* const rec = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(ws) + kWsRecOff);
 
     {
@@ -513,7 +514,7 @@ __global__ void __launch_bounds__(32 * ring_max_warps<NC, 1>(), 1)
             constexpr int ph = decltype(phc)::value;
             const int k = 4 * l + ph;  // phase number within the launch
             if (sp.R[ph] == 0) {  // a phase left out: only its flag moves on
-                if (ctid == 0 && k + 1 < nphase) st_relaxed_u32(flags + b, unsigned(k + 1));
+                if (ctid == 0 && k + 1 < nphase) red_relaxed_add_u32(count, 1u);
                 return true;
             }
             const MvPlan& P = sp.ph[ph];
@@ -528,7 +529,7 @@ __global__ void __launch_bounds__(32 * ring_max_warps<NC, 1>(), 1)
             // records; the other phases, whose inputs are separate buffers standing
             // for the previous phase's results, wait for every CTA's flag of that
             // phase
-            if (k > 0 && ph != 3 && !from_rec && !wait_flags(flags, G, unsigned(k), ws + 1, limit_ns, ctid, cthr) &&
+            if (k > 0 && ph != 3 && !from_rec && !wait_count(count, unsigned(G) * unsigned(k), ws + 1, limit_ns, ctid) &&
                 lane == 0)
                 abort_flag = 1;
             const UnitAct act{reinterpret_cast<uint4*>(smem + P0.off_act),
@@ -573,7 +574,7 @@ __global__ void __launch_bounds__(32 * ring_max_warps<NC, 1>(), 1)
                     mv_epilogue<NC>(part, P.nseg, pr.nrows, pr.r0, j.y, j.y_ld, ctid, cthr);
             }
             named_barrier_sync(1, cthr);  // this CTA's outputs of phase k are written
-            if (ctid == 0 && k + 1 < nphase) st_relaxed_u32(flags + b, unsigned(k + 1));
+            if (ctid == 0 && k + 1 < nphase) red_relaxed_add_u32(count, 1u);
             return true;
         };
         for (int l = 0; l < sp.n_layers; ++l)
