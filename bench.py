@@ -683,6 +683,8 @@ def run_kernel_case(args):
     mq.init(device.index)
     f = synth.FFN_7B
     R, K = 2 * f.I, f.H  # the 7B ffn_gu projection
+    if args.kernel_case.startswith("gemm_o"):
+        R = K = f.H  # the 7B o projection: 224 tiles on 152 CTAs, the last wave split
     W = torch.from_numpy(synth.q4K_matrix(R, K, seed=f.seed, tag=synth.TAG_GU)).to(device)
     if args.kernel_case.startswith("gemm"):
         T = 2048
@@ -893,7 +895,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-config timings (context only)")
     ap.add_argument("--no-chained-arm", action="store_true", help="skip the chained-step arm (context only)")
-    ap.add_argument("--kernel-case", choices=["gemm_gu_T2048", "mmq_gu_ncols16", "mmq_gu_ncols64"], default=None,
+    ap.add_argument("--kernel-case", choices=["gemm_gu_T2048", "gemm_o_T2048", "mmq_gu_ncols16", "mmq_gu_ncols64"],
+                    default=None,
                     help="run one kernel on a fixed small case a few times (a target for ncu), not the benchmark")
     ap.add_argument("--layers", type=int, default=28,
                     help="layers of the 7B stack (28 = the bench workload; fewer only for small profiling runs)")
