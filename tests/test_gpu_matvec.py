@@ -195,3 +195,24 @@ def test_matvec_k_split_matches_oracle_and_exports_xq(cuda_ready, ncols):
     _check_y(y1, W, xq_np, rows, K)
     assert np.array_equal(y1.view(np.uint32), y2.cpu().numpy().view(np.uint32))
     assert np.array_equal(xq_out.cpu().numpy(), xq_np.reshape(ncols, -1))
+
+
+@pytest.mark.parametrize("K,ncols", [(131072, 1), (65536, 2)])
+def test_matvec_k_split_long_rows(cuda_ready, K, ncols):
+    """The longest rows the library takes (K * ncols up to its staged-activation
+    limit) do not fit beside a ring in one launch either: one or two columns run
+    as a K split of the whole-row kernels' two-column consumer."""
+    import torch
+    mq = cuda_ready
+    rows = 37
+    W = synth.q4K_matrix(rows, K, seed=K + ncols, tag=synth.TAG_W)
+    x = synth.activation(K, ncols, seed=K + 1, tag=synth.TAG_X)
+    xq_np = oracle.quantize_q8_0(x)
+    Wd = _to_dev(W)
+    y1, _ = mq.matvec_q4K_q8_0(Wd, rows, K, x=_to_dev(x))
+    y2, _ = mq.matvec_q4K_q8_0(Wd, rows, K, xq=_to_dev(xq_np))
+    torch.cuda.synchronize()
+    assert mq.mq_read_device_status(0) == 0
+    y1 = y1.cpu().numpy()
+    _check_y(y1, W, xq_np, rows, K)
+    assert np.array_equal(y1.view(np.uint32), y2.cpu().numpy().view(np.uint32))
