@@ -37,6 +37,9 @@ if ROOT not in sys.path:
 
 METRIC = "q4_K×q8_0 decode matvec weight GB/s vs HBM peak; 7B-class step µs (1 GPU)"
 UNIT = "GB/s"
+# per-config timings: timed graph replays (each of one or more calls) and untimed ones before them
+CONFIG_REPS = 50
+CONFIG_WARMUP = 10
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
 
@@ -432,8 +435,13 @@ def config_suite(mq, device, oracle_arms=True):
                          oracle_us_all_threads=round(tn * 1e6 / per, 1), oracle_threads=arms[1].threads,
                          gpu_over_oracle_all_threads=round(tn * 1e6 / per / out[name]["us_per_call"], 1))
 
-    def timed(calls, reps=10):
-        """median per-call ms of a graph holding `calls` (a list of zero-arg launches)."""
+    last = {}
+
+    def timed(calls, reps=CONFIG_REPS):
+        """median per-call ms of a graph holding `calls` (a list of zero-arg launches), over at
+        least CONFIG_REPS timed replays after CONFIG_WARMUP untimed ones; the mean and its
+        standard error go to `last` for rec()."""
+        reps = max(reps, CONFIG_REPS)
         with torch.cuda.stream(stream):
             for c in calls:  # warm (lazy state, caches)
                 c()
@@ -442,7 +450,7 @@ def config_suite(mq, device, oracle_arms=True):
         with torch.cuda.graph(g, stream=stream):
             for c in calls:
                 c()
-        for _ in range(2):
+        for _ in range(CONFIG_WARMUP):
             g.replay()
         torch.cuda.synchronize()
         t = []
@@ -454,7 +462,15 @@ def config_suite(mq, device, oracle_arms=True):
                 e1.record(stream)
             torch.cuda.synchronize()
             t.append(e0.elapsed_time(e1))
-        return statistics.median(t) / len(calls)
+        per = [v / len(calls) for v in t]
+        last.update(median=statistics.median(per), mean=statistics.mean(per), sem=sem(per), n=len(per))
+        return last["median"]
+
+    def stats_us(ms):
+        """mean and standard error (µs) of the last timing, on the scale of `ms`"""
+        k = ms / last["median"] if last.get("median") else 0.0
+        return dict(us_mean=round(last["mean"] * k * 1e3, 3), us_sem=round(last["sem"] * k * 1e3, 3),
+                    timed_replays=last["n"])
 
     def mv_calls(Ws, rows, K, x, y):
         descs = [mq.upload_struct(mq.mv_desc(W, rows, K, y, x=x, ncols=x.shape[0]), device) for W in Ws]
@@ -479,8 +495,8 @@ def config_suite(mq, device, oracle_arms=True):
 
     def rec(name, ms, wbytes, **extra):
         gbs = wbytes / (ms / 1e3) / 1e9
-        out[name] = dict(us_per_call=round(ms * 1e3, 3), weight_bytes=wbytes, weight_gbs=round(gbs, 1),
-                         frac_of_measured_hbm=round(gbs / peak, 3), **extra)
+        out[name] = dict(us_per_call=round(ms * 1e3, 3), **stats_us(ms), weight_bytes=wbytes,
+                         weight_gbs=round(gbs, 1), frac_of_measured_hbm=round(gbs / peak, 3), **extra)
 
     # single matvec 512 x 1024 (seed 0): warm, and rotated copies (HBM)
     c = synth.MATVEC_512x1024
@@ -611,7 +627,7 @@ def config_suite(mq, device, oracle_arms=True):
         ms = timed([lambda: mq.gemm_f16(W16, X16, out=Y, stream=torch.cuda.current_stream())], reps=5)
         tf = 2.0 * T * R * K / (ms / 1e3) / 1e12
         out[f"prefill_gemm_{name}_{R}x{K}_T{T}"] = dict(
-            us_per_call=round(ms * 1e3, 2), tflops=round(tf, 1), bound="tensor",
+            us_per_call=round(ms * 1e3, 2), **stats_us(ms), tflops=round(tf, 1), bound="tensor",
             frac_of_measured_f16_peak=round(tf / tflops_peak, 3) if tflops_peak else None,
             kernel="gemm_f16_kernel (tcgen05.mma kind::f16, 128x256 tiles, TMA 128-byte swizzle)")
         layer_us += ms * 1e3
