@@ -153,7 +153,11 @@ mq_status mq_check_mv_desc(const mq_mv_desc* h_desc);
 /* y[c][r] = sum over K of W[r] . q8_0(x)[c], fp32 output.  rows, K, ncols are
  * the host copies of the descriptor's shapes: they size the grid (the capture
  * key) and must equal the device descriptor's.  rows == 0 or ncols == 0
- * launches nothing; K must be a positive multiple of 256. */
+ * launches nothing; K must be a positive multiple of 256.  Where the whole
+ * staged activation does not fit beside the weight ring (e.g. 8 columns of
+ * K = 18944), the call runs as 2..4 launches in stream order, each over an
+ * equal part of every row, the later ones adding to y (y = part 0 + part 1
+ * + ..., in that order); a captured graph then holds one kernel per part. */
 mq_status mq_matvec_q4K_q8_0(const mq_mv_desc* d_desc, int32_t rows, int32_t K, int32_t ncols,
                              void* stream);
 
@@ -199,7 +203,10 @@ typedef struct mq_ffn_desc {
 
 mq_status mq_check_ffn_desc(const mq_ffn_desc* h_desc);
 /* Two launches on `stream`: (1) g|u = W_gu . q8_0(x), h = SiLU(g)*u, h_q8 =
- * q8_0(h) in the epilogue; (2) y = W_down . h_q8. */
+ * q8_0(h) in the epilogue; (2) y = W_down . h_q8 (split over K like the
+ * matvec where h does not fit beside the ring).  The down launch uses
+ * programmatic dependent launch: its weight copies start while (1) drains, and
+ * it reads h only after its grid-dependency wait. */
 mq_status mq_ffn_gu_silu_down(const mq_ffn_desc* d_desc, int32_t H, int32_t I, int32_t ncols,
                               void* stream);
 /* The first of those two launches alone: fills h_q8 (and the debug outputs),
