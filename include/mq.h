@@ -396,10 +396,14 @@ mq_status mq_debug_set_variant(int32_t policy);
  * CTA (which always owns h blocks) never writes its h records and every wait is limited to 50 ms, so every
  * CTA's down phase runs out of time waiting for them: the kernel records
  * MQ_DEV_TIMEOUT, the abort word stops every CTA, and the launch returns.
+ * MQ_FAULT_WITHHOLD_COUNT: in the persistent step kernel the last CTA never
+ * adds its finished phases to the phase counter (waits limited to 50 ms), so
+ * every CTA's wait for the first phase's end runs out, with the same outcome.
  * MQ_FAULT_NONE restores normal operation. */
 #define MQ_FAULT_NONE 0
 #define MQ_FAULT_WITHHOLD_TILE 1
 #define MQ_FAULT_WITHHOLD_RECORDS 2
+#define MQ_FAULT_WITHHOLD_COUNT 3
 mq_status mq_debug_set_fault(int32_t fault);
 
 #ifdef __cplusplus

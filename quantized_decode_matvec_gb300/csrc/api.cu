@@ -438,7 +438,8 @@ int mq_abi_version(void) { return MQ_ABI_VERSION; }
 
 mq_status mq_debug_set_fault(int32_t fault)
 {
-    if (fault != mq::FAULT_NONE && fault != mq::FAULT_WITHHOLD_TILE && fault != mq::FAULT_WITHHOLD_RECORDS)
+    if (fault != mq::FAULT_NONE && fault != mq::FAULT_WITHHOLD_TILE && fault != mq::FAULT_WITHHOLD_RECORDS &&
+        fault != mq::FAULT_WITHHOLD_COUNT)
         return MQ_ERR_INVALID_ARG;
     g_fault_policy = fault;
     return MQ_OK;

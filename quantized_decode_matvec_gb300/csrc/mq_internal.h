@@ -97,7 +97,7 @@ struct StepPlan {
 };
 
 // test-only fault injection (mq_debug_set_fault)
-enum Fault { FAULT_NONE = 0, FAULT_WITHHOLD_TILE = 1, FAULT_WITHHOLD_RECORDS = 2 };
+enum Fault { FAULT_NONE = 0, FAULT_WITHHOLD_TILE = 1, FAULT_WITHHOLD_RECORDS = 2, FAULT_WITHHOLD_COUNT = 3 };
 int fault_policy();
 
 enum Kind { KIND_MV = 0, KIND_DOWN = 1, KIND_GU = 2 };

@@ -424,6 +424,8 @@ __global__ void __launch_bounds__(32 * ring_max_warps<NC, 1>(), 1)
     const int nwc = sp.nwc;
     const uint64_t limit_ns = uint64_t(P0.wait_ms) * 1000000ull;
     unsigned* const count = ws + kWsCountWord;
+    // what a CTA adds per finished phase (test-only fault: the last CTA adds nothing)
+    const unsigned count_inc = (P0.fault == FAULT_WITHHOLD_COUNT && b == G - 1) ? 0u : 1u;
     uint64_t* const rec = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(ws) + kWsRecOff);
 
     {
@@ -514,7 +516,7 @@ __global__ void __launch_bounds__(32 * ring_max_warps<NC, 1>(), 1)
             constexpr int ph = decltype(phc)::value;
             const int k = 4 * l + ph;  // phase number within the launch
             if (sp.R[ph] == 0) {  // a phase left out: only its flag moves on
-                if (ctid == 0 && k + 1 < nphase) red_relaxed_add_u32(count, 1u);
+                if (ctid == 0 && k + 1 < nphase) red_relaxed_add_u32(count, count_inc);
                 return true;
             }
             const MvPlan& P = sp.ph[ph];
@@ -574,7 +576,7 @@ __global__ void __launch_bounds__(32 * ring_max_warps<NC, 1>(), 1)
                     mv_epilogue<NC>(part, P.nseg, pr.nrows, pr.r0, j.y, j.y_ld, ctid, cthr);
             }
             named_barrier_sync(1, cthr);  // this CTA's outputs of phase k are written
-            if (ctid == 0 && k + 1 < nphase) red_relaxed_add_u32(count, 1u);
+            if (ctid == 0 && k + 1 < nphase) red_relaxed_add_u32(count, count_inc);
             return true;
         };
         for (int l = 0; l < sp.n_layers; ++l)

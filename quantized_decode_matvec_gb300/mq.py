@@ -46,6 +46,7 @@ MQ_VARIANT_FORCE_REGISTER = 1
 MQ_FAULT_NONE = 0
 MQ_FAULT_WITHHOLD_TILE = 1
 MQ_FAULT_WITHHOLD_RECORDS = 2
+MQ_FAULT_WITHHOLD_COUNT = 3
 MQ_TYPE_Q4_K = 1
 MQ_TYPE_Q8_0 = 2
 MQ_TYPE_Q4_0 = 3

@@ -47,10 +47,12 @@ def test_fault_setter_rejects_unknown(cuda_ready):
     assert mq.mq_debug_set_variant(7) == mq.MQ_ERR_INVALID_ARG
 
 
-def test_persistent_step_record_wait_runs_out_and_reports(cuda_ready):
-    # the persistent step's dependency waits are bounded too: with the last
-    # CTA's h records withheld, every CTA's down phase runs out of time, the abort word
-    # stops the launch, and the next step runs normally
+@pytest.mark.parametrize("fault", ["records", "count"])
+def test_persistent_step_dependency_wait_runs_out_and_reports(cuda_ready, fault):
+    # the persistent step's dependency waits are bounded too: with the last CTA's h
+    # records withheld (every CTA's down phase runs out of time), or its phases never
+    # added to the phase counter (every CTA's wait for the first phase's end runs out),
+    # the abort word stops the launch, and the next step runs normally
     import torch
     mq = cuda_ready
     case = synth.StepCase("step_fault", 2, 512, 1024, 512, 128, 1, 11)
@@ -68,7 +70,8 @@ def test_persistent_step_record_wait_runs_out_and_reports(cuda_ready):
             b.b[l].copy_(torch.from_numpy(inp["b"]))
             b.c[l].copy_(torch.from_numpy(inp["c"]))
     assert mq.mq_read_device_status(0) == 0
-    assert mq.mq_debug_set_fault(mq.MQ_FAULT_WITHHOLD_RECORDS) == mq.MQ_OK
+    code = mq.MQ_FAULT_WITHHOLD_RECORDS if fault == "records" else mq.MQ_FAULT_WITHHOLD_COUNT
+    assert mq.mq_debug_set_fault(code) == mq.MQ_OK
     try:
         bufs[0].step(flags=mq.MQ_STEP_PERSISTENT)
         torch.cuda.synchronize()                     # returns: every wait is bounded
