@@ -162,11 +162,42 @@ bool plan_mv(int64_t rows, int K, int nc, int kind, int I, const DeviceInfo& dev
 // Returns false when the segments do not fit in the warps.
 // 3..8 columns of q4_K weights as column groups where the split fits
 constexpr bool kColumnGroups = true;
+// 4 or 8 columns of q4_K weights on half-unit lanes where the split fits
+constexpr bool kHalfUnits = true;
 
 static bool unit_split(int C, int nc, bool allow_cols, MvPlan& q)
 {
     q.cmap = 0;
     q.cgw = q.cgu = 0;
+    q.hu = 0;
+    if ((nc == 4 || nc == 8) && allow_cols && kHalfUnits) {
+        // half-unit lanes, groups of four columns: the split counts 2C half-units
+        const int ng = nc / 4, wpg = 15 / ng, CH = 2 * C;
+        double best = 0.0;
+        for (const int L : {32, 16, 8, 4}) {
+            int nseg = (CH + L - 1) / L;
+            const int S = (CH + nseg - 1) / nseg;
+            nseg = (CH + S - 1) / S;
+            if (nseg > wpg) continue;
+            const int used = nseg * (wpg / nseg);
+            const double score = double(CH) / double(nseg * L) * double(used) / double(wpg);
+            if (score > best + 1e-9) {
+                best = score;
+                q.L = L;
+                q.nseg = nseg;
+                q.S = S;
+                q.cgu = used;
+            }
+        }
+        if (best > 0.0) {
+            q.hu = 1;
+            q.cgw = wpg;
+            q.nwc = ng * wpg;
+            q.rg = (q.cgu / q.nseg) * (32 / q.L);
+            return true;
+        }
+        q.cgu = 0;
+    }
     if (nc >= 3 && allow_cols && kColumnGroups) {
         // column groups: (nc+1)/2 groups of 15/groups warps, each group split as
         // the two-column consumer would split its warps

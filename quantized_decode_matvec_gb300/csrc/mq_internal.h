@@ -37,6 +37,9 @@ struct MvPlan {
     // warps, group g on columns 2g, 2g+1 with their activation in registers (the
     // one- and two-column consumer), cgu of each group's warps with work; 0: off
     int cgw, cgu;
+    // half-unit lanes (4 or 8 columns): the unit split above counts half-units
+    // and the groups take four columns each (cgw, cgu as for column groups)
+    int hu;
     // K split (matvec and down, q4_K, when one launch cannot stage the whole
     // activation): ksplit launches in stream order, each over kpn super-blocks
     // of every row starting at super-block kp0; launch i > 0 adds its sums to y

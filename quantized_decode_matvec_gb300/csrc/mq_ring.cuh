@@ -255,6 +255,107 @@ __device__ __noinline__ bool ring_consume_cols(const ConsumeArgs p, const uint8_
     return true;
 }
 
+// Half-unit lanes (3..8 columns, q4_K weights): lane l of a (row, segment)
+// item works on half-unit v = seg*S + l of every row: 64 weights, the two
+// sub-blocks 2hh, 2hh+1 (hh = v & 1) of unit v >> 1, i.e. 32 quant bytes and
+// the super-block's header.  Its activation is 16 code words and two scale
+// pairs per column, so a lane holds up to four columns in registers and
+// unpacks each weight once for them.  Warps form groups of four columns (as
+// ring_consume_groups does for two); the unit split counts half-units.
+template <int NCW, int L>
+__device__ __noinline__ bool ring_consume_half(const ConsumeArgs p, const uint8_t* ring, uint64_t* full,
+                                               uint64_t* empty, const UnitAct act, float* __restrict__ part,
+                                               uint64_t limit_ns)
+{
+    const int nrows = p.nrows, nwc_used = p.nwc_used;
+    const int warp = (threadIdx.x >> 5) - p.warp0, lane = threadIdx.x & 31;
+    const int nseg = p.nseg;
+    const int seg = warp % nseg, jj = warp / nseg;
+    constexpr int ipw = 32 / L;
+    const int sub = lane / L, l = lane - sub * L;
+    const int rho0 = jj * ipw;
+    const int rg = p.rg;
+    const int v = seg * p.S + l;
+    const bool warp_active = warp < nwc_used;
+    const bool on = warp_active && (l < p.S) && (v < 2 * p.C);
+    const int vv = on ? v : 0;
+    const int u = vv >> 1, hh = vv & 1;
+    const bool upper = (u & 1) != 0;
+    const uint32_t row_bytes = uint32_t(p.C / 2) * kQ4KBytes;
+    const uint32_t off_h = uint32_t(u >> 1) * kQ4KBytes;
+    const uint32_t off_q = off_h + 16 + 64 * uint32_t(u & 1) + 32 * uint32_t(hh);
+    const uint32_t j0 = 2 * uint32_t(hh);  // the half's low-nibble sub-block within the unit
+    uint4 A[NCW][4];
+    float dq0[NCW], dq1[NCW], dqs0[NCW], dqs1[NCW];
+#pragma unroll
+    for (int c = 0; c < NCW; ++c) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) A[c][i] = act.planes[size_t(c * 8 + 4 * hh + i) * act.U + u];
+        const float4 d4 = act.scales[(size_t(c) * act.U + u) * 2], s4 = act.scales[(size_t(c) * act.U + u) * 2 + 1];
+        dq0[c] = hh ? d4.z : d4.x;
+        dq1[c] = (hh ? d4.w : d4.y) * 0.0625f;  // high nibbles are used as 16*q
+        dqs0[c] = hh ? s4.z : s4.x;
+        dqs1[c] = hh ? s4.w : s4.y;
+    }
+    const bool storer = l == 0 || l == (L >> 1);
+    const int srow = sub + (l == 0 ? 0 : rg);
+    const int pstep = 2 * rg * nseg * p.pcols;
+    // one row's contribution per column
+    auto row = [&](const uint8_t* stage, int r, float (&x)[NCW]) {
+        const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(stage)) + uint32_t(r) * row_bytes;
+        uint4 hd, q0, q1;
+        lds128(hd, a + off_h);
+        lds128(q0, a + off_q);
+        lds128(q1, a + off_q + 16);
+        const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&hd.x));
+        const uint32_t S0 = hd.y, S1 = hd.z, S2 = hd.w;
+        const uint32_t mlo = upper ? 0x0f0f0f0fu : 0x3f3f3f3fu;
+        const uint32_t mhi = upper ? 0x30303030u : 0u;
+        const uint32_t scw = ((upper ? S2 : S0) & mlo) | ((S0 >> 2) & mhi);
+        const uint32_t mw = ((upper ? (S2 >> 4) : S1) & mlo) | ((S1 >> 2) & mhi);
+        const int sc0 = int(__byte_perm(scw, 0u, 0x4440u | j0)), sc1 = int(__byte_perm(scw, 0u, 0x4440u | (j0 + 1)));
+        const float m0 = __int_as_float(__byte_perm(mw, 0x4B000000u, 0x7540u | j0)) - 8388608.0f;
+        const float m1 = __int_as_float(__byte_perm(mw, 0x4B000000u, 0x7540u | (j0 + 1))) - 8388608.0f;
+#pragma unroll
+        for (int c = 0; c < NCW; ++c) {
+            const int s0 = dot16_lo(q1, A[c][1], dot16_lo(q0, A[c][0], 0));
+            const int s1 = dot16_hi(q1, A[c][3], dot16_hi(q0, A[c][2], 0));
+            const float t = fmaf(dq1[c], float(sc1 * s1), dq0[c] * float(sc0 * s0));
+            const float um = fmaf(m1, dqs1[c], m0 * dqs0[c]);
+            x[c] = fmaf(-dd.y, um, dd.x * t);
+        }
+    };
+    int s = p.tile_base % p.ns;
+    uint32_t par = uint32_t(p.tile_base / p.ns) & 1u;
+    for (int tr0 = 0; tr0 < nrows; tr0 += p.T) {
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], par, limit_ns));
+        if (!ok) return false;
+        const uint8_t* stage = ring + uint32_t(s) * uint32_t(p.stage_bytes);
+        const int tn = min(p.T, nrows - tr0);
+        float* pq = part + (size_t(tr0 + rho0 + srow) * nseg + seg) * p.pcols + p.pc0;
+        for (int r = warp_active ? rho0 : tn; r < tn; r += 2 * rg, pq += pstep) {  // r is warp-uniform
+            const int ra = r + sub, rb = r + rg + sub;
+            const bool st = storer && r + srow < tn;
+            const bool va = on && ra < tn, vb = on && rb < tn;
+            float xa[NCW], xb[NCW];
+            row(stage, min(ra, tn - 1), xa);
+            row(stage, min(rb, tn - 1), xb);
+#pragma unroll
+            for (int c = 0; c < NCW; ++c) {
+                const float t = group_sum2<L>(va ? xa[c] : 0.0f, vb ? xb[c] : 0.0f, l);
+                if (st) pq[c] = t;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        if (++s == p.ns) {
+            s = 0;
+            par ^= 1u;
+        }
+    }
+    return true;
+}
+
 // Column groups (3..8 columns): the consumer warps split into groups of
 // p.cgw warps; group g runs the one- or two-column consumer (activation in
 // registers, the row loop without branches) on columns 2g and 2g+1 of every
@@ -288,8 +389,29 @@ __device__ __forceinline__ bool ring_consume_groups(ConsumeArgs a, int cgw, cons
 #undef MQ_GROUP_L
 }
 
+// Groups of four columns on half-unit lanes (4 or 8 columns): group g on
+// columns 4g..4g+3.
+template <int NC>
+__device__ __forceinline__ bool ring_consume_half_groups(ConsumeArgs a, int cgw, const uint8_t* ring, uint64_t* full,
+                                                         uint64_t* empty, const UnitAct& act,
+                                                         float* __restrict__ part, uint64_t limit_ns)
+{
+    static_assert(NC % 4 == 0, "half-unit lanes take groups of four columns");
+    constexpr int NG = NC / 4;
+    const int g = (int(threadIdx.x) >> 5) / cgw;
+    a.pc0 = 4 * g;
+    a.warp0 = g * cgw;
+    if (g >= NG) a.nwc_used = 0;
+    const int gc = g < NG ? 4 * g : 0;
+    const UnitAct v{act.planes + size_t(gc) * 8 * act.U, act.scales + size_t(gc) * act.U * 2, act.U};
+    if (a.L == 32) return ring_consume_half<4, 32>(a, ring, full, empty, v, part, limit_ns);
+    if (a.L == 16) return ring_consume_half<4, 16>(a, ring, full, empty, v, part, limit_ns);
+    if (a.L == 8) return ring_consume_half<4, 8>(a, ring, full, empty, v, part, limit_ns);
+    return ring_consume_half<4, 4>(a, ring, full, empty, v, part, limit_ns);
+}
+
 // kMode 1: the kernel was built for column lanes (its plans all have cmap = 1);
-// kMode 3: for column groups (cgw > 0)
+// kMode 3: for column groups (cgw > 0); kMode 4: for half-unit lanes (hu = 1)
 template <int NC, class Fmt = FmtQ4K, int kMode = 0>
 __device__ __forceinline__ bool ring_consume(const MvPlan& p, int nrows, int tile_base, int nwc_used,
                                              const uint8_t* ring, uint64_t* full, uint64_t* empty,
@@ -299,6 +421,13 @@ __device__ __forceinline__ bool ring_consume(const MvPlan& p, int nrows, int til
     if constexpr (kMode == 3) {
         ConsumeArgs ag = consume_args(p, nrows, tile_base, p.cgu, NC);
         return ring_consume_groups<NC, Fmt>(ag, p.cgw, ring, full, empty, act, part, limit_ns);
+    }
+    if constexpr (kMode == 4) {
+        if constexpr (NC % 4 == 0) {
+            ConsumeArgs ag = consume_args(p, nrows, tile_base, p.cgu, NC);
+            return ring_consume_half_groups<NC>(ag, p.cgw, ring, full, empty, act, part, limit_ns);
+        }
+        return false;
     }
     if constexpr (kMode == 1) return ring_consume_cols<NC, Fmt>(a, ring, full, empty, act, part, limit_ns);
     if (p.L == 32) return ring_consume_L<NC, 32, Fmt>(a, ring, full, empty, act, part, limit_ns);

@@ -553,7 +553,9 @@ __global__ void __launch_bounds__(32 * ring_max_warps<NC, 1>(), 1)
             named_barrier_sync(1, cthr);
             if (abort_flag) return false;
             bool ok;
-            if (NC >= 3 && P.cgw)  // the same split as the per-matrix kernel of this shape
+            if (NC % 4 == 0 && P.hu)  // the same split as the per-matrix kernel of this shape
+                ok = ring_consume<NC, FmtQ4K, 4>(P, pr.nrows, gi, P.nwc, ring, full, empty, act, part, limit_ns);
+            else if (NC >= 3 && P.cgw)
                 ok = ring_consume<NC, FmtQ4K, 3>(P, pr.nrows, gi, P.nwc, ring, full, empty, act, part, limit_ns);
             else if (NC >= 3 && P.cmap)
                 ok = ring_consume<NC, FmtQ4K, 1>(P, pr.nrows, gi, P.nwc, ring, full, empty, act, part, limit_ns);

@@ -30,11 +30,37 @@ static cudaError_t launch_cols_kind(const void* desc, int a, int b, int ncols, c
     return cudaErrorInvalidValue;
 }
 
+// half-unit lanes: 4 or 8 columns only
+template <int KIND>
+static cudaError_t launch_half_kind(const void* desc, int a, int b, int ncols, const MvPlan& p, unsigned* status,
+                                    cudaStream_t s, bool pdl)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.grid);
+    cfg.blockDim = dim3(p.block);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (ncols == 4) return cudaLaunchKernelEx(&cfg, ring_kernel<4, KIND, FmtQ4K, 4>, desc, a, b, p, status);
+    if (ncols == 8) return cudaLaunchKernelEx(&cfg, ring_kernel<8, KIND, FmtQ4K, 4>, desc, a, b, p, status);
+    return cudaErrorInvalidConfiguration;
+}
+
 cudaError_t launch_ring_cols(const void* desc, int kind, int a, int b, int ncols, const MvPlan& p, unsigned* status,
                              cudaStream_t s, bool pdl)
 {
     if (ncols < 3 || p.block > 32 * ring_max_warps<3, 1>()) return cudaErrorInvalidConfiguration;
-    if (p.cgw) {
+    if (p.hu) {
+        switch (kind) {
+            case KIND_MV: return launch_half_kind<KIND_MV>(desc, a, b, ncols, p, status, s, pdl);
+            case KIND_DOWN: return launch_half_kind<KIND_DOWN>(desc, a, b, ncols, p, status, s, pdl);
+            case KIND_GU: return launch_half_kind<KIND_GU>(desc, a, b, ncols, p, status, s, pdl);
+        }
+    } else if (p.cgw) {
         switch (kind) {
             case KIND_MV: return launch_cols_kind<KIND_MV, 3>(desc, a, b, ncols, p, status, s, pdl);
             case KIND_DOWN: return launch_cols_kind<KIND_DOWN, 3>(desc, a, b, ncols, p, status, s, pdl);
@@ -66,6 +92,8 @@ cudaError_t set_ring_cols_attributes(int max_smem)
         MQ_SET1(N, KIND_DOWN, 2) MQ_SET1(N, KIND_GU, 2) MQ_SET1(N, KIND_MV, 3) MQ_SET1(N, KIND_DOWN, 3) \
             MQ_SET1(N, KIND_GU, 3)
     MQ_SET(3) MQ_SET(4) MQ_SET(5) MQ_SET(6) MQ_SET(7) MQ_SET(8)
+    MQ_SET1(4, KIND_MV, 4) MQ_SET1(4, KIND_DOWN, 4) MQ_SET1(4, KIND_GU, 4)
+    MQ_SET1(8, KIND_MV, 4) MQ_SET1(8, KIND_DOWN, 4) MQ_SET1(8, KIND_GU, 4)
 #undef MQ_SET
 #undef MQ_SET1
     return e;

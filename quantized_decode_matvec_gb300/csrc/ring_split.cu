@@ -48,6 +48,25 @@ cudaError_t launch_ring_split(const void* desc, int kind, int a, int b, int ncol
     }
     // 3..8 columns: the 16-warp instances (column groups, column lanes or unit lanes)
     if (p.block > 32 * ring_max_warps<3, 1>()) return cudaErrorInvalidConfiguration;
+    if (p.hu) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(p.grid);
+        cfg.blockDim = dim3(p.block);
+        cfg.dynamicSmemBytes = p.smem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (ncols == 4)
+            return mv ? cudaLaunchKernelEx(&cfg, ring_kernel<4, KIND_MV, FmtQ4K, 4, true>, desc, a, b, p, status)
+                      : cudaLaunchKernelEx(&cfg, ring_kernel<4, KIND_DOWN, FmtQ4K, 4, true>, desc, a, b, p, status);
+        if (ncols == 8)
+            return mv ? cudaLaunchKernelEx(&cfg, ring_kernel<8, KIND_MV, FmtQ4K, 4, true>, desc, a, b, p, status)
+                      : cudaLaunchKernelEx(&cfg, ring_kernel<8, KIND_DOWN, FmtQ4K, 4, true>, desc, a, b, p, status);
+        return cudaErrorInvalidConfiguration;
+    }
     if (p.cgw)
         return mv ? launch_split_kind<KIND_MV, 3>(desc, a, b, ncols, p, status, s, pdl)
                   : launch_split_kind<KIND_DOWN, 3>(desc, a, b, ncols, p, status, s, pdl);
@@ -69,6 +88,7 @@ cudaError_t set_ring_split_attributes(int max_smem)
     MQ_SET1(N, KIND_MV, 1) MQ_SET1(N, KIND_DOWN, 1) MQ_SET1(N, KIND_MV, 2) MQ_SET1(N, KIND_DOWN, 2) \
         MQ_SET1(N, KIND_MV, 3) MQ_SET1(N, KIND_DOWN, 3)
     MQ_SET(3) MQ_SET(4) MQ_SET(5) MQ_SET(6) MQ_SET(7) MQ_SET(8)
+    MQ_SET1(4, KIND_MV, 4) MQ_SET1(4, KIND_DOWN, 4) MQ_SET1(8, KIND_MV, 4) MQ_SET1(8, KIND_DOWN, 4)
 #undef MQ_SET
 #undef MQ_SET1
     return e;
