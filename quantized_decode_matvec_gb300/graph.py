@@ -12,6 +12,7 @@ before each replay); the descriptors and the grid sizes are fixed at capture.
 """
 from __future__ import annotations
 
+import contextlib
 import logging
 from typing import Callable, Optional
 
@@ -162,3 +163,99 @@ class PinnedFeeder:
     def push(self, stream) -> None:
         with torch.cuda.stream(stream):
             self.bufs.inputs.copy_(self.inputs, non_blocking=True)  # one host-to-device copy
+
+
+class PinnedReadback:
+    """Device-to-host readback through a self-held pinned staging buffer.
+
+    "07 · R3 — small-model per-token overhead", A2 (the pinned readback): a
+    read copies the device bytes into a page-locked buffer that this object
+    keeps (one DMA, no bounce through the driver's own staging) and then into
+    the caller's host tensor with an ordinary host copy.  The buffer is
+    allocated on first use and replaced by a larger one when a read needs more
+    than it holds; it is never smaller than ``min_bytes`` (4 MiB), so that
+    small changes in the read size do not reallocate it.  When page-locked
+    memory cannot be had, the read copies straight into the caller's pageable
+    tensor and a warning is logged once per process; the next read tries the
+    allocation again.
+
+    ``pinned=False`` always takes the pageable path (an A/B switch).
+    ``alloc`` (test hook) replaces the allocator: ``alloc(nbytes)`` returns a
+    1-D uint8 host tensor or raises, which lets a host-only test plant an
+    allocation failure.
+    """
+
+    MIN_BYTES = 4 * 1024 * 1024
+    _warned = False  # one warning per process
+
+    def __init__(self, pinned: bool = True, min_bytes: int = MIN_BYTES,
+                 alloc: Optional[Callable[[int], torch.Tensor]] = None):
+        self.pinned = pinned
+        self.min_bytes = int(min_bytes)
+        self._alloc = alloc if alloc is not None else self._alloc_pinned
+        self._buf: Optional[torch.Tensor] = None
+        self.allocations = 0  # buffers allocated (the first one and each growth)
+        self.fallbacks = 0    # reads that took the pageable path after a failed allocation
+
+    @staticmethod
+    def _alloc_pinned(nbytes: int) -> torch.Tensor:
+        return torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+
+    @property
+    def capacity(self) -> int:
+        """Bytes of the pinned buffer held now (0 before the first read or after a failure)."""
+        return 0 if self._buf is None else self._buf.numel()
+
+    def _staging(self, nbytes: int) -> Optional[torch.Tensor]:
+        if self._buf is not None and self._buf.numel() >= nbytes:
+            return self._buf
+        self._buf = None  # release the smaller buffer before asking for the larger one
+        need = max(nbytes, self.min_bytes)
+        try:
+            buf = self._alloc(need)
+        except (RuntimeError, MemoryError) as e:
+            if not PinnedReadback._warned:
+                PinnedReadback._warned = True
+                log.warning("pinned readback buffer of %d bytes not allocated (%s); "
+                            "reading through pageable memory", need, e)
+            return None
+        if buf.dtype != torch.uint8 or buf.dim() != 1 or buf.numel() < need:
+            raise ValueError("readback allocator returned a buffer of the wrong type or size")
+        self._buf = buf
+        self.allocations += 1
+        return buf
+
+    def read_into(self, dst: torch.Tensor, src: torch.Tensor, stream=None) -> torch.Tensor:
+        """Copy ``src`` (a contiguous tensor, normally on the GPU) into the contiguous host
+        tensor ``dst`` of the same dtype and number of elements; returns ``dst``.
+
+        The device-to-host copy runs on ``stream`` (torch's current stream if None) and is
+        complete when this returns.
+        """
+        if dst.device.type != "cpu" or not dst.is_contiguous() or not src.is_contiguous():
+            raise ValueError("read_into needs a contiguous host dst and a contiguous src")
+        if dst.dtype != src.dtype or dst.numel() != src.numel():
+            raise ValueError("dst and src differ in dtype or element count")
+        nbytes = src.numel() * src.element_size()
+        if nbytes == 0:
+            return dst
+        st = self._staging(nbytes) if self.pinned else None
+        on_gpu = src.device.type == "cuda"
+        ctx = torch.cuda.stream(stream) if (on_gpu and stream is not None) else contextlib.nullcontext()
+        with ctx:
+            if st is None:
+                if self.pinned:
+                    self.fallbacks += 1
+                dst.copy_(src)  # pageable: the copy blocks until the bytes are in dst
+                return dst
+            stage = st[:nbytes]
+            stage.copy_(src.reshape(-1).view(torch.uint8), non_blocking=on_gpu)
+            if on_gpu:
+                torch.cuda.current_stream().synchronize()
+        dst.reshape(-1).view(torch.uint8).copy_(stage)  # host to host
+        return dst
+
+    def read(self, src: torch.Tensor, stream=None) -> torch.Tensor:
+        """A new host tensor with the contents of ``src`` (same dtype and shape)."""
+        return self.read_into(torch.empty(src.shape, dtype=src.dtype), src.contiguous(), stream)
+

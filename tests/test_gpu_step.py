@@ -324,3 +324,28 @@ def test_step_graph_with_host_io(cuda_ready):
         torch.cuda.synchronize()
         assert np.array_equal(host_out.numpy().view(np.uint8), eager.outputs.cpu().numpy().view(np.uint8)), r
     assert mq.mq_read_device_status(0) == 0
+
+
+def test_step_outputs_through_pinned_readback(cuda_ready):
+    # the step's outputs read back through the self-held pinned buffer: a first
+    # read into a buffer sized for it, then a read larger than that buffer
+    # (5.6 MB against 4 MiB), which grows it; every read byte-identical to .cpu()
+    import torch
+    from quantized_decode_matvec_gb300.graph import PinnedReadback
+    mq = cuda_ready
+    wdev, host = _weights(SMALL)
+    bufs = _bufs(mq, SMALL, wdev)
+    _set_inputs(bufs, *_inputs(SMALL, 77))
+    bufs.step(flags=mq.MQ_STEP_PERSISTENT)
+    torch.cuda.synchronize()
+    rb = PinnedReadback()
+    out = rb.read(bufs.outputs)
+    assert rb.capacity == PinnedReadback.MIN_BYTES and rb._buf.is_pinned() and rb.fallbacks == 0
+    assert np.array_equal(out.numpy().view(np.uint8), bufs.outputs.cpu().numpy().view(np.uint8))
+    big = torch.randint(-2**31, 2**31 - 1, (1_400_000,), dtype=torch.int32, device="cuda")
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    got = rb.read(big, stream=st)
+    assert rb.capacity == 5_600_000 and rb.allocations == 2 and rb._buf.is_pinned()
+    assert torch.equal(got, big.cpu())
+    assert mq.mq_read_device_status(0) == 0
