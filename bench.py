@@ -702,7 +702,18 @@ def run_kernel_case(args):
     if args.kernel_case.startswith("gemm_o"):
         R = K = f.H  # the 7B o projection: 224 tiles on 152 CTAs, the last wave split
     W = torch.from_numpy(synth.q4K_matrix(R, K, seed=f.seed, tag=synth.TAG_GU)).to(device)
-    if args.kernel_case.startswith("gemm"):
+    if args.kernel_case.startswith("ffn"):
+        # the whole 7B FFN (gate/up + SiLU·mul + q8_0(h), then down) for ncols columns
+        nc = int(args.kernel_case.split("ncols")[1])
+        Wd = torch.from_numpy(synth.q4K_matrix(f.H, f.I, seed=f.seed + 1)).to(device)
+        x = torch.from_numpy(synth.activation(f.H, nc, seed=93)).to(device)
+        y = torch.empty((nc, f.H), dtype=torch.float32, device=device)
+        h = torch.empty((nc, mq.mq_q8_0_bytes(f.I)), dtype=torch.uint8, device=device)
+        d = mq.upload_struct(mq.ffn_desc(W, Wd, f.H, f.I, h, y, x=x, ncols=nc), device)
+        run = lambda: mq._check(mq.mq_ffn_gu_silu_down(d.data_ptr(), f.H, f.I, nc,
+                                                        torch.cuda.current_stream().cuda_stream), "ffn")
+        work = {"weight_bytes_per_launch": W.numel() + Wd.numel()}
+    elif args.kernel_case.startswith("gemm"):
         T = 2048
         W16 = mq.dequant_q4K_f16(W, R, K)
         X16 = mq.convert_f32_f16(torch.from_numpy(synth.activation(K, T, seed=91)).to(device))
@@ -911,7 +922,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-config timings (context only)")
     ap.add_argument("--no-chained-arm", action="store_true", help="skip the chained-step arm (context only)")
-    ap.add_argument("--kernel-case", choices=["gemm_gu_T2048", "gemm_o_T2048", "mmq_gu_ncols16", "mmq_gu_ncols64"],
+    ap.add_argument("--kernel-case", choices=["gemm_gu_T2048", "gemm_o_T2048", "mmq_gu_ncols16", "mmq_gu_ncols64",
+                                              "ffn_ncols4", "ffn_ncols8"],
                     default=None,
                     help="run one kernel on a fixed small case a few times (a target for ncu), not the benchmark")
     ap.add_argument("--layers", type=int, default=28,
