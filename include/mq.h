@@ -261,7 +261,10 @@ typedef struct mq_step_shape {
  * `workspace` as tagged records (a data word and its phase in one 8-byte
  * store), which the down phase reads and checks word by word.  Both paths give
  * bit-identical outputs.  The persistent kernel needs every SM: it fails with
- * MQ_ERR_CUDA if the device cannot host its whole grid at once.
+ * MQ_ERR_CUDA if the device cannot host its whole grid at once.  It returns
+ * MQ_ERR_UNSUPPORTED where its shared memory cannot hold a phase's whole
+ * activation beside its weight ring (H = 3584, I = 18944 from 4 columns on); the
+ * four-launch form runs those shapes.
  *
  * Inputs of the persistent step:
  *  - default: every input (a_l, b_l, c_l or their q8_0 forms) is a buffer that
@@ -405,6 +408,45 @@ mq_status mq_debug_set_variant(int32_t policy);
 #define MQ_FAULT_WITHHOLD_RECORDS 2
 #define MQ_FAULT_WITHHOLD_COUNT 3
 mq_status mq_debug_set_fault(int32_t fault);
+
+/* Test-only view of the launch planner, on the host: no GPU and no mq_init
+ * needed.  Gives the plan a call would take on a device with num_sms SMs,
+ * l2_bytes of L2 and max_smem bytes of opt-in shared memory per block, under
+ * the current variant policy.
+ *  - mq_debug_plan_mv: one q4_K projection as mq_matvec_q4K_q8_0
+ *    (MQ_PLAN_MATVEC: rows x K) or mq_ffn_gu_silu_down plans it
+ *    (MQ_PLAN_GATE_UP: rows = 2I, K = H, I given; MQ_PLAN_DOWN: rows = H,
+ *    K = I).  Writes MQ_PLAN_FIELDS values to out.
+ *  - mq_debug_plan_step: the persistent step (MQ_STEP_PERSISTENT) of *shape.
+ *    Writes MQ_STEP_PLAN_FIELDS values, then MQ_PLAN_FIELDS values for each
+ *    phase (qkv, o, gate/up, down; a phase left out has variant 0 and rows
+ *    per CTA 0).
+ * Per-projection fields, in order: 0 variant (1: bulk-copy ring kernels,
+ * 0: register-streaming kernels), 1 grid, 2 block, 3 dynamic shared memory
+ * bytes, 4 C (ring plans: 128-weight units per row or per part of a K split;
+ * register plans: 64-weight chunks), 5 L (lanes per item), 6 S (units, or
+ * half-units, per segment), 7 nseg (segments per row), 8 consumer warps,
+ * 9 row-lanes per segment, 10 T (rows per tile), 11 ring stages, 12 bytes
+ * per stage, 13 rows per CTA, 14 column lanes (0/1), 15 warps per column
+ * group (0: none), 16 warps with work per group, 17 half-unit lanes (0/1),
+ * 18 K-split parts (1: whole rows), 19 super-blocks per part (0: whole rows).
+ * Step fields: 0 grid, 1 block, 2 dynamic shared memory bytes, 3 consumer
+ * warps, 4 ring stages, 5 bytes per stage, 6 L2-prefetched tiles per CTA,
+ * 7 workspace bytes.
+ * Both return MQ_ERR_INVALID_ARG for a null pointer, an n_out smaller than
+ * what they write, a bad kind or a non-positive device description; the
+ * shape checks of the call they stand for (MQ_ERR_SHAPE ...); and
+ * MQ_ERR_UNSUPPORTED where that call would find no plan on the device.
+ * Nothing is written unless they return MQ_OK. */
+#define MQ_PLAN_MATVEC 0
+#define MQ_PLAN_DOWN 1
+#define MQ_PLAN_GATE_UP 2
+#define MQ_PLAN_FIELDS 20
+#define MQ_STEP_PLAN_FIELDS 8
+mq_status mq_debug_plan_mv(int32_t kind, int64_t rows, int32_t K, int32_t ncols, int32_t I, int32_t num_sms,
+                           int64_t l2_bytes, int32_t max_smem, int64_t* out, int32_t n_out);
+mq_status mq_debug_plan_step(const mq_step_shape* shape, int32_t num_sms, int64_t l2_bytes, int32_t max_smem,
+                             int64_t* out, int32_t n_out);
 
 #ifdef __cplusplus
 }

@@ -893,4 +893,73 @@ mq_status mq_debug_block_sums_q4K_q8_0(const mq_mv_desc* d_desc, int32_t rows, i
     return e == cudaSuccess ? MQ_OK : cuda_fail(e);
 }
 
+// the planner's view for the test hooks below (field order as in mq.h)
+static void plan_fields(const mq::MvPlan& p, int64_t* o)
+{
+    const int64_t v[MQ_PLAN_FIELDS] = {p.variant, p.grid,         p.block,        p.smem, p.C,   p.L,   p.S,
+                                       p.nseg,    p.nwc,          p.rg,           p.T,    p.ns,  p.stage_bytes,
+                                       p.rows_per_cta, p.cmap,    p.cgw,          p.cgu,  p.hu,  p.ksplit,
+                                       p.kpn};
+    for (int i = 0; i < MQ_PLAN_FIELDS; ++i) o[i] = v[i];
+}
+
+static bool fake_device(int32_t num_sms, int64_t l2_bytes, int32_t max_smem, mq::DeviceInfo* d)
+{
+    if (num_sms <= 0 || l2_bytes <= 0 || l2_bytes > INT32_MAX || max_smem <= 0) return false;
+    d->num_sms = num_sms;
+    d->l2_bytes = int(l2_bytes);
+    d->max_smem_optin = max_smem;
+    return true;
+}
+
+mq_status mq_debug_plan_mv(int32_t kind, int64_t rows, int32_t K, int32_t ncols, int32_t I, int32_t num_sms,
+                           int64_t l2_bytes, int32_t max_smem, int64_t* out, int32_t n_out)
+{
+    mq::DeviceInfo dev;
+    if (!out || n_out < MQ_PLAN_FIELDS || !fake_device(num_sms, l2_bytes, max_smem, &dev)) return MQ_ERR_INVALID_ARG;
+    mq_status st;
+    int mk = mq::KIND_MV;
+    if (kind == MQ_PLAN_MATVEC) {
+        st = check_mv_shape(rows, K, ncols);
+    } else if (kind == MQ_PLAN_DOWN) {
+        st = check_ffn_shape(rows, K, ncols);  // rows = H, K = I
+        mk = mq::KIND_DOWN;
+    } else if (kind == MQ_PLAN_GATE_UP) {
+        st = (rows != 2 * int64_t(I)) ? MQ_ERR_SHAPE : check_ffn_shape(K, I, ncols);  // rows = 2I, K = H
+        mk = mq::KIND_GU;
+    } else {
+        return MQ_ERR_INVALID_ARG;
+    }
+    if (st != MQ_OK) return st;
+    if (rows == 0 || ncols == 0) return MQ_ERR_INVALID_ARG;  // the call would launch nothing
+    mq::MvPlan p;
+    if (!mq::plan_mv(rows, K, ncols, mk, mk == mq::KIND_GU ? I : 0, dev, &p)) return MQ_ERR_UNSUPPORTED;
+    plan_fields(p, out);
+    return MQ_OK;
+}
+
+mq_status mq_debug_plan_step(const mq_step_shape* h, int32_t num_sms, int64_t l2_bytes, int32_t max_smem,
+                             int64_t* out, int32_t n_out)
+{
+    mq::DeviceInfo dev;
+    if (!h || !out || n_out < MQ_STEP_PLAN_FIELDS + 4 * MQ_PLAN_FIELDS ||
+        !fake_device(num_sms, l2_bytes, max_smem, &dev))
+        return MQ_ERR_INVALID_ARG;
+    mq_status st = check_step_shape(h);
+    if (st != MQ_OK) return st;
+    if (h->n_layers == 0 || h->ncols == 0) return MQ_ERR_INVALID_ARG;  // the call would launch nothing
+    mq::StepPlan sp;
+    if (!mq::plan_step(*h, dev, &sp)) return MQ_ERR_UNSUPPORTED;
+    const int64_t g[MQ_STEP_PLAN_FIELDS] = {sp.grid, 32 * (sp.nwc + 1), sp.smem, sp.nwc, sp.ph[0].ns,
+                                            sp.ph[0].stage_bytes, sp.pf_tiles, int64_t(sp.ws_bytes)};
+    for (int i = 0; i < MQ_STEP_PLAN_FIELDS; ++i) out[i] = g[i];
+    for (int ph = 0; ph < 4; ++ph) {
+        mq::MvPlan q = sp.ph[ph];
+        if (sp.R[ph] == 0) q = mq::MvPlan{};  // a phase left out
+        q.ksplit = 1;                          // the persistent kernel takes whole rows
+        plan_fields(q, out + MQ_STEP_PLAN_FIELDS + ph * MQ_PLAN_FIELDS);
+    }
+    return MQ_OK;
+}
+
 }  // extern "C"

@@ -59,6 +59,11 @@ MQ_STEP_CHAINED = 4
 MQ_STEP_WORKSPACE_BYTES = 4352
 MQ_NOALLOC_HQ8_MAX_BYTES = 131072
 MQ_MMQ_MAX_NCOLS = 64
+MQ_PLAN_MATVEC = 0
+MQ_PLAN_DOWN = 1
+MQ_PLAN_GATE_UP = 2
+MQ_PLAN_FIELDS = 20
+MQ_STEP_PLAN_FIELDS = 8
 
 
 class MvDesc(ctypes.Structure):
@@ -119,6 +124,8 @@ _sig("mq_gemm_f16", c_i32, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_vp)
 _sig("mq_debug_block_sums_q4K_q8_0", c_i32, c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp)
 _sig("mq_debug_set_variant", c_i32, c_i32)
 _sig("mq_debug_set_fault", c_i32, c_i32)
+_sig("mq_debug_plan_mv", c_i32, c_i32, c_i64, c_i32, c_i32, c_i32, c_i32, c_i64, c_i32, ctypes.POINTER(c_i64), c_i32)
+_sig("mq_debug_plan_step", c_i32, ctypes.POINTER(StepShape), c_i32, c_i64, c_i32, ctypes.POINTER(c_i64), c_i32)
 
 # the exported names, one per declaration in include/mq.h
 EXPORTS = ["mq_status_string", "mq_abi_version", "mq_last_cuda_error", "mq_init", "mq_read_device_status",
@@ -127,7 +134,8 @@ EXPORTS = ["mq_status_string", "mq_abi_version", "mq_last_cuda_error", "mq_init"
            "mq_matvec_q4K_q8_0", "mq_matvec_q4_0_q8_0", "mq_matvec_q8_0_q8_0", "mq_check_ffn_desc", "mq_ffn_gu_silu_down", "mq_ffn_gate_up", "mq_step", "mq_step_workspace_bytes",
            "mq_ffn_gu_silu_down_noalloc", "mq_dequant_q4K_f16", "mq_convert_f32_f16", "mq_gemm_f16",
            "mq_mmq_workspace_bytes", "mq_mmq_q4K_q8_0",
-           "mq_debug_block_sums_q4K_q8_0", "mq_debug_set_variant", "mq_debug_set_fault"]
+           "mq_debug_block_sums_q4K_q8_0", "mq_debug_set_variant", "mq_debug_set_fault", "mq_debug_plan_mv",
+           "mq_debug_plan_step"]
 
 
 class MQError(RuntimeError):
@@ -281,6 +289,45 @@ def mq_debug_set_variant(policy: int) -> int:
 
 def mq_debug_set_fault(fault: int) -> int:
     return _lib.mq_debug_set_fault(fault)
+
+
+# the planner's fields, in the order mq.h gives them
+PLAN_FIELDS = ("variant", "grid", "block", "smem", "C", "L", "S", "nseg", "nwc", "rg", "T", "ns", "stage_bytes",
+               "rows_per_cta", "cmap", "cgw", "cgu", "hu", "ksplit", "kpn")
+STEP_PLAN_FIELDS = ("grid", "block", "smem", "nwc", "ns", "stage_bytes", "pf_tiles", "ws_bytes")
+PHASES = ("qkv", "o", "gu", "down")
+
+
+def mq_debug_plan_mv(kind: int, rows: int, K: int, ncols: int, I: int, num_sms: int, l2_bytes: int,
+                     max_smem: int, out, n_out: int) -> int:
+    return _lib.mq_debug_plan_mv(kind, rows, K, ncols, I, num_sms, l2_bytes, max_smem, out, n_out)
+
+
+def mq_debug_plan_step(shape: StepShape, num_sms: int, l2_bytes: int, max_smem: int, out, n_out: int) -> int:
+    return _lib.mq_debug_plan_step(ctypes.byref(shape), num_sms, l2_bytes, max_smem, out, n_out)
+
+
+def debug_plan_mv(kind: int, rows: int, K: int, ncols: int, I: int = 0, *, num_sms: int, l2_bytes: int,
+                  max_smem: int) -> dict:
+    """The plan a q4_K projection call takes on the stated device (host only), as a dict."""
+    out = (c_i64 * MQ_PLAN_FIELDS)()
+    _check(mq_debug_plan_mv(kind, rows, K, ncols, I, num_sms, l2_bytes, max_smem, out, MQ_PLAN_FIELDS),
+           "mq_debug_plan_mv")
+    return dict(zip(PLAN_FIELDS, list(out)))
+
+
+def debug_plan_step(shape: StepShape, *, num_sms: int, l2_bytes: int, max_smem: int) -> dict:
+    """The persistent step's plan on the stated device (host only): the kernel's fields and one
+    dict per phase under "qkv", "o", "gu", "down"."""
+    n = MQ_STEP_PLAN_FIELDS + 4 * MQ_PLAN_FIELDS
+    out = (c_i64 * n)()
+    _check(mq_debug_plan_step(shape, num_sms, l2_bytes, max_smem, out, n), "mq_debug_plan_step")
+    v = list(out)
+    d = dict(zip(STEP_PLAN_FIELDS, v[:MQ_STEP_PLAN_FIELDS]))
+    for i, ph in enumerate(PHASES):
+        o = MQ_STEP_PLAN_FIELDS + i * MQ_PLAN_FIELDS
+        d[ph] = dict(zip(PLAN_FIELDS, v[o:o + MQ_PLAN_FIELDS]))
+    return d
 
 
 def _check(st: int, where: str):
