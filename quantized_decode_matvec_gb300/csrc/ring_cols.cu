@@ -1,8 +1,10 @@
 // ring_cols.cu -- the q4_K ring kernels for 3..8 activation columns, all with
-// 16 warps: column groups (kMode 3, two columns per warp group with their
-// activation in registers; see ring_consume_groups), column lanes (kMode 1,
-// every column's activation in registers; see ring_consume_cols) or unit lanes
-// (kMode 2), in a translation unit of their own.
+// 16 warps: half-unit lanes (kMode 4, 4 or 8 columns, four columns per warp
+// group with their activation in registers; see ring_consume_half), column
+// groups (kMode 3, two columns per warp group; see ring_consume_groups),
+// column lanes (kMode 1, every column's activation in registers; see
+// ring_consume_cols) or unit lanes (kMode 2), in a translation unit of their
+// own.
 #include "mq_ring_kernel.cuh"
 
 namespace mq {
