@@ -172,18 +172,37 @@ def test_7b_down_matrix_full(cuda_ready, variant):
     _check_y(y.cpu().numpy(), W, oracle.quantize_q8_0(x), 3584, 18944)
 
 
-@pytest.mark.parametrize("ncols", [8, 6])
-def test_matvec_k_split_matches_oracle_and_exports_xq(cuda_ready, ncols):
-    """Eight (or six) staged columns of K = 18944 leave no room for a ring in one
-    launch, so the matvec runs as a K split: one launch per half of every row,
-    the second adding its sums to y.  The result stays within tolerance of the
-    oracle, the fp32 and q8_0 inputs give the same bits, and the q8_0 export of
-    the activation is the whole activation, bit for bit."""
+def _device_plan(mq, rows, K, ncols):
+    """The launch plan of this matvec on the current device, from the host planner."""
+    import torch
+    pr = torch.cuda.get_device_properties(torch.cuda.current_device())
+    smem = getattr(pr, "shared_memory_per_block_optin", 0)
+    l2 = getattr(pr, "L2_cache_size", 0)
+    if not smem or not l2:
+        pytest.skip("device properties for the planner not exposed by this torch")
+    return mq.debug_plan_mv(mq.MQ_PLAN_MATVEC, rows, K, ncols, 0, num_sms=pr.multi_processor_count,
+                            l2_bytes=l2, max_smem=smem)
+
+
+# (rows, K, ncols) whose staged activation does not fit beside a ring of their
+# rows: 8 and 4 columns on half-unit lanes (two parts), 6 columns on column
+# groups (three parts), 3 columns on column groups (two parts)
+K_SPLIT_CASES = [(200, 18944, 8), (200, 32256, 4), (200, 23808, 6), (200, 38912, 3)]
+
+
+@pytest.mark.parametrize("rows,K,ncols", K_SPLIT_CASES)
+def test_matvec_k_split_matches_oracle_and_exports_xq(cuda_ready, rows, K, ncols):
+    """Columns x K too large to stage beside a ring of the CTA's rows: the matvec
+    runs as a K split, one launch per part of every row, the later parts adding
+    their sums to y.  The result stays within tolerance of the oracle, the fp32
+    and q8_0 inputs give the same bits, and the q8_0 export of the activation
+    (each part writes its range) is the whole activation, bit for bit."""
     import torch
     mq = cuda_ready
-    rows, K = 67, 18944
-    W = synth.q4K_matrix(rows, K, seed=91, tag=synth.TAG_W)
-    x = synth.activation(K, ncols, seed=92, tag=synth.TAG_X)
+    plan = _device_plan(mq, rows, K, ncols)
+    assert plan["variant"] == 1 and plan["ksplit"] > 1, plan
+    W = synth.q4K_matrix(rows, K, seed=91 + ncols, tag=synth.TAG_W)
+    x = synth.activation(K, ncols, seed=92 + ncols, tag=synth.TAG_X)
     xq_np = oracle.quantize_q8_0(x)
     Wd = _to_dev(W)
     xq_out = torch.zeros((ncols, K // 32 * 34), dtype=torch.uint8, device="cuda")
@@ -205,6 +224,8 @@ def test_matvec_k_split_long_rows(cuda_ready, K, ncols):
     import torch
     mq = cuda_ready
     rows = 37
+    plan = _device_plan(mq, rows, K, ncols)
+    assert plan["variant"] == 1 and plan["ksplit"] > 1, plan
     W = synth.q4K_matrix(rows, K, seed=K + ncols, tag=synth.TAG_W)
     x = synth.activation(K, ncols, seed=K + 1, tag=synth.TAG_X)
     xq_np = oracle.quantize_q8_0(x)
